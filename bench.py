@@ -1,0 +1,459 @@
+"""Benchmark: one decode step of the ReplaySSM checkpointing SSU on GB300.
+
+A step = rssm_flush (classify + fold) -> rssm_step (precompute + readout) ->
+rssm_accept over one batch of synthetic decode inputs.  Default workload:
+Mamba-2-style decode, batch 64 of 256 slots, 128 heads, 8 groups, bf16
+checkpoints, window 16, T = 4 drafts.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+                    [--config NAME] [--force-flush] [--no-e2e] [--no-cpu-baseline]
+
+Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
+on the launching stream; a 1 GiB buffer is written between steps (outside the
+events) so every step starts with a cold L2.  Under torchrun (N > 1) every
+rank runs an independent replica (weak scaling, no data-path collective);
+the time is the max over ranks.  Prints one JSON line on rank 0.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from speculative_state_replay_gb300 import workloads as W  # noqa: E402
+
+METRIC = "slot-head SSU updates/s and achieved HBM GB/s vs GB300 roofline (1 GPU)"
+UNIT = "slot-head updates/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=32)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default="mamba2_decode")
+    ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
+    ap.add_argument("--force-flush", action="store_true", help="flush every active row every step")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU budget of the oracle baseline sample")
+    return ap.parse_args()
+
+
+def workload(args):
+    kw = {}
+    if args.batch is not None:
+        kw["batch"] = args.batch
+    return W.config(args.config, **kw)
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            d = json.load(open(p))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# --------------------------------------------------------------------------- #
+# distributed plumbing (timing only)
+# --------------------------------------------------------------------------- #
+def dist_setup():
+    import torch
+
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if ws > 1:
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, ws, local
+
+
+def max_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, ws: int, device=None) -> float:
+    if ws <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# --------------------------------------------------------------------------- #
+# clocks
+# --------------------------------------------------------------------------- #
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
+                                         stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- #
+# GPU arm
+# --------------------------------------------------------------------------- #
+def algorithmic_bytes(wl, rows_rec, ntok_b, esz):
+    """Algorithmic HBM bytes of one readout launch from its per-row records:
+    S0 (+ scales) once per (row, head), live x ring rows, new x, C per group,
+    y and the appended x; inactive rows only write zero outputs."""
+    total = 0
+    hpg = wl.hpg
+    for (s, r, p, Tb, tok0, flags) in rows_rec:
+        if flags and Tb > 0:
+            per_head = (64 * 128 * esz + (256 if esz == 1 else 0) + p * 128 + Tb * 128 + Tb * 256 / hpg
+                        + Tb * 128 + Tb * 128)
+            total += per_head * wl.nheads
+        elif Tb > 0:
+            total += Tb * 128 * wl.nheads
+    return total
+
+
+def flush_bytes(wl, recs, esz):
+    """Algorithmic bytes of one fold launch: S0 read + write (+ scales), live x
+    and B rows per flagged (row, head)."""
+    total = 0
+    for p in recs:
+        total += wl.nheads * (2 * 64 * 128 * esz + (512 if esz == 1 else 0) + p * 128 + p * 256 / wl.hpg + p * 4)
+    return total
+
+
+def run_gpu(args, rank, ws, local):
+    import torch
+
+    from speculative_state_replay_gb300 import api, build
+
+    build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wl = workload(args)
+    gen = W.Generator(wl)
+    A, D, dt_bias = gen.params()
+    ids = gen.slot_idx()
+    esz = W.DTYPE_BYTES[wl.state_dtype]
+
+    gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
+                       wl.rounding, device=dev, slot_pad_bytes=wl.slot_pad_bytes)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    active = ids[ids > 0]
+    chunk = 16
+    for i in range(0, active.size, chunk):
+        sl = active[i:i + chunk]
+        api.rssm_init_state(gc, t(gen.init_states(i, sl.size)), t(sl.astype(np.int32)), seed=wl.sr_seed)
+    pnat0 = np.zeros(ids.size, np.int32)
+    if wl.prefill_live:
+        for b, s in enumerate(ids):
+            if s > 0:
+                x, B, dtp, live = gen.ring_prefill(int(s))
+                gc.x_view()[s] = t(x.view(np.int16))
+                gc.B_view()[s] = t(B.view(np.int16))
+                gc.dt_view()[s] = t(dtp)
+                pnat0[b] = live
+    gc.ring_start.copy_(t(gen.ring_start()))
+    torch.cuda.synchronize()
+
+    gA, gD, gb, gids = t(A), t(D), t(dt_bias), t(ids)
+    pnat = t(pnat0)
+    nsteps = args.warmup + args.steps
+    host = [gen.step(k) for k in range(nsteps)]
+    dev_inp = []
+    for inp in host:
+        dev_inp.append(dict(x=t(inp.x.view(np.int16)), dt=t(inp.dt), B=t(inp.B.view(np.int16)),
+                            C=t(inp.C.view(np.int16)), acc=t(inp.accepted),
+                            cu=None if inp.cu_seqlens is None else t(inp.cu_seqlens), ntok=inp.ntok))
+    max_tok = max(i.ntok for i in host)
+    out = torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16, device=dev)
+    scr_flush = api.alloc_scratch(gc, ids.size, wl.T)
+    scr_step = api.alloc_scratch(gc, ids.size, wl.T)
+    l2 = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    force = 1 if args.force_flush else 0
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    def one_step(di):
+        api.rssm_flush(gc, gA, gids, pnat, wl.T, scr_flush, cu_seqlens=di["cu"], force=force, seed=wl.sr_seed)
+        e_f = ev()
+        e_f.record(stream)
+        api.rssm_step_precompute(gc, di["x"], di["dt"], gA, di["B"], di["C"], gD, gb, gids, pnat, wl.T, out,
+                                 scr_step, cu_seqlens=di["cu"])
+        e_r0 = ev()
+        e_r0.record(stream)
+        api.rssm_step_readout(gc, di["x"], di["dt"], gA, di["B"], di["C"], gD, gb, gids, pnat, wl.T, out, scr_step,
+                              cu_seqlens=di["cu"])
+        e_r1 = ev()
+        e_r1.record(stream)
+        api.rssm_accept(gc, gids, pnat, di["acc"], wl.T, cu_seqlens=di["cu"])
+        return e_f, e_r0, e_r1
+
+    for k in range(args.warmup):
+        l2.zero_()
+        one_step(dev_inp[k])
+    torch.cuda.synchronize()
+
+    step_ms, read_ms, flush_ms, read_bytes, fold_bytes, units = [], [], [], 0.0, 0.0, 0
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    for k in range(args.warmup, nsteps):
+        l2.zero_()
+        e0 = ev()
+        e0.record(stream)
+        e_f, e_r0, e_r1 = one_step(dev_inp[k])
+        e1 = ev()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        flush_ms.append(e0.elapsed_time(e_f))
+        read_ms.append(e_r0.elapsed_time(e_r1))
+        # per-row records the readout used, and the flagged rows of the flush
+        rr = scr_step[: ids.size * 32].view(torch.int32).view(ids.size, 8).cpu().numpy()
+        read_bytes += algorithmic_bytes(wl, [tuple(r[:6]) for r in rr], None, esz)
+        units += int(((rr[:, 5] == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
+        cnt = int(scr_flush[:4].view(torch.int32).item())
+        recs = scr_flush[256: 256 + cnt * 32].view(torch.int32).view(cnt, 8).cpu().numpy() if cnt else np.zeros((0, 8))
+        fold_bytes += flush_bytes(wl, [int(r[3]) for r in recs], esz)
+    clk = clocks.stop() if clocks else None
+    barrier(ws)
+    torch.cuda.synchronize()
+    err = int(gc.error_word.item())
+    if err:
+        raise RuntimeError(f"device error bits set: {err:#x}")
+
+    total_ms = sum(step_ms)
+    t_max = max_over_ranks(total_ms, ws, dev)
+    units_all = sum_over_ranks(units, ws, dev)
+    value = units_all / (t_max / 1e3)
+
+    # end to end through the public calls, host buffers, copies inside the timing
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+        hin = [dict(x=pin(i.x.view(np.int16)), dt=pin(i.dt), B=pin(i.B.view(np.int16)), C=pin(i.C.view(np.int16)),
+                    acc=pin(i.accepted), cu=None if i.cu_seqlens is None else pin(i.cu_seqlens), ntok=i.ntok)
+               for i in host[args.warmup:]]
+        dbuf = dict(x=torch.empty_like(dev_inp[0]["x"]), dt=torch.empty_like(dev_inp[0]["dt"]),
+                    B=torch.empty_like(dev_inp[0]["B"]), C=torch.empty_like(dev_inp[0]["C"]),
+                    acc=torch.empty_like(dev_inp[0]["acc"]))
+        yh = torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16).pin_memory()
+        e2e_ms, h2d, d2h = [], 0, 0
+        for hi in hin:
+            l2.zero_()
+            e0 = ev()
+            e0.record(stream)
+            di = {}
+            for key in ("x", "dt", "B", "C", "acc"):
+                dst = dbuf[key] if dbuf[key].shape == hi[key].shape else torch.empty(hi[key].shape, dtype=hi[key].dtype,
+                                                                                     device=dev)
+                dst.copy_(hi[key], non_blocking=True)
+                di[key] = dst
+            di["cu"] = None
+            if hi["cu"] is not None:
+                di["cu"] = hi["cu"].to(dev, non_blocking=True)
+            di["ntok"] = hi["ntok"]
+            one_step(di)
+            yh[: hi["ntok"]].copy_(out[: hi["ntok"]], non_blocking=True)
+            e1 = ev()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            e2e_ms.append(e0.elapsed_time(e1))
+            h2d = sum(hi[k].numel() * hi[k].element_size() for k in ("x", "dt", "B", "C", "acc")) + (
+                0 if hi["cu"] is None else hi["cu"].numel() * 4)
+            d2h = hi["ntok"] * wl.nheads * 64 * 2
+        t_e2e = max_over_ranks(sum(e2e_ms), ws, dev)
+        e2e = {"value": units_all / (t_e2e / 1e3), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    peak, peak_kind = measured_peaks()
+    achieved = read_bytes / (sum(read_ms) / 1e3) / 1e9
+    fold_achieved = fold_bytes / (sum(flush_ms) / 1e3) / 1e9 if sum(flush_ms) > 0 else 0.0
+    res = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB buffer written between steps",
+                       force_flush=bool(args.force_flush)),
+        "roofline": {"bound": "hbm", "kernel": "readout_kernel", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
+                     "avg_launch_us": 1e3 * statistics.mean(read_ms),
+                     "algorithmic_bytes_per_launch": read_bytes / args.steps},
+        "flush_roofline": {"bound": "hbm", "kernel": "flag_kernel+fold_kernel", "achieved": fold_achieved,
+                           "peak": peak, "unit": "GB/s", "frac": fold_achieved / peak,
+                           "avg_us": 1e3 * statistics.mean(flush_ms),
+                           "algorithmic_bytes_per_step": fold_bytes / args.steps},
+        "e2e": e2e,
+        "gpu_launches": 5 * args.steps,
+        "clocks": clk,
+        "device_time_ms": {"step": statistics.mean(step_ms), "readout": statistics.mean(read_ms),
+                           "flush": statistics.mean(flush_ms)},
+    }
+    return res, wl
+
+
+# --------------------------------------------------------------------------- #
+# CPU oracle (baseline leg and reference arm)
+# --------------------------------------------------------------------------- #
+def oracle_sample(wl, seconds: float, max_steps: int, rows: int | None = None):
+    """Time the oracle as it stands on the workload: flush + step + accept per
+    step over `rows` rows, until `seconds` of wall time or max_steps."""
+    import oracle
+
+    oracle.build()
+    gen = W.Generator(wl)
+    A, D, dtb = gen.params()
+    ids = gen.slot_idx()
+    if rows is not None and rows < ids.size:
+        ids = ids[:rows]
+    oc = oracle.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
+                            wl.rounding, slot_pad_bytes=wl.slot_pad_bytes)
+    act = ids[ids > 0]
+    oc.init_state(gen.init_states(0, act.size), act, seed=wl.sr_seed)
+    pnat = np.zeros(ids.size, np.int32)
+    units, t_all, steps = 0, 0.0, 0
+    T = wl.T
+    for k in range(max_steps):
+        inp = gen.step(k)
+        # restrict the step inputs to the sampled rows
+        if inp.cu_seqlens is None:
+            tok = np.arange(ids.size * T)
+            cu = None
+        else:
+            cu = inp.cu_seqlens[: ids.size + 1].copy()
+            tok = np.arange(int(cu[-1]))
+        t0 = time.perf_counter()
+        oc.flush(A, ids, pnat, T, cu_seqlens=cu, seed=wl.sr_seed)
+        oc.step(inp.x[tok], inp.dt[tok], A, inp.B[tok], inp.C[tok], D, dtb, ids, pnat, T, cu_seqlens=cu)
+        oc.accept(ids, pnat, inp.accepted[: ids.size], T, cu_seqlens=cu)
+        t_all += time.perf_counter() - t0
+        units += int((ids > 0).sum()) * wl.nheads
+        steps += 1
+        if t_all >= seconds:
+            break
+    thr = oracle.openmp_threads() or 1
+    return units / t_all, thr, steps, ids.size, t_all
+
+
+def cpu_baseline(wl, seconds):
+    v, thr, steps, rows, secs = oracle_sample(wl, seconds, max_steps=64)
+    return {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
+            "sample": f"{steps} steps x {rows} rows x {wl.nheads} heads of {wl.name} "
+                      f"(flush+step+accept, {secs:.1f} s wall, OpenMP over (row, head))"}
+
+
+def run_reference(args, rank, ws):
+    if rank != 0:
+        return None
+    wl = workload(args)
+    per_step = max(0.5, 60.0 / max(1, args.steps + args.warmup))
+    vals = []
+    for k in range(args.warmup + args.steps):
+        v, thr, steps, rows, secs = oracle_sample(wl, per_step, max_steps=1, rows=min(16, wl.batch))
+        if k >= args.warmup:
+            vals.append((v, secs, steps, rows))
+    value = statistics.mean(v for v, *_ in vals)
+    sample = f"each step: 1 decode step of {vals[0][3]} rows x {wl.nheads} heads of {wl.name} on the CPU oracle"
+    cb = {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample}
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(s for _, s, *_ in vals),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(wl.describe(), parallelism=f"replicas{ws}"), "cpu_baseline": cb,
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, ws, local = dist_setup()
+    if args.impl == "reference":
+        res = run_reference(args, rank, ws)
+        if rank == 0:
+            print(json.dumps(res))
+        return
+    res, wl = run_gpu(args, rank, ws, local)
+    if rank == 0:
+        if not args.no_cpu_baseline and ws == 1:
+            res["cpu_baseline"] = cpu_baseline(wl, args.cpu_seconds)
+        else:
+            res["cpu_baseline"] = None
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,226 @@
+/*
+ * rssm.h -- C ABI of librssm, a GB300 (sm_103a) implementation of the
+ * ReplaySSM checkpointing selective-state-update for Mamba-2 decode with
+ * speculative draft tokens.
+ *
+ * The op.  Each (slot, head) keeps a checkpoint state S0[dim=64][dstate=128]
+ * and head-major ring buffers of the recent inputs (x, B and dt').  A decode
+ * step with T draft tokens replays the live ring plus the drafts against S0
+ * to produce the outputs, and appends the drafts to the rings; when the live
+ * window fills, a flush folds the accepted prefix into a new checkpoint.
+ * Sources, cited throughout by page and section:
+ *   [FI]   FlashInfer PR #3975 "mamba checkpointing SSU: two-kernel split +
+ *          ring-buffer cache for checkpointing SSU" (Description items 1-2,
+ *          commit notes).
+ *   [vS]   vLLM PR #65660 "WIP: [Mamba] Add separate CuTeDSL ReplaySSM
+ *          checkpoints" (Overview, Claims, Details, commit notes).
+ *   [vAPI] vLLM API docs for vllm.model_executor.layers.mamba.ops.
+ *          replayssm_cutedsl (initialize_replayssm_state,
+ *          selective_state_update_replayssm).
+ *
+ * Conventions shared by every entry point.
+ *  - Memory: every pointer is caller-owned device memory unless stated
+ *    otherwise; the library never allocates, frees or keeps a pointer after a
+ *    call returns.  Temporary storage is a caller-provided `scratch` buffer
+ *    of at least rssm_scratch_bytes() bytes ([FI] Description item 1:
+ *    caller-provided scratch, allocated like the output, graph safe).
+ *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default
+ *    stream).  Every call only enqueues kernels on it: no host
+ *    synchronisation and no host read of device data, so calls can be
+ *    captured in a CUDA graph ([vAPI] selective_state_update_replayssm: the
+ *    call is prepared for graph capture).  Calls on one cache must be ordered
+ *    on one stream (or by the caller).
+ *  - Alignment: all pointers and slot strides must give 16-byte aligned rows
+ *    (the kernels move rows with bulk copies); violations return
+ *    RSSM_ERR_INVALID_ARGUMENT before anything is launched.
+ *  - Slots: slot 0 is a padding slot; rows whose slot id is <= 0 or >= the
+ *    number of slots are ignored: their outputs are written as zeros and no
+ *    cache byte is touched ([vAPI] module docstring and
+ *    initialize_replayssm_state).  Active slot ids in one call must be
+ *    unique ([vAPI] selective_state_update_replayssm docstring);
+ *    duplicates are undefined behaviour.
+ *  - Errors: host-detectable problems return a status before any launch.
+ *    Data-dependent problems found on the device (bad pnat, bad cu_seqlens,
+ *    bad accepted counts) set bits in cache->error_word (sticky, never
+ *    cleared by the library) and the affected row is skipped (outputs 0).
+ *    A kernel that gives up waiting on its own pipeline sets
+ *    RSSM_ERRBIT_TIMEOUT and returns.
+ *
+ * Call order of one decode step (the library owns the ring bookkeeping on
+ * the device):
+ *     rssm_flush   -- rows whose live window would overflow fold their live
+ *                     prefix into S0, advance ring_start, reset pnat
+ *     rssm_step    -- outputs for the drafts; appends them to the rings
+ *     rssm_accept  -- pnat += accepted drafts (after verification)
+ */
+#ifndef RSSM_H
+#define RSSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RSSM_OK = 0,
+  RSSM_ERR_INVALID_ARGUMENT = 1, /* null pointer, bad size/stride/alignment, bad enum */
+  RSSM_ERR_UNSUPPORTED = 2,      /* shape outside what the kernels are built for */
+  RSSM_ERR_SCRATCH_TOO_SMALL = 3,
+  RSSM_ERR_CUDA = 4              /* a CUDA runtime call or launch failed */
+} rssm_status;
+
+/* Checkpoint state formats.  8-bit formats carry one FP32 scale per
+ * (slot, head, d) row of 128 dstate values ([vS] commit notes: quantised
+ * checkpoints with FP32 row scales). */
+typedef enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2, RSSM_I8 = 3, RSSM_E4M3 = 4 } rssm_dtype;
+
+/* How a flush or init rounds fp32 values to the state format: nearest
+ * (ties to even, saturating) or stochastic with a Philox4x32-7 hash keyed by
+ * the seed and countered by (element/4, head, slot, flush epoch).  Both are
+ * deterministic functions of the inputs ([vS] Claims; [FI] commit notes on
+ * Philox stochastic rounding). */
+typedef enum { RSSM_ROUND_NEAREST = 0, RSSM_ROUND_STOCHASTIC = 1 } rssm_rounding;
+
+/* bits of *error_word */
+#define RSSM_ERRBIT_PNAT 1u    /* pnat < 0, or pnat + tokens > L (step), or pnat > L (flush) */
+#define RSSM_ERRBIT_SEQLEN 2u  /* a row's token count (cu_seqlens) < 0 or > T */
+#define RSSM_ERRBIT_ACCEPT 4u  /* accepted < 0 or > the row's token count */
+#define RSSM_ERRBIT_TIMEOUT 8u /* a kernel gave up waiting on its own copy pipeline */
+
+/*
+ * The cache of all slots.  Layouts follow the ring-buffer cache contract of
+ * [FI] Description item 2 (head-major, single-buffered rings) with
+ * L = max_window + npredicted.  Strides are in ELEMENTS between consecutive
+ * slots and may exceed the dense size ([vAPI] module docstring: cache pages
+ * may carry padding between slots).
+ */
+typedef struct {
+  int32_t num_slots;   /* S, including padding slot 0 */
+  int32_t nheads;      /* H */
+  int32_t ngroups;     /* G; head h uses group h / (H / G) */
+  int32_t dim;         /* must be 64 */
+  int32_t dstate;      /* must be 128 */
+  int32_t max_window;  /* W: a row flushes before a step when pnat + tokens > W */
+  int32_t npredicted;  /* max draft tokens per step; L = W + npredicted <= 32 */
+  int32_t state_dtype; /* rssm_dtype */
+  int32_t rounding;    /* rssm_rounding, used by rssm_flush and rssm_init_state */
+  void *state;         int64_t state_slot_stride; /* [slot][H][64][128] of state_dtype */
+  float *scale;        int64_t scale_slot_stride; /* [slot][H][64] f32; 8-bit only (else may be NULL) */
+  void *x_cache;       int64_t x_slot_stride;     /* bf16 [slot][H][L][64] */
+  void *B_cache;       int64_t B_slot_stride;     /* bf16 [slot][G][L][128] */
+  float *dt_cache;     int64_t dt_slot_stride;    /* f32 [slot][H][L], post-softplus dt' */
+  int32_t *ring_start; /* [slot]: physical position of live token 0 */
+  uint32_t *flush_epoch; /* [slot]: number of flushes since init (random counter) */
+  uint32_t *error_word;  /* [1]: sticky RSSM_ERRBIT_* bits */
+} rssm_cache;
+
+/*
+ * Bytes of scratch rssm_flush / rssm_step need for `batch` rows of up to T
+ * tokens.  The same buffer may serve both calls (they are stream ordered).
+ * Returns 0 if the cache description is invalid.
+ */
+size_t rssm_scratch_bytes(const rssm_cache *cache, int32_t batch, int32_t T);
+
+/*
+ * Initialise checkpoints from FP32 prefill states ([vAPI]
+ * initialize_replayssm_state): for i < n, states[i] ([H][64][128] f32,
+ * contiguous, device) is rounded to the state format (flush epoch 0) into
+ * slot slot_idx[i]; that slot's x/B/dt rings are zeroed and its ring_start
+ * and flush_epoch set to 0.  Ids <= 0 or >= num_slots are ignored.  The
+ * caller sets the rows' pnat to 0.  `seed` keys stochastic rounding.
+ */
+rssm_status rssm_init_state(const rssm_cache *cache, const float *states, const int32_t *slot_idx, int32_t n,
+                            uint64_t seed, void *stream);
+
+/*
+ * Flush ([FI] commit notes: the write decision is taken per slot at run time
+ * as prev_k + T > max_window; [vS] Details: only the accepted prefix enters
+ * the checkpoint).  For every active row b (slot s = slot_idx[b], p =
+ * pnat[b] live tokens, T_b tokens this step):
+ *   flagged  = force ? 1 : (p + T_b > max_window)
+ * and for flagged rows, per head h, with c_j = sum_{i<=j} A[h] dt'_i over the
+ * live tokens (fp32, ascending), c_end = c_{p-1} (0 if p = 0):
+ *   S0' = e^{c_end} S0 + sum_{j<p} e^{c_end - c_j} dt'_j x_j (outer) B_j
+ * computed in fp32 in one canonical order (acc = e^{c_end} S0; then for j
+ * ascending acc = fma(e^{c_end-c_j} dt'_j x_j[d], B_j[n], acc)), rounded to
+ * the state format with flush epoch flush_epoch[s] + 1; then ring_start[s] =
+ * (ring_start[s] + p) mod L, pnat[b] = 0, flush_epoch[s] += 1.
+ *   A        [H] f32 (device)
+ *   slot_idx [batch] i32 (device)
+ *   pnat     [batch] i32 (device, in/out): live accepted tokens per row
+ *   cu_seqlens [batch+1] i32 (device) or NULL: row b has cu[b+1]-cu[b]
+ *            tokens (<= T); NULL: every row has T tokens
+ *   force    0: flush iff pnat + T_b > max_window; 1: every active row
+ */
+rssm_status rssm_flush(const rssm_cache *cache, const float *A, const int32_t *slot_idx, int32_t *pnat,
+                       const int32_t *cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
+                       void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * Step: replay/readout and ring append ([FI] Description items 1-2).  For
+ * active row b (slot s, p = pnat[b] live tokens, T_b new tokens, token
+ * offset tok0 = cu_seqlens[b] or b*T) and head h (group g = h/(H/G)), with
+ * the live ring followed by the new tokens as logical tokens k = 0..p+T_b-1:
+ *   dt'_k = softplus(dt[tok][h] + dt_bias[h]) for new tokens, dt_cache for live
+ *   c_k   = sum_{i<=k} A[h] dt'_i
+ *   y_t   = e^{c_{p+t}} (S0 . C_t) + sum_{k<=p+t} e^{c_{p+t}-c_k} dt'_k (C_t . B_k) x_k
+ *           + D[h] x_t,                         rounded to bf16
+ * then x_t, B_t (once per group) and dt'_t are appended at physical position
+ * (ring_start[s] + p + t) mod L.  S0 is never written ([vS] Details).
+ *   x   bf16 [tok][H][64]     dt f32 [tok][H]       A, D, dt_bias f32 [H]
+ *   B,C bf16 [tok][G][128]    out bf16 [tok][H][64] (written)
+ *   slot_idx, pnat [batch] i32 (read only); cu_seqlens as in rssm_flush.
+ *   T   tokens per row (max tokens per row with cu_seqlens), 1..min(8, npredicted).
+ * Requires p + T_b <= L on the device (guaranteed after rssm_flush).
+ */
+rssm_status rssm_step(const rssm_cache *cache, const void *x, const float *dt, const float *A, const void *B,
+                      const void *C, const float *D, const float *dt_bias, const int32_t *slot_idx,
+                      const int32_t *pnat, const int32_t *cu_seqlens, int32_t batch, int32_t T, void *out,
+                      void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * The two halves of rssm_step, exposed for profiling and for callers that
+ * want to place other work between them.  rssm_step == rssm_step_precompute
+ * followed by rssm_step_readout with the same arguments and scratch.
+ *   precompute: per (row, group): dt', cumulative A dt', C.B contraction and
+ *               the decayed replay coefficients into scratch; appends B, dt'.
+ *   readout:    per (row, head): streams S0 once, forms y, appends x.
+ */
+rssm_status rssm_step_precompute(const rssm_cache *cache, const void *x, const float *dt, const float *A,
+                                 const void *B, const void *C, const float *D, const float *dt_bias,
+                                 const int32_t *slot_idx, const int32_t *pnat, const int32_t *cu_seqlens,
+                                 int32_t batch, int32_t T, void *out, void *scratch, size_t scratch_bytes,
+                                 void *stream);
+rssm_status rssm_step_readout(const rssm_cache *cache, const void *x, const float *dt, const float *A,
+                              const void *B, const void *C, const float *D, const float *dt_bias,
+                              const int32_t *slot_idx, const int32_t *pnat, const int32_t *cu_seqlens,
+                              int32_t batch, int32_t T, void *out, void *scratch, size_t scratch_bytes,
+                              void *stream);
+
+/*
+ * Commit verified drafts: pnat[b] += accepted[b] for active rows, so the
+ * first accepted[b] tokens appended by the last rssm_step join the live
+ * prefix; the rest stay outside it and are overwritten by later appends
+ * ([vS] Details: rejected drafts never reach the checkpoint).  accepted
+ * [batch] i32 (device), 0 <= accepted[b] <= T_b, else RSSM_ERRBIT_ACCEPT.
+ */
+rssm_status rssm_accept(const rssm_cache *cache, const int32_t *slot_idx, int32_t *pnat, const int32_t *accepted,
+                        const int32_t *cu_seqlens, int32_t batch, int32_t T, void *stream);
+
+/*
+ * Diagnostics: the device versions of the fixed-sequence fp32 exp and
+ * softplus the flush and the dt' ring use (Cody-Waite reduction with a
+ * degree-7 Taylor polynomial; softplus(v) = log1p(exp(v)) via an atanh
+ * series, v itself above 20).  in/out_exp/out_softplus are [n] f32 device.
+ */
+rssm_status rssm_eval_spec_math(const float *in, float *out_exp, float *out_softplus, int64_t n, void *stream);
+
+const char *rssm_status_string(rssm_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSSM_H */

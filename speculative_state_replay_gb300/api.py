@@ -1,0 +1,165 @@
+"""Python binding of librssm: the C ABI entry points with torch tensors.
+
+Every function marshals tensor pointers, sizes and the current CUDA stream
+into the C call of the same name and raises on a non-OK status.  All work
+runs in the library's CUDA kernels; nothing here computes any part of the op.
+Layouts and semantics are those of include/rssm.h.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+
+F32, BF16, F16, I8, E4M3 = 0, 1, 2, 3, 4
+NEAREST, STOCHASTIC = 0, 1
+ERRBIT_PNAT, ERRBIT_SEQLEN, ERRBIT_ACCEPT, ERRBIT_TIMEOUT = 1, 2, 4, 8
+DIM, DSTATE = 64, 128
+STATE_TORCH = {F32: torch.float32, BF16: torch.int16, F16: torch.int16, I8: torch.int8, E4M3: torch.uint8}
+
+
+class RssmError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        msg = _lib.load().rssm_status_string(status).decode()
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise RssmError(fn, status)
+
+
+class RssmCache:
+    """Cache of all slots on one device: checkpoints, rings, bookkeeping.
+
+    Every tensor is 2-D [slot, slot_stride]; `slot_pad_bytes` adds padding
+    after each slot's page.  bf16/f16 data is held as raw 16-bit words.
+    """
+
+    def __init__(self, num_slots, nheads, ngroups, max_window, npredicted, state_dtype, rounding=NEAREST,
+                 device="cuda", slot_pad_bytes=0):
+        self.S, self.H, self.G = num_slots, nheads, ngroups
+        self.W, self.Tmax = max_window, npredicted
+        self.L = max_window + npredicted
+        self.state_dtype, self.rounding = state_dtype, rounding
+        dev = torch.device(device)
+        sd = STATE_TORCH[state_dtype]
+        esz = torch.empty(0, dtype=sd).element_size()
+
+        def stride(n, itemsize):
+            return n + slot_pad_bytes // itemsize
+
+        z = lambda shape, dt: torch.zeros(shape, dtype=dt, device=dev)  # noqa: E731
+        self.state = z((num_slots, stride(nheads * DIM * DSTATE, esz)), sd)
+        self.scale = torch.ones((num_slots, stride(nheads * DIM, 4)), dtype=torch.float32, device=dev)
+        self.x_cache = z((num_slots, stride(nheads * self.L * DIM, 2)), torch.int16)
+        self.B_cache = z((num_slots, stride(ngroups * self.L * DSTATE, 2)), torch.int16)
+        self.dt_cache = z((num_slots, stride(nheads * self.L, 4)), torch.float32)
+        self.ring_start = z((num_slots,), torch.int32)
+        self.flush_epoch = z((num_slots,), torch.int32)
+        self.error_word = z((1,), torch.int32)
+        self._struct = None
+
+    def struct(self):
+        if self._struct is None:
+            c = _lib.RssmCacheStruct()
+            c.num_slots, c.nheads, c.ngroups = self.S, self.H, self.G
+            c.dim, c.dstate = DIM, DSTATE
+            c.max_window, c.npredicted = self.W, self.Tmax
+            c.state_dtype, c.rounding = self.state_dtype, self.rounding
+            c.state, c.state_slot_stride = self.state.data_ptr(), self.state.shape[1]
+            c.scale, c.scale_slot_stride = self.scale.data_ptr(), self.scale.shape[1]
+            c.x_cache, c.x_slot_stride = self.x_cache.data_ptr(), self.x_cache.shape[1]
+            c.B_cache, c.B_slot_stride = self.B_cache.data_ptr(), self.B_cache.shape[1]
+            c.dt_cache, c.dt_slot_stride = self.dt_cache.data_ptr(), self.dt_cache.shape[1]
+            c.ring_start = self.ring_start.data_ptr()
+            c.flush_epoch = self.flush_epoch.data_ptr()
+            c.error_word = self.error_word.data_ptr()
+            self._struct = c
+        return ctypes.byref(self._struct)
+
+    # logical views (without the slot padding)
+    def state_view(self):
+        return self.state[:, : self.H * DIM * DSTATE].view(self.S, self.H, DIM, DSTATE)
+
+    def scale_view(self):
+        return self.scale[:, : self.H * DIM].view(self.S, self.H, DIM)
+
+    def x_view(self):
+        return self.x_cache[:, : self.H * self.L * DIM].view(self.S, self.H, self.L, DIM)
+
+    def B_view(self):
+        return self.B_cache[:, : self.G * self.L * DSTATE].view(self.S, self.G, self.L, DSTATE)
+
+    def dt_view(self):
+        return self.dt_cache[:, : self.H * self.L].view(self.S, self.H, self.L)
+
+
+def rssm_scratch_bytes(cache: RssmCache, batch: int, T: int) -> int:
+    return int(_lib.load().rssm_scratch_bytes(cache.struct(), batch, T))
+
+
+def alloc_scratch(cache: RssmCache, batch: int, T: int) -> torch.Tensor:
+    n = rssm_scratch_bytes(cache, batch, T)
+    if n == 0:
+        raise RssmError("rssm_scratch_bytes", 1)
+    return torch.empty(n, dtype=torch.uint8, device=cache.state.device)
+
+
+def rssm_init_state(cache, states, slot_idx, seed=0, stream=None):
+    _check("rssm_init_state", _lib.load().rssm_init_state(cache.struct(), _ptr(states), _ptr(slot_idx),
+                                                          slot_idx.numel(), seed, _stream(stream)))
+
+
+def rssm_flush(cache, A, slot_idx, pnat, T, scratch, cu_seqlens=None, force=0, seed=0, stream=None):
+    _check("rssm_flush", _lib.load().rssm_flush(cache.struct(), _ptr(A), _ptr(slot_idx), _ptr(pnat),
+                                                _ptr(cu_seqlens), slot_idx.numel(), T, force, seed,
+                                                _ptr(scratch), scratch.numel(), _stream(stream)))
+
+
+def _step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, stream):
+    f = getattr(_lib.load(), fn)
+    _check(fn, f(cache.struct(), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                 _ptr(slot_idx), _ptr(pnat), _ptr(cu_seqlens), slot_idx.numel(), T, _ptr(out), _ptr(scratch),
+                 scratch.numel(), _stream(stream)))
+
+
+def rssm_step(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None, stream=None):
+    _step("rssm_step", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, stream)
+
+
+def rssm_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
+                         stream=None):
+    _step("rssm_step_precompute", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens,
+          stream)
+
+
+def rssm_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
+                      stream=None):
+    _step("rssm_step_readout", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens,
+          stream)
+
+
+def rssm_accept(cache, slot_idx, pnat, accepted, T, cu_seqlens=None, stream=None):
+    _check("rssm_accept", _lib.load().rssm_accept(cache.struct(), _ptr(slot_idx), _ptr(pnat), _ptr(accepted),
+                                                  _ptr(cu_seqlens), slot_idx.numel(), T, _stream(stream)))
+
+
+def rssm_eval_spec_math(x, out_exp=None, out_softplus=None, stream=None):
+    _check("rssm_eval_spec_math", _lib.load().rssm_eval_spec_math(_ptr(x), _ptr(out_exp), _ptr(out_softplus),
+                                                                  x.numel(), _stream(stream)))

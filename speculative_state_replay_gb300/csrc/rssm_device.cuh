@@ -1,0 +1,365 @@
+// rssm_device.cuh -- device building blocks of librssm (sm_103a).
+//
+// Pipeline primitives (mbarrier, 1-D bulk copies), the fixed-sequence fp32
+// exp / softplus, the Philox4x32-7 hash and the checkpoint quantiser.  The
+// arithmetic that decides stored bits (dt' in the ring, flushed checkpoints)
+// is written with explicit __fmul_rn/__fadd_rn/__fmaf_rn so the compiler
+// cannot contract or reorder it.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rssm_internal.h"
+
+namespace rssm {
+
+// --------------------------------------------------------------------------
+// bit helpers
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+__device__ __forceinline__ float bf16f(uint16_t b) { return __uint_as_float(static_cast<uint32_t>(b) << 16); }
+__device__ __forceinline__ float2 h2f2(uint32_t w) {
+  __half2 h = *reinterpret_cast<__half2*>(&w);
+  return __half22float2(h);
+}
+
+__device__ __forceinline__ void set_error(unsigned* err, unsigned bit) {
+  if (err) atomicOr(err, bit);
+}
+
+// --------------------------------------------------------------------------
+// mbarrier / bulk-copy primitives (PTX, sm_90+)
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile(
+      "{\n\t.reg .b64 st;\n\t"
+      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a phase of an mbarrier: gives up after roughly a second.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+  for (uint32_t i = 0; i < kWaitSpins; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (i >= 64) __nanosleep(256);
+  }
+  return false;
+}
+// 1-D bulk copy global -> shared, completion counted in bytes on `bar`.
+// Both addresses 16-byte aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, uint32_t bytes, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(smem_dst)),
+      "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+// named barrier over the consumer warps only (the producer warp never joins)
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
+
+// --------------------------------------------------------------------------
+// Fixed-sequence fp32 exp / log1p / softplus.  Methods: Cody-Waite range
+// reduction x = k ln2 + r with ln2 split into two floats, degree-7 Taylor
+// polynomial of e^r in Horner form, scaling by 2^k; log1p(z) = 2 atanh(s)
+// with s = z/(2+z) for small z, else log(w) = e ln2 + 2 atanh((m-1)/(m+1))
+// for w = 1 + z = m 2^e plus the correction (z - (w-1))/w.  Coefficients are
+// 1/k! and 1/(2k+1) rounded once to float.  Every operation is an IEEE
+// round-to-nearest primitive, so the result is a fixed function of x.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ float spec_exp(float x) {
+  if (x != x) return x;
+  if (x < -87.0f) return 0.0f;
+  if (x > 88.0f) return __uint_as_float(0x7f800000u);
+  const float log2e = (float)1.4426950408889634;
+  const float ln2_hi = (float)0.6931471805599453;
+  const float ln2_lo = (float)(0.6931471805599453 - (double)(float)0.6931471805599453);
+  const float kf = rintf(__fmul_rn(x, log2e));
+  float r = __fmaf_rn(-kf, ln2_hi, x);
+  r = __fmaf_rn(-kf, ln2_lo, r);
+  float q = (float)(1.0 / 5040.0);
+  q = __fmaf_rn(q, r, (float)(1.0 / 720.0));
+  q = __fmaf_rn(q, r, (float)(1.0 / 120.0));
+  q = __fmaf_rn(q, r, (float)(1.0 / 24.0));
+  q = __fmaf_rn(q, r, (float)(1.0 / 6.0));
+  q = __fmaf_rn(q, r, 0.5f);
+  q = __fmaf_rn(q, r, 1.0f);
+  q = __fmaf_rn(q, r, 1.0f);
+  const int k = static_cast<int>(kf);
+  return __fmul_rn(q, __uint_as_float(static_cast<uint32_t>(k + 127) << 23));
+}
+
+__device__ __forceinline__ float spec_log1p(float z) {
+  if (z != z || z == __uint_as_float(0x7f800000u)) return z;
+  const float ln2_hi = (float)0.6931471805599453;
+  const float ln2_lo = (float)(0.6931471805599453 - (double)(float)0.6931471805599453);
+  if (z < 0.25f) {
+    const float s = __fdiv_rn(z, __fadd_rn(2.0f, z));
+    const float s2 = __fmul_rn(s, s);
+    float q = (float)(1.0 / 11.0);
+    q = __fmaf_rn(q, s2, (float)(1.0 / 9.0));
+    q = __fmaf_rn(q, s2, (float)(1.0 / 7.0));
+    q = __fmaf_rn(q, s2, (float)(1.0 / 5.0));
+    q = __fmaf_rn(q, s2, (float)(1.0 / 3.0));
+    q = __fmul_rn(q, s2);
+    const float t = __fmaf_rn(s, q, s);
+    return __fadd_rn(t, t);
+  }
+  const float w = __fadd_rn(1.0f, z);
+  const uint32_t wb = __float_as_uint(w);
+  int e = static_cast<int>((wb >> 23) & 0xffu) - 127;
+  float m = __uint_as_float((wb & 0x7fffffu) | 0x3f800000u);
+  if (m > (float)1.4142135623730951) {
+    m = __fmul_rn(m, 0.5f);
+    e += 1;
+  }
+  const float f = __fsub_rn(m, 1.0f);
+  const float s = __fdiv_rn(f, __fadd_rn(2.0f, f));
+  const float s2 = __fmul_rn(s, s);
+  float q = (float)(1.0 / 13.0);
+  q = __fmaf_rn(q, s2, (float)(1.0 / 11.0));
+  q = __fmaf_rn(q, s2, (float)(1.0 / 9.0));
+  q = __fmaf_rn(q, s2, (float)(1.0 / 7.0));
+  q = __fmaf_rn(q, s2, (float)(1.0 / 5.0));
+  q = __fmaf_rn(q, s2, (float)(1.0 / 3.0));
+  q = __fmul_rn(q, s2);
+  const float t = __fmaf_rn(s, q, s);
+  const float logm = __fadd_rn(t, t);
+  const float corr = __fdiv_rn(__fsub_rn(z, __fsub_rn(w, 1.0f)), w);
+  const float ef = static_cast<float>(e);
+  return __fmaf_rn(ef, ln2_hi, __fmaf_rn(ef, ln2_lo, __fadd_rn(logm, corr)));
+}
+
+__device__ __forceinline__ float spec_softplus(float v) {
+  if (v > 20.0f) return v;
+  return spec_log1p(spec_exp(v));
+}
+
+// --------------------------------------------------------------------------
+// Philox4x32 with 7 rounds (Salmon et al., SC'11): the stochastic-rounding
+// hash.  Counter (element/4, head, slot, flush epoch), key = 64-bit seed.
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint4 philox4x32_7(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, uint32_t k0,
+                                              uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 7; ++r) {
+    if (r) {
+      k0 += 0x9E3779B9u;
+      k1 += 0xBB67AE85u;
+    }
+    const uint32_t hi0 = __umulhi(0xD2511F53u, c0), lo0 = 0xD2511F53u * c0;
+    const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2), lo1 = 0xCD9E8D57u * c2;
+    const uint32_t n0 = hi1 ^ c1 ^ k0, n2 = hi0 ^ c3 ^ k1;
+    c0 = n0;
+    c1 = lo1;
+    c2 = n2;
+    c3 = lo0;
+  }
+  return make_uint4(c0, c1, c2, c3);
+}
+
+// --------------------------------------------------------------------------
+// Rounding onto the state formats.  Nearest: ties to even, saturating at
+// the largest finite value.  Stochastic: |v| goes to the grid point above
+// with probability equal to its fractional distance from the one below,
+// using u = (rnd >> 8) 2^-24; all steps are exact (power-of-two scaling).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t round_bf16(float v, bool sr, uint32_t rnd) {
+  const uint32_t u = __float_as_uint(v);
+  uint32_t r;
+  if (sr) {
+    const uint32_t low = u & 0xffffu;
+    r = (u >> 16) + (((rnd >> 8) < (low << 8)) ? 1u : 0u);
+  } else {
+    r = (u + 0x7fffu + ((u >> 16) & 1u)) >> 16;
+  }
+  if ((r & 0x7fffu) == 0x7f80u) r = (r & 0x8000u) | 0x7f7fu;  // saturate
+  return static_cast<uint16_t>(r);
+}
+
+// grid with mbits fraction bits, lowest normal exponent emin: round |v| up or
+// down stochastically, saturate at maxf, keep the sign.
+__device__ __forceinline__ float sr_grid(float v, int mbits, int emin, float maxf, uint32_t rnd) {
+  const float a = fabsf(v);
+  int e = static_cast<int>((__float_as_uint(a) >> 23) & 0xffu) - 127;
+  e = max(e, emin);
+  const int qe = e - mbits;
+  const float inv_q = __uint_as_float(static_cast<uint32_t>(127 - qe) << 23);  // 2^-qe
+  const float q = __uint_as_float(static_cast<uint32_t>(127 + qe) << 23);      // 2^qe
+  const float ratio = __fmul_rn(a, inv_q);
+  const float n = floorf(ratio);
+  const float f = __fsub_rn(ratio, n);
+  const float uu = __fmul_rn(static_cast<float>(rnd >> 8), 5.9604644775390625e-8f);  // 2^-24
+  float mag = __fmul_rn(uu < f ? __fadd_rn(n, 1.0f) : n, q);
+  mag = fminf(mag, maxf);
+  return copysignf(mag, v);
+}
+
+__device__ __forceinline__ uint16_t round_f16(float v, bool sr, uint32_t rnd) {
+  float g = sr ? sr_grid(v, 10, -14, 65504.0f, rnd) : v;
+  __half h = __float2half_rn(g);
+  uint16_t bits = *reinterpret_cast<uint16_t*>(&h);
+  if ((bits & 0x7fffu) == 0x7c00u) bits = (bits & 0x8000u) | 0x7bffu;  // saturate
+  return bits;
+}
+
+__device__ __forceinline__ uint8_t round_e4m3(float v, bool sr, uint32_t rnd) {
+  float g = sr ? sr_grid(v, 3, -6, 448.0f, rnd) : v;
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(g, __NV_SATFINITE, __NV_E4M3));
+}
+
+__device__ __forceinline__ int8_t round_i8(float v, bool sr, uint32_t rnd) {
+  float g;
+  if (sr) {
+    const float a = fabsf(v);
+    const float n = floorf(a);
+    const float f = __fsub_rn(a, n);
+    const float uu = __fmul_rn(static_cast<float>(rnd >> 8), 5.9604644775390625e-8f);
+    g = copysignf(fminf(uu < f ? __fadd_rn(n, 1.0f) : n, 127.0f), v);
+  } else {
+    g = fminf(fmaxf(rintf(v), -127.0f), 127.0f);
+  }
+  return static_cast<int8_t>(static_cast<int>(g));
+}
+
+__device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
+  __half_raw hr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(c), __NV_E4M3);
+  return __half2float(__half(hr));
+}
+
+// --------------------------------------------------------------------------
+// Checkpoint quantiser for one thread's 4 rows x 8 columns (rows r0..r0+3,
+// columns c0..c0+7 of a [64][128] head), the fragment the flush and init
+// kernels own.  Lanes sharing rows must be the 16 lanes with equal
+// (lane >> 4) of a warp (they hold the 128 columns of those rows).
+// 8-bit formats: per-row scale = amax/QMAX (1 for amax < 2^-100), v = acc *
+// (1/scale), then nearest or stochastic rounding.
+// --------------------------------------------------------------------------
+template <int DT>
+__device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c0, int lane, void* head_state,
+                                               float* head_scale, int rounding, uint32_t h, uint32_t s,
+                                               uint32_t epoch, uint64_t seed) {
+  const bool sr = rounding == RSSM_ROUND_STOCHASTIC;
+  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+  uint32_t rnd[4][8];
+  if (DT != RSSM_F32 && sr) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const uint32_t elem = static_cast<uint32_t>((r0 + i) * 128 + c0 + 4 * q);
+        const uint4 w = philox4x32_7(elem >> 2, h, s, epoch, k0, k1);
+        rnd[i][4 * q + 0] = w.x;
+        rnd[i][4 * q + 1] = w.y;
+        rnd[i][4 * q + 2] = w.z;
+        rnd[i][4 * q + 3] = w.w;
+      }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int q = 0; q < 8; ++q) rnd[i][q] = 0u;
+  }
+  if constexpr (DT == RSSM_F32) {
+    float* st = static_cast<float*>(head_state);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float4* dst = reinterpret_cast<float4*>(st + (r0 + i) * 128 + c0);
+      dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+    }
+  } else if constexpr (DT == RSSM_BF16 || DT == RSSM_F16) {
+    uint16_t* st = static_cast<uint16_t*>(head_state);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t wds[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        uint16_t lo, hi;
+        if constexpr (DT == RSSM_BF16) {
+          lo = round_bf16(acc[i][2 * q], sr, rnd[i][2 * q]);
+          hi = round_bf16(acc[i][2 * q + 1], sr, rnd[i][2 * q + 1]);
+        } else {
+          lo = round_f16(acc[i][2 * q], sr, rnd[i][2 * q]);
+          hi = round_f16(acc[i][2 * q + 1], sr, rnd[i][2 * q + 1]);
+        }
+        wds[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+      }
+      *reinterpret_cast<uint4*>(st + (r0 + i) * 128 + c0) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+    }
+  } else {
+    constexpr float qmax = (DT == RSSM_I8) ? 127.0f : 448.0f;
+    float amax[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float m = 0.0f;
+#pragma unroll
+      for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(acc[i][q]));
+#pragma unroll
+      for (int off = 1; off < 16; off <<= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+      amax[i] = m;
+    }
+    // lane (lane & 3) of each 16-lane group computes row (lane & 3)'s scale
+    const int mine = lane & 3;
+    float am = amax[0];
+#pragma unroll
+    for (int i = 1; i < 4; ++i)
+      if (mine == i) am = amax[i];
+    const float sc = am < 7.888609052210118e-31f /* 2^-100 */ ? 1.0f : __fdiv_rn(am, qmax);
+    const float iv = __frcp_rn(sc);
+    float scale[4], inv[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      scale[i] = __shfl_sync(0xffffffffu, sc, (lane & 16) | i);
+      inv[i] = __shfl_sync(0xffffffffu, iv, (lane & 16) | i);
+    }
+    uint8_t* st = static_cast<uint8_t*>(head_state);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      uint32_t wds[2] = {0u, 0u};
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const float v = __fmul_rn(acc[i][q], inv[i]);
+        uint32_t code;
+        if constexpr (DT == RSSM_I8)
+          code = static_cast<uint8_t>(round_i8(v, sr, rnd[i][q]));
+        else
+          code = round_e4m3(v, sr, rnd[i][q]);
+        wds[q >> 2] |= code << (8 * (q & 3));
+      }
+      *reinterpret_cast<uint2*>(st + (r0 + i) * 128 + c0) = make_uint2(wds[0], wds[1]);
+    }
+    if ((lane & 15) == 0)
+      *reinterpret_cast<float4*>(head_scale + r0) = make_float4(scale[0], scale[1], scale[2], scale[3]);
+  }
+}
+
+}  // namespace rssm

@@ -1,0 +1,470 @@
+// rssm_flush.cu -- flush (classify + fold + requantise), init, accept.
+//
+// Flush of the ReplaySSM checkpointing SSU (FlashInfer PR #3975, commit note
+// on the persistent path: the write decision prev_k + T > max_window is
+// taken per slot at run time; vLLM PR #65660, Details: only the accepted
+// prefix enters the checkpoint).  Two kernels:
+//   flag_kernel  one CTA: per row decide flush, compact the flagged rows into
+//                scratch records and advance the ring bookkeeping
+//                (ring_start += p mod L, pnat = 0, epoch += 1).
+//   fold_kernel  persistent, one (flagged row, head) unit at a time:
+//                S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
+//                in fp32, canonical order, then rounding to the state format.
+// The fold streams S0 (and the live x/B rows) through a 3-stage shared-memory
+// ring filled by 1-D bulk copies from a producer warp; 8 consumer warps own a
+// 4x8 fragment of the [64][128] state each and accumulate with packed f32x2
+// FMAs.  HBM traffic per unit: read + write of S0 (+ scales) and p rows of x
+// and B.
+#include <cuda_runtime.h>
+
+#include "rssm_device.cuh"
+
+namespace rssm {
+
+// ---------------------------------------------------------------------------
+// classification + compaction + bookkeeping (one CTA of 1024 threads)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) flag_kernel(FlushArgs a) {
+  __shared__ int warp_tot[32];
+  __shared__ int base;
+  const Cache& c = a.c;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) base = 0;
+  __syncthreads();
+  for (int b0 = 0; b0 < a.batch; b0 += 1024) {
+    const int b = b0 + tid;
+    int flag = 0;
+    FlushRec rec = {};
+    if (b < a.batch) {
+      const int s = a.slot_idx[b];
+      if (s >= 1 && s < c.S) {
+        const int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
+        const int p = a.pnat[b];
+        if (Tb < 0 || Tb > a.T) {
+          set_error(c.err, RSSM_ERRBIT_SEQLEN);
+        } else if (p < 0 || p > c.L) {
+          set_error(c.err, RSSM_ERRBIT_PNAT);
+        } else if (a.force || p + Tb > c.W) {
+          const int r = c.ring_start[s];
+          const unsigned e = c.epoch[s] + 1u;
+          rec.b = b;
+          rec.s = s;
+          rec.r = r;
+          rec.p = p;
+          rec.epoch = e;
+          flag = 1;
+          c.ring_start[s] = (r + p) % c.L;
+          a.pnat[b] = 0;
+          c.epoch[s] = e;
+        }
+      }
+    }
+    // block-wide inclusive scan of the flags
+    int v = flag;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int n = __shfl_up_sync(0xffffffffu, v, off);
+      if (lane >= off) v += n;
+    }
+    if (lane == 31) warp_tot[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int t = warp_tot[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, t, off);
+        if (lane >= off) t += n;
+      }
+      warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int excl = base + v - flag + (warp ? warp_tot[warp - 1] : 0);
+    if (flag) a.recs[excl] = rec;
+    __syncthreads();
+    if (tid == 0) base += warp_tot[31];
+    __syncthreads();
+  }
+  if (tid == 0) *a.count = base;
+}
+
+// ---------------------------------------------------------------------------
+// fold kernel
+// ---------------------------------------------------------------------------
+struct FoldMeta {
+  int s, h, p;
+  unsigned epoch;
+};
+
+struct FoldLayout {
+  int ns, KB;
+  uint32_t s0_bytes, scale_off, x_off, b_off, w_off, stage_bytes;
+  uint32_t meta_off, stages_off, uf_off, bf_off, total;
+};
+
+__host__ __device__ inline FoldLayout fold_layout(int dtype, int L) {
+  FoldLayout f;
+  f.ns = 3;
+  f.KB = (L + 3) & ~3;
+  const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
+  f.s0_bytes = kHeadElems * esz;
+  uint32_t o = f.s0_bytes;
+  f.scale_off = o;
+  if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
+  f.x_off = o;
+  o += f.KB * kDim * 2;
+  f.b_off = o;
+  o += f.KB * kDstate * 2;
+  f.w_off = o;
+  o += (f.KB + 4) * 4;
+  f.stage_bytes = (o + 127) & ~127u;
+  f.meta_off = 256;  // after the barriers
+  f.stages_off = 512;
+  f.uf_off = f.stages_off + f.ns * f.stage_bytes;
+  f.bf_off = f.uf_off + f.KB * kDim * 8;
+  f.total = f.bf_off + f.KB * kDstate * 4;
+  return f;
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kThreads, 1) fold_kernel(FlushArgs a) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Cache& c = a.c;
+  const FoldLayout lay = fold_layout(DT, c.L);
+  constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
+  constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
+
+  const long long units = static_cast<long long>(*a.count) * c.H;
+  const long long per = units / gridDim.x, rem = units % gridDim.x;
+  const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
+  const int nu = static_cast<int>(per + (blockIdx.x < rem ? 1 : 0));
+  if (nu == 0) return;
+
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + 4;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
+  FoldMeta* meta = reinterpret_cast<FoldMeta*>(smem + lay.meta_off);
+  float2* uf2 = reinterpret_cast<float2*>(smem + lay.uf_off);
+  float* bfv = reinterpret_cast<float*>(smem + lay.bf_off);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int st = 0; st < lay.ns; ++st) {
+      mbar_init(&full[st], 1);
+      mbar_init(&empty[st], kConsumerWarps);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+
+  if (warp == kConsumerWarps) {
+    // ---------------- producer warp ----------------
+    int cur = -1;
+    FlushRec rec = {};
+    float Ah = 0.0f;
+    int issued = 0;
+    bool ok = true;
+    for (int i = 0; i < nu && ok; ++i) {
+      const int st = i % lay.ns;
+      const uint32_t ph = (i / lay.ns) & 1;
+      if (i >= lay.ns && !mbar_wait(&empty[st], ph ^ 1)) {
+        ok = false;
+        break;
+      }
+      const long long u = u0 + i;
+      const int li = static_cast<int>(u / c.H), h = static_cast<int>(u % c.H);
+      if (li != cur) {
+        rec = a.recs[li];
+        cur = li;
+      }
+      Ah = a.A[h];
+      const int s = rec.s, r = rec.r, p = rec.p, g = h / c.hpg;
+      uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
+      if (lane == 0) {
+        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + static_cast<uint32_t>(p) * (kDim * 2 + kDstate * 2);
+        mbar_expect_tx(&full[st], bytes);
+        const uint8_t* st_g = static_cast<const uint8_t*>(c.state) +
+                              (static_cast<long long>(s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz;
+        bulk_g2s(sb, st_g, lay.s0_bytes, &full[st]);
+        if (k8bit) bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256,
+                            &full[st]);
+        const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * c.L * kDim;
+        const uint16_t* bg = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * c.L * kDstate;
+        const int n1 = min(p, c.L - r);
+        if (n1 > 0) {
+          bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
+          bulk_g2s(sb + lay.b_off, bg + r * kDstate, n1 * kDstate * 2, &full[st]);
+        }
+        if (p > n1) {
+          bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (p - n1) * kDim * 2, &full[st]);
+          bulk_g2s(sb + lay.b_off + n1 * kDstate * 2, bg, (p - n1) * kDstate * 2, &full[st]);
+        }
+      }
+      // canonical cumulative sums c_j (sequential fp32) and weights
+      float dtj = 0.0f, aj = 0.0f;
+      if (lane < p) {
+        dtj = c.dt_cache[static_cast<long long>(s) * c.dt_stride + static_cast<long long>(h) * c.L + (r + lane) % c.L];
+        aj = __fmul_rn(Ah, dtj);
+      }
+      float cj = 0.0f;
+      for (int k = 0; k < p; ++k) {
+        const float ak = __shfl_sync(0xffffffffu, aj, k);
+        if (lane >= k) cj = __fadd_rn(cj, ak);
+      }
+      const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
+      float* wv = reinterpret_cast<float*>(sb + lay.w_off);
+      if (lane < p) wv[lane] = __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj);
+      if (lane == 0) {
+        wv[lay.KB] = spec_exp(c_end);
+        meta[st] = FoldMeta{s, h, p, rec.epoch};
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&full[st]);
+      issued = i + 1;
+    }
+    if (!ok) {
+      if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+      // let copies already in flight land before the CTA can exit
+      for (int i = max(0, issued - lay.ns); i < issued; ++i) mbar_wait(&full[i % lay.ns], (i / lay.ns) & 1);
+    }
+    return;
+  }
+
+  // ---------------- consumer warps ----------------
+  const int rs = lane >> 4, cc = lane & 15;
+  const int r0 = 8 * warp + 4 * rs, c0 = 8 * cc;
+  for (int i = 0; i < nu; ++i) {
+    const int st = i % lay.ns;
+    const uint32_t ph = (i / lay.ns) & 1;
+    if (!mbar_wait(&full[st], ph)) {
+      *abort_flag = 1;
+      if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+    }
+    consumer_sync();  // previous unit done with uf2/bfv; abort decision is uniform
+    if (*abort_flag) return;
+    const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
+    const FoldMeta m = meta[st];
+    const float* wv = reinterpret_cast<const float*>(sb + lay.w_off);
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
+    const uint32_t* bs = reinterpret_cast<const uint32_t*>(sb + lay.b_off);
+    for (int idx = tid; idx < m.p * kDim; idx += kConsumerThreads) {
+      const float uu = __fmul_rn(wv[idx >> 6], bf16f(xs[idx]));
+      uf2[idx] = make_float2(uu, uu);
+    }
+    for (int idx = tid; idx < m.p * (kDstate / 2); idx += kConsumerThreads) {
+      const uint32_t wd = bs[idx];
+      reinterpret_cast<float2*>(bfv)[idx] = make_float2(bf16lo(wd), bf16hi(wd));
+    }
+    // acc = e^{c_end} * S0f
+    const float decay = wv[lay.KB];
+    float2 acc[4][4];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4) {
+      const int row = r0 + i4;
+      float v[8];
+      if constexpr (DT == RSSM_F32) {
+        const float4* p4 = reinterpret_cast<const float4*>(sb + (row * kDstate + c0) * 4);
+        const float4 x0 = p4[0], x1 = p4[1];
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+      } else if constexpr (DT == RSSM_BF16) {
+        const uint4 q = *reinterpret_cast<const uint4*>(sb + (row * kDstate + c0) * 2);
+        v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+        v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+      } else if constexpr (DT == RSSM_F16) {
+        const uint4 q = *reinterpret_cast<const uint4*>(sb + (row * kDstate + c0) * 2);
+        float2 t0 = h2f2(q.x), t1 = h2f2(q.y), t2 = h2f2(q.z), t3 = h2f2(q.w);
+        v[0] = t0.x; v[1] = t0.y; v[2] = t1.x; v[3] = t1.y; v[4] = t2.x; v[5] = t2.y; v[6] = t3.x; v[7] = t3.y;
+      } else {
+        const uint2 q = *reinterpret_cast<const uint2*>(sb + row * kDstate + c0);
+        const float sc = reinterpret_cast<const float*>(sb + lay.scale_off)[row];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t byte = ((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xffu;
+          const float code = DT == RSSM_I8 ? static_cast<float>(static_cast<int8_t>(byte)) : e4m3_to_f32(byte);
+          v[e] = __fmul_rn(code, sc);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        acc[i4][q] = make_float2(__fmul_rn(decay, v[2 * q]), __fmul_rn(decay, v[2 * q + 1]));
+    }
+    consumer_sync();  // uf2 / bfv complete
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);  // the stage is no longer read
+    // acc[d][n] = fma(u_j[d], B_j[n], acc), j ascending
+    for (int j = 0; j < m.p; ++j) {
+      const float4* up = reinterpret_cast<const float4*>(uf2 + j * kDim + r0);
+      const float4 u01 = up[0], u23 = up[1];
+      const float4* bp = reinterpret_cast<const float4*>(bfv + j * kDstate + c0);
+      const float4 b0 = bp[0], b1 = bp[1];
+      const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
+                            make_float2(b1.z, b1.w)};
+      const float2 uu[4] = {make_float2(u01.x, u01.y), make_float2(u01.z, u01.w), make_float2(u23.x, u23.y),
+                            make_float2(u23.z, u23.w)};
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i4][q] = __ffma2_rn(uu[i4], bb[q], acc[i4][q]);
+    }
+    float accf[4][8];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        accf[i4][2 * q] = acc[i4][q].x;
+        accf[i4][2 * q + 1] = acc[i4][q].y;
+      }
+    void* head_state = static_cast<uint8_t*>(c.state) +
+                       (static_cast<long long>(m.s) * c.state_stride + static_cast<long long>(m.h) * kHeadElems) * esz;
+    float* head_scale = k8bit ? c.scale + static_cast<long long>(m.s) * c.scale_stride + m.h * kDim : nullptr;
+    quantize_store<DT>(accf, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(m.h),
+                       static_cast<uint32_t>(m.s), m.epoch, a.seed);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// init: quantise FP32 prefill states, clear rings
+// ---------------------------------------------------------------------------
+template <int DT>
+__global__ void __launch_bounds__(kConsumerThreads) init_quant_kernel(InitArgs a) {
+  const Cache& c = a.c;
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int s = a.ids[i];
+  if (s < 1 || s >= c.S) return;
+  constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
+  const float* src = a.states + (static_cast<long long>(i) * c.H + h) * kHeadElems;
+  float acc[4][8];
+#pragma unroll
+  for (int i4 = 0; i4 < 4; ++i4) {
+    const float4* p4 = reinterpret_cast<const float4*>(src + (r0 + i4) * kDstate + c0);
+    const float4 x0 = p4[0], x1 = p4[1];
+    acc[i4][0] = x0.x; acc[i4][1] = x0.y; acc[i4][2] = x0.z; acc[i4][3] = x0.w;
+    acc[i4][4] = x1.x; acc[i4][5] = x1.y; acc[i4][6] = x1.z; acc[i4][7] = x1.w;
+  }
+  void* head_state = static_cast<uint8_t*>(c.state) +
+                     (static_cast<long long>(s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz;
+  float* head_scale =
+      (DT == RSSM_I8 || DT == RSSM_E4M3) ? c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim : nullptr;
+  quantize_store<DT>(acc, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(h),
+                     static_cast<uint32_t>(s), 0u, a.seed);
+}
+
+__global__ void __launch_bounds__(256) init_clear_kernel(InitArgs a) {
+  const Cache& c = a.c;
+  const int s = a.ids[blockIdx.x];
+  if (s < 1 || s >= c.S) return;
+  const int tid = threadIdx.x + blockIdx.y * blockDim.x, nth = blockDim.x * gridDim.y;
+  uint4* xr = reinterpret_cast<uint4*>(c.x_cache + static_cast<long long>(s) * c.x_stride);
+  const int nx = c.H * c.L * kDim * 2 / 16;
+  for (int k = tid; k < nx; k += nth) xr[k] = make_uint4(0, 0, 0, 0);
+  uint4* br = reinterpret_cast<uint4*>(c.B_cache + static_cast<long long>(s) * c.B_stride);
+  const int nb = c.G * c.L * kDstate * 2 / 16;
+  for (int k = tid; k < nb; k += nth) br[k] = make_uint4(0, 0, 0, 0);
+  float* dr = c.dt_cache + static_cast<long long>(s) * c.dt_stride;
+  for (int k = tid; k < c.H * c.L; k += nth) dr[k] = 0.0f;
+  if (tid == 0) {
+    c.ring_start[s] = 0;
+    c.epoch[s] = 0u;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// accept: pnat += accepted
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) accept_kernel(Cache c, const int* slot_idx, int* pnat, const int* accepted,
+                                                     const int* cu, int batch, int T) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= batch) return;
+  const int s = slot_idx[b];
+  if (s < 1 || s >= c.S) return;
+  const int Tb = cu ? cu[b + 1] - cu[b] : T;
+  if (Tb < 0 || Tb > T) {
+    set_error(c.err, RSSM_ERRBIT_SEQLEN);
+    return;
+  }
+  const int acc = accepted[b];
+  if (acc < 0 || acc > Tb) {
+    set_error(c.err, RSSM_ERRBIT_ACCEPT);
+    return;
+  }
+  const int p = pnat[b];
+  if (p < 0 || p + acc > c.L) {
+    set_error(c.err, RSSM_ERRBIT_PNAT);
+    return;
+  }
+  pnat[b] = p + acc;
+}
+
+__global__ void spec_math_kernel(const float* in, float* oexp, float* osp, long long n) {
+  for (long long k = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; k < n;
+       k += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const float v = in[k];
+    if (oexp) oexp[k] = spec_exp(v);
+    if (osp) osp[k] = spec_softplus(v);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// launchers
+// ---------------------------------------------------------------------------
+template <int DT>
+static int launch_fold_t(const FlushArgs& a, int num_sms, cudaStream_t st) {
+  const FoldLayout lay = fold_layout(DT, a.c.L);
+  cudaError_t e = cudaFuncSetAttribute(fold_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+  if (e != cudaSuccess) return e;
+  // the number of flagged rows is only known on the device: size the grid for
+  // the worst case (every row flagged), capped at one CTA per SM
+  const long long units = static_cast<long long>(a.batch) * a.c.H;
+  const int grid = static_cast<int>(units < num_sms ? (units > 0 ? units : 1) : num_sms);
+  fold_kernel<DT><<<grid, kThreads, lay.total, st>>>(a);
+  return cudaGetLastError();
+}
+
+int launch_flush(const FlushArgs& a, int num_sms, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  flag_kernel<<<1, 1024, 0, st>>>(a);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  switch (a.c.dtype) {
+    case RSSM_F32: return launch_fold_t<RSSM_F32>(a, num_sms, st);
+    case RSSM_BF16: return launch_fold_t<RSSM_BF16>(a, num_sms, st);
+    case RSSM_F16: return launch_fold_t<RSSM_F16>(a, num_sms, st);
+    case RSSM_I8: return launch_fold_t<RSSM_I8>(a, num_sms, st);
+    default: return launch_fold_t<RSSM_E4M3>(a, num_sms, st);
+  }
+}
+
+int launch_init(const InitArgs& a, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dim3 grid(a.n, a.c.H);
+  switch (a.c.dtype) {
+    case RSSM_F32: init_quant_kernel<RSSM_F32><<<grid, kConsumerThreads, 0, st>>>(a); break;
+    case RSSM_BF16: init_quant_kernel<RSSM_BF16><<<grid, kConsumerThreads, 0, st>>>(a); break;
+    case RSSM_F16: init_quant_kernel<RSSM_F16><<<grid, kConsumerThreads, 0, st>>>(a); break;
+    case RSSM_I8: init_quant_kernel<RSSM_I8><<<grid, kConsumerThreads, 0, st>>>(a); break;
+    default: init_quant_kernel<RSSM_E4M3><<<grid, kConsumerThreads, 0, st>>>(a); break;
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  init_clear_kernel<<<dim3(a.n, 8), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* accepted, const int* cu, int batch,
+                  int T, void* stream) {
+  accept_kernel<<<(batch + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(c, slot_idx, pnat, accepted,
+                                                                                    cu, batch, T);
+  return cudaGetLastError();
+}
+
+int launch_spec_math(const float* in, float* oexp, float* osp, long long n, void* stream) {
+  const long long blocks = (n + 255) / 256;
+  spec_math_kernel<<<static_cast<int>(blocks < 4096 ? blocks : 4096), 256, 0, static_cast<cudaStream_t>(stream)>>>(
+      in, oexp, osp, n);
+  return cudaGetLastError();
+}
+
+}  // namespace rssm

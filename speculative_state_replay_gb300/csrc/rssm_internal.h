@@ -1,0 +1,116 @@
+// rssm_internal.h -- structures shared by the host entry points and the
+// kernels of librssm.  Not part of the public ABI.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "rssm.h"
+
+namespace rssm {
+
+constexpr int kDim = 64;      // head dim
+constexpr int kDstate = 128;  // state dim
+constexpr int kHeadElems = kDim * kDstate;
+constexpr int kMaxL = 32;     // ring length the kernels are built for (one lane per ring slot)
+constexpr int kMaxT = 8;      // draft tokens per step
+constexpr int kConsumerWarps = 8;
+constexpr int kConsumerThreads = kConsumerWarps * 32;
+constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
+constexpr uint32_t kWaitSpins = 1u << 22;        // ~1 s of bounded mbarrier polling
+
+// device view of an rssm_cache
+struct Cache {
+  int S, H, G, hpg, W, Tmax, L;
+  int dtype, rounding;
+  void* state;
+  long long state_stride;
+  float* scale;
+  long long scale_stride;
+  uint16_t* x_cache;
+  long long x_stride;
+  uint16_t* B_cache;
+  long long B_stride;
+  float* dt_cache;
+  long long dt_stride;
+  int* ring_start;
+  unsigned* epoch;
+  unsigned* err;
+};
+
+// one flagged row of a flush (written by the flag kernel), 32 bytes
+struct FlushRec {
+  int b, s, r, p;
+  unsigned epoch;  // epoch of the state this flush writes
+  int pad[3];
+};
+
+// one row of a step (written by the precompute, read by the readout), 32 bytes
+struct RowRec {
+  int s, r, p, Tb, tok0;
+  int flags;  // 1: compute; 0: write zeros for Tb tokens
+  int pad[2];
+};
+
+struct FlushArgs {
+  Cache c;
+  const float* A;
+  const int* slot_idx;
+  int* pnat;
+  const int* cu;
+  int batch, T, force;
+  unsigned long long seed;
+  int* count;      // scratch: number of flagged rows
+  FlushRec* recs;  // scratch: flagged rows
+};
+
+struct StepArgs {
+  Cache c;
+  const uint16_t* x;
+  const float* dt;
+  const float* A;
+  const uint16_t* B;
+  const uint16_t* C;
+  const float* D;
+  const float* dt_bias;
+  const int* slot_idx;
+  const int* pnat;
+  const int* cu;
+  int batch, T;
+  int TP;  // T padded to 4 or 8
+  int KB;  // ring rows padded to a multiple of 4
+  uint16_t* out;
+  RowRec* rows;  // scratch [batch]
+  float* coef;   // scratch [batch][H][KB+1][TP]
+};
+
+struct InitArgs {
+  Cache c;
+  const float* states;
+  const int* ids;
+  int n;
+  unsigned long long seed;
+};
+
+inline int ring_pad(int L) { return (L + 3) & ~3; }
+inline int t_pad(int T) { return T <= 4 ? 4 : 8; }
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// scratch layout
+inline size_t flush_scratch_bytes(int batch) { return 256 + align_up(sizeof(FlushRec) * (size_t)batch, 256); }
+inline size_t step_rows_bytes(int batch) { return align_up(sizeof(RowRec) * (size_t)batch, 256); }
+inline size_t step_scratch_bytes(int batch, int H, int L, int T) {
+  const size_t blk = (size_t)(ring_pad(L) + 1) * t_pad(T) * sizeof(float);
+  return step_rows_bytes(batch) + align_up(blk * (size_t)batch * H, 256);
+}
+
+// launchers (defined in the .cu files); return a cudaError_t as int
+int launch_flush(const FlushArgs& a, int num_sms, void* stream);
+int launch_precompute(const StepArgs& a, void* stream);
+int launch_readout(const StepArgs& a, int num_sms, void* stream);
+int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* accepted, const int* cu, int batch,
+                  int T, void* stream);
+int launch_init(const InitArgs& a, void* stream);
+int launch_spec_math(const float* in, float* oexp, float* osp, long long n, void* stream);
+
+}  // namespace rssm

@@ -1,0 +1,97 @@
+"""The C ABI library (CPU only): it builds, loads, exports every function the
+header declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_state_replay_gb300 import _lib, build
+
+    try:
+        build.nvcc()
+    except RuntimeError:
+        pytest.skip("nvcc not available")
+    build.build()
+    return _lib.load()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "rssm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(rssm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ("rssm_init_state", "rssm_flush", "rssm_step", "rssm_accept", "rssm_scratch_bytes",
+              "rssm_status_string", "rssm_step_precompute", "rssm_step_readout"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in header_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_binding_exports_match_header():
+    from speculative_state_replay_gb300 import _lib
+
+    assert set(_lib.EXPORTS) <= set(header_functions())
+
+
+def _cache(**kw):
+    from speculative_state_replay_gb300 import _lib
+
+    c = _lib.RssmCacheStruct()
+    c.num_slots, c.nheads, c.ngroups, c.dim, c.dstate = 5, 8, 1, 64, 128
+    c.max_window, c.npredicted, c.state_dtype, c.rounding = 16, 4, 1, 0
+    base = 1 << 20  # fake, aligned, never dereferenced on these paths
+    c.state, c.state_slot_stride = base, 8 * 64 * 128
+    c.scale, c.scale_slot_stride = base, 8 * 64
+    c.x_cache, c.x_slot_stride = base, 8 * 20 * 64
+    c.B_cache, c.B_slot_stride = base, 1 * 20 * 128
+    c.dt_cache, c.dt_slot_stride = base, 8 * 20
+    c.ring_start = c.flush_epoch = c.error_word = base
+    for k, v in kw.items():
+        setattr(c, k, v)
+    return c
+
+
+def test_scratch_bytes_and_shape_validation(lib):
+    good = _cache()
+    n = lib.rssm_scratch_bytes(ctypes.byref(good), 64, 4)
+    assert n >= 64 * 32
+    assert lib.rssm_scratch_bytes(ctypes.byref(_cache(dim=32)), 64, 4) == 0
+    assert lib.rssm_scratch_bytes(ctypes.byref(_cache(ngroups=3)), 64, 4) == 0
+    assert lib.rssm_scratch_bytes(ctypes.byref(_cache(npredicted=20)), 64, 4) == 0  # L > 32
+    assert lib.rssm_scratch_bytes(ctypes.byref(_cache(x_slot_stride=10)), 64, 4) == 0
+    assert lib.rssm_scratch_bytes(ctypes.byref(_cache(state=(1 << 20) + 8)), 64, 4) == 0  # misaligned
+    assert lib.rssm_scratch_bytes(ctypes.byref(good), 64, 9) == 0
+
+
+def test_entry_points_reject_bad_arguments_before_launching(lib):
+    c = ctypes.byref(_cache())
+    nul = None
+    assert lib.rssm_step(None, *([nul] * 10), 4, 4, nul, nul, 0, nul) == 1
+    assert lib.rssm_step(c, *([nul] * 10), 4, 4, nul, nul, 0, nul) == 1  # null inputs
+    assert lib.rssm_step(ctypes.byref(_cache(dim=32)), *([nul] * 10), 4, 4, nul, nul, 0, nul) == 2
+    p = ctypes.c_void_p(1 << 20)
+    args = [p] * 10
+    assert lib.rssm_step(c, *args, 4, 5, p, p, 1 << 30, nul) == 2  # T > npredicted
+    assert lib.rssm_step(c, *args, 4, 4, p, p, 16, nul) == 3  # scratch too small
+    assert lib.rssm_flush(c, p, p, p, nul, 4, 4, 2, 0, p, 1 << 20, nul) == 1  # force not 0/1
+    assert lib.rssm_flush(c, p, p, p, nul, 4, 4, 0, 0, p, 8, nul) == 3
+    assert lib.rssm_init_state(c, ctypes.c_void_p((1 << 20) + 4), p, 2, 0, nul) == 1  # misaligned states
+    assert lib.rssm_accept(c, nul, nul, nul, nul, 4, 4, nul) == 1
+    # empty batches are a no-op
+    assert lib.rssm_step(c, *args, 0, 4, p, p, 0, nul) == 0
+    assert lib.rssm_flush(c, p, p, p, nul, 0, 4, 0, 0, p, 0, nul) == 0
+    for s, text in [(0, b"ok"), (3, b"scratch buffer too small")]:
+        assert lib.rssm_status_string(s) == text

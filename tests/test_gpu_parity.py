@@ -1,0 +1,220 @@
+"""CUDA library vs CPU oracle on the same seeded inputs (needs a GPU).
+
+Bar: bf16 outputs within atol 2e-2 / rtol 1e-2; f32 checkpoints within 1e-4
+relative; 2-byte checkpoints within the bf16 tolerance; 8-bit codes and
+scales, rings, ring_start, pnat, flush epochs and error bits bit-exact.
+"""
+import numpy as np
+import pytest
+import torch
+
+from speculative_state_replay_gb300 import api
+from speculative_state_replay_gb300 import workloads as W
+from tests.gpu_harness import Pair, bf16_f32, dev_of, host_of
+from tests.harness import oracle_cache
+
+pytestmark = pytest.mark.gpu
+
+DTYPES = [W.F32, W.BF16, W.F16, W.I8, W.E4M3]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_state_replay_gb300 import _lib, build
+
+    build.build()
+    _lib.load()
+
+
+def run_pair(orc, wl, steps=None, force_every=0, oracle_ids=None):
+    gen = W.Generator(wl)
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    pair = Pair(orc, wl, oc, ids, pnat)
+    for k in range(wl.steps if steps is None else steps):
+        force = 1 if force_every and k % force_every == force_every - 1 else 0
+        pair.step(gen.step(k), force=force)
+    return pair
+
+
+def test_spec_math_bit_exact(orc):
+    rng = np.random.default_rng(0)
+    x = np.concatenate([rng.uniform(-90, 90, 1 << 22), rng.normal(-2.0, 0.5, 1 << 22),
+                        np.linspace(-30, 25, 1 << 20), np.float32([0.0, -0.0, 20.0, 20.000002, -87.0, 88.0])])
+    x = x.astype(np.float32)
+    gx = dev_of(x, "cuda")
+    ge, gs = torch.empty_like(gx), torch.empty_like(gx)
+    api.rssm_eval_spec_math(gx, ge, gs)
+    torch.cuda.synchronize()
+    assert np.array_equal(ge.cpu().numpy().view(np.uint32), orc.spec_exp(x).view(np.uint32))
+    assert np.array_equal(gs.cpu().numpy().view(np.uint32), orc.spec_softplus(x).view(np.uint32))
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("rounding", [W.NEAREST, W.STOCHASTIC])
+def test_init_state_bit_exact(orc, dtype, rounding):
+    wl = W.config("tiny", state_dtype=dtype, rounding=rounding, sr_seed=7)
+    gen = W.Generator(wl)
+    states = gen.init_states(0, 4)
+    states[0, 0, 3] = 0.0  # an all-zero row
+    states[1, 2, 5, 7] = 1e4  # a row with a large outlier
+    ids = np.array([3, 0, 1, 4], np.int32)  # slot 0 is ignored
+    oc = orc.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, dtype, rounding)
+    oc.x_cache[:] = 5
+    oc.ring_start[:] = 2
+    oc.init_state(states, ids, seed=wl.sr_seed)
+    gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, dtype, rounding)
+    gc.x_cache.fill_(5)
+    gc.ring_start.fill_(2)
+    api.rssm_init_state(gc, dev_of(states, "cuda"), dev_of(ids, "cuda"), seed=wl.sr_seed)
+    torch.cuda.synchronize()
+    for name in ("state", "scale", "x_cache", "ring_start", "flush_epoch"):
+        o = getattr(oc, name)
+        assert np.array_equal(host_of(getattr(gc, name), o), o), name
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_tiny_all_dtypes(orc, dtype):
+    wl = W.config("tiny", state_dtype=dtype, prefill_live=14, ring_start_random=True)
+    pair = run_pair(orc, wl)
+    assert pair.oc.flush_epoch.max() >= 1
+
+
+def test_tiny_config_f32_full(orc):
+    """The Tiny configuration exactly as specified: f32 state, 12 steps."""
+    pair = run_pair(orc, W.config("tiny"))
+    assert pair.exact_state_steps == W.config("tiny").steps
+
+
+@pytest.mark.parametrize("dtype,rounding", [(W.I8, W.NEAREST), (W.I8, W.STOCHASTIC), (W.E4M3, W.NEAREST),
+                                            (W.E4M3, W.STOCHASTIC), (W.F16, W.STOCHASTIC),
+                                            (W.BF16, W.STOCHASTIC)])
+def test_eight_bit_config_reduced(orc, dtype, rounding):
+    """8-bit checkpoint configuration (accept all -> flush every 4 steps), 8 rows."""
+    wl = W.config("eight_bit", batch=8, state_dtype=dtype, rounding=rounding, sr_seed=7)
+    pair = run_pair(orc, wl)
+    assert pair.oc.flush_epoch.max() >= 3
+    assert pair.exact_state_steps == wl.steps
+
+
+def test_mamba2_decode_reduced(orc):
+    wl = W.config("mamba2_decode", batch=12, steps=20)
+    pair = run_pair(orc, wl)
+    assert pair.oc.flush_epoch.max() >= 1
+
+
+def test_large_batch_reduced(orc):
+    """fp16 state, T = 7 drafts (L = 23), random ring starts: wraparound."""
+    wl = W.config("large_batch", batch=24, steps=16)
+    run_pair(orc, wl)
+
+
+def test_sweep_reduced_varlen_padded(orc):
+    """varlen 1..5 tokens, padded slot pages, prefilled rings, mixed pnat."""
+    wl = W.config("sweep", batch=24, steps=10)
+    pair = run_pair(orc, wl)
+    assert pair.oc.flush_epoch.max() >= 1
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_forced_full_window_flush(orc, dtype):
+    """Every active row flushes with a full window (p = 16)."""
+    wl = W.config("mamba2_decode", batch=6, state_dtype=dtype, prefill_live=16, ring_start_random=True, steps=3)
+    gen = W.Generator(wl)
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    pnat[:] = 16
+    pair = Pair(orc, wl, oc, ids, pnat)
+    for k in range(wl.steps):
+        pair.step(gen.step(k), force=1)
+
+
+@pytest.mark.parametrize("T,W_,G", [(1, 16, 8), (8, 24, 8), (3, 0, 128), (8, 0, 1)])
+def test_shape_edges(orc, T, W_, G):
+    """T = 1; the largest ring (L = 32) with T = 8; one head per group;
+    max_window 0 (flush every step); one group for all heads."""
+    H = 128 if G == 128 else 16
+    wl = W.Workload(name="edge", num_slots=9, nheads=H, ngroups=G, max_window=W_, npredicted=T,
+                    state_dtype=W.BF16, batch=6, T=T, steps=6, pad_row=True, ring_start_random=True,
+                    config_id=9)
+    run_pair(orc, wl)
+
+
+def test_bad_rows_set_error_bits_and_zero_outputs(orc):
+    wl = W.config("tiny", state_dtype=W.BF16)
+    gen = W.Generator(wl)
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    rows = np.nonzero(ids > 0)[0]
+    pnat[rows[0]] = wl.L - 1  # p + T > L after no flush (force = 0 flushes it: p + T > W)
+    pair = Pair(orc, wl, oc, ids, pnat)
+    inp = gen.step(0)
+    inp.accepted[rows[1]] = wl.T + 3  # bad accept count
+    pair.step(inp)
+    assert pair.oc.error_word[0] & api.ERRBIT_ACCEPT
+    # a step without the flush on an overfull row: y = 0, error bit, no cache change
+    p2 = pair.pnat.copy()
+    p2[rows[2]] = wl.L
+    gp = dev_of(p2, "cuda")
+    out = torch.full((inp.ntok, wl.nheads, 64), 0x3F80, dtype=torch.int16, device="cuda")
+    before = pair.gc.x_cache.clone()
+    api.rssm_step(pair.gc, dev_of(inp.x, "cuda"), dev_of(inp.dt, "cuda"), pair.gA, dev_of(inp.B, "cuda"),
+                  dev_of(inp.C, "cuda"), pair.gD, pair.gb, pair.gids, gp, wl.T, out, pair.scratch)
+    torch.cuda.synchronize()
+    r = rows[2]
+    assert not out[r * wl.T:(r + 1) * wl.T].any()
+    assert int(pair.gc.error_word.item()) & api.ERRBIT_PNAT
+    s = int(ids[r])
+    assert torch.equal(pair.gc.x_cache[s], before[s])
+
+
+def test_empty_batch_is_noop():
+    wl = W.config("tiny")
+    gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype)
+    z = torch.zeros(0, dtype=torch.int32, device="cuda")
+    f = torch.zeros(wl.nheads, dtype=torch.float32, device="cuda")
+    scratch = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    api.rssm_flush(gc, f, z, z, wl.T, scratch)
+    e = torch.zeros(16, dtype=torch.int16, device="cuda")
+    api.rssm_step(gc, e, f, f, e, e, f, f, z, z, wl.T, e, scratch)
+    api.rssm_accept(gc, z, z, z, wl.T)
+    torch.cuda.synchronize()
+    assert int(gc.error_word.item()) == 0
+
+
+def test_full_size_mamba2_decode_sampled_rows(orc):
+    """The benchmark's launch configuration (64 rows x 128 heads, bf16) on the
+    GPU; the oracle recomputes a sample of rows one by one."""
+    wl = W.config("mamba2_decode")
+    gen = W.Generator(wl)
+    oc_full, ids, pnat = oracle_cache(orc, wl, gen)
+    A, D, dtb = gen.params()
+    from tests.gpu_harness import gpu_cache_from
+
+    gc = gpu_cache_from(oc_full)
+    g = lambda a: dev_of(a, "cuda")  # noqa: E731
+    gA, gD, gb, gids, gp = g(A), g(D), g(dtb), g(ids), g(pnat)
+    scratch = api.alloc_scratch(gc, ids.size, wl.T)
+    sample = np.array([0, 17, 40, 63])
+    p_o = pnat.copy()
+    for k in range(24):
+        inp = gen.step(k)
+        out = torch.empty((inp.ntok, wl.nheads, 64), dtype=torch.int16, device="cuda")
+        api.rssm_flush(gc, gA, gids, gp, wl.T, scratch)
+        api.rssm_step(gc, g(inp.x), g(inp.dt), gA, g(inp.B), g(inp.C), gD, gb, gids, gp, wl.T, out, scratch)
+        api.rssm_accept(gc, gids, gp, g(inp.accepted), wl.T)
+        # oracle on the sampled rows only (rows are independent)
+        sid = ids[sample]
+        ps = p_o[sample].copy()
+        tok = (sample[:, None] * wl.T + np.arange(wl.T)[None]).reshape(-1)
+        oc_full.flush(A, sid, ps, wl.T)
+        yo = oc_full.step(inp.x[tok], inp.dt[tok], A, inp.B[tok], inp.C[tok], D, dtb, sid, ps, wl.T)
+        oc_full.accept(sid, ps, inp.accepted[sample], wl.T)
+        p_o[sample] = ps
+        torch.cuda.synchronize()
+        yg = out.cpu().numpy().view(np.uint16)[tok]
+        assert np.allclose(bf16_f32(yg), bf16_f32(yo), atol=2e-2, rtol=1e-2), k
+        assert np.array_equal(gp.cpu().numpy()[sample], ps)
+        gsid = torch.from_numpy(sid.astype(np.int64)).cuda()
+        for name in ("state", "x_cache", "B_cache", "dt_cache", "ring_start", "flush_epoch"):
+            o = getattr(oc_full, name)[sid]
+            assert np.array_equal(host_of(getattr(gc, name)[gsid], o), o), (k, name)
