@@ -100,11 +100,13 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   if (st != RSSM_OK) return st;
   if (batch < 0 || T < 1) return RSSM_ERR_INVALID_ARGUMENT;
   if (T > cache->npredicted || T > kMaxT) return RSSM_ERR_UNSUPPORTED;
+  a->batch = batch;
+  if (batch == 0) return RSSM_OK;  // nothing to do; pointers of empty tensors may be NULL
   if (!x || !dt || !A || !B || !C || !D || !dt_bias || !slot_idx || !pnat || !out || !scratch)
     return RSSM_ERR_INVALID_ARGUMENT;
   if (!aligned16(x) || !aligned16(B) || !aligned16(C) || !aligned16(out) || !aligned16(scratch))
     return RSSM_ERR_INVALID_ARGUMENT;
-  const size_t need = step_scratch_bytes(batch, cache->nheads, a->c.L, T);
+  const size_t need = step_scratch_bytes(batch, cache->nheads, cache->ngroups, a->c.L, T);
   if (scratch_bytes < need) return RSSM_ERR_SCRATCH_TOO_SMALL;
   a->x = static_cast<const uint16_t*>(x);
   a->dt = dt;
@@ -122,7 +124,9 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->KB = ring_pad(a->c.L);
   a->out = static_cast<uint16_t*>(out);
   a->rows = static_cast<RowRec*>(scratch);
-  a->coef = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch));
+  a->cf = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch));
+  a->coef = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch) +
+                                     step_cf_bytes(batch, cache->ngroups, T));
   return RSSM_OK;
 }
 
@@ -133,7 +137,7 @@ extern "C" {
 size_t rssm_scratch_bytes(const rssm_cache* cache, int32_t batch, int32_t T) {
   Cache c;
   if (check_cache(cache, &c) != RSSM_OK || batch < 0 || T < 1 || T > kMaxT) return 0;
-  const size_t f = flush_scratch_bytes(batch), s = step_scratch_bytes(batch, c.H, c.L, T);
+  const size_t f = flush_scratch_bytes(batch), s = step_scratch_bytes(batch, c.H, c.G, c.L, T);
   return f > s ? f : s;
 }
 

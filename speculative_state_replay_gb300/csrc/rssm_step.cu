@@ -23,11 +23,16 @@ namespace rssm {
 // ---------------------------------------------------------------------------
 // precompute
 // ---------------------------------------------------------------------------
+// swizzled 16-byte chunk index of a converted f32 C row: keeps the lanes of a
+// quarter warp of the readout on distinct bank groups for every state layout
+__host__ __device__ __forceinline__ int cswz(int m) { return m ^ ((m >> 3) & 3); }
+
 template <int TP>
 __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
-  __shared__ float Bf[kMaxL][kDstate + 1];
-  __shared__ float Cf[TP][kDstate + 1];
+  __shared__ float Bf[kMaxL][kDstate + 4];
+  __shared__ float Cf[TP][kDstate + 4];
   __shared__ float CB[TP][kMaxL];
+  __shared__ float dtl[16][kMaxL];  // live dt' of up to 16 heads of the group
   __shared__ int meta[6];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
@@ -58,8 +63,9 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
   __syncthreads();
   const int s = meta[0], r = meta[1], p = meta[2], Tb = meta[3], tok0 = meta[4];
   if (!meta[5] || Tb == 0) return;
-  const int K = p + Tb, L = c.L, H = c.H, G = c.G;
-  const uint16_t* bring = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
+  const int K = p + Tb, L = c.L, H = c.H, G = c.G, hpg = c.hpg;
+  uint16_t* bring = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
+  // independent loads first: B rows (live ring + new), C rows, live dt' of the group's heads
   for (int idx = tid; idx < K * (kDstate / 2); idx += 256) {
     const int k = idx >> 6, q = idx & 63;
     const uint16_t* src = k < p ? bring + ((r + k) % L) * kDstate
@@ -68,38 +74,65 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
     Bf[k][2 * q] = bf16lo(w);
     Bf[k][2 * q + 1] = bf16hi(w);
   }
-  for (int idx = tid; idx < Tb * (kDstate / 2); idx += 256) {
+  for (int idx = tid; idx < TP * (kDstate / 2); idx += 256) {
     const int t = idx >> 6, q = idx & 63;
-    const uint32_t w =
-        reinterpret_cast<const uint32_t*>(a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate)[q];
-    Cf[t][2 * q] = bf16lo(w);
-    Cf[t][2 * q + 1] = bf16hi(w);
+    float2 v = make_float2(0.0f, 0.0f);
+    if (t < Tb) {
+      const uint32_t w =
+          reinterpret_cast<const uint32_t*>(a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate)[q];
+      v = make_float2(bf16lo(w), bf16hi(w));
+    }
+    Cf[t][2 * q] = v.x;
+    Cf[t][2 * q + 1] = v.y;
   }
-  // append the new B rows after the live prefix
+  const int hl = hpg < 16 ? hpg : 16;
+  for (int idx = tid; idx < hl * p; idx += 256) {
+    const int hh = idx / p, k = idx % p;
+    dtl[hh][k] = c.dt_cache[static_cast<long long>(s) * c.dt_stride + static_cast<long long>(g * hpg + hh) * L +
+                            (r + k) % L];
+  }
+  // ring appends: the new B rows (once per group) and the new x rows of the group's heads
   for (int idx = tid; idx < Tb * 16; idx += 256) {
     const int t = idx >> 4, q = idx & 15;
     const uint4 v = reinterpret_cast<const uint4*>(a.B + (static_cast<long long>(tok0 + t) * G + g) * kDstate)[q];
-    reinterpret_cast<uint4*>(const_cast<uint16_t*>(bring) + ((r + p + t) % L) * kDstate)[q] = v;
+    reinterpret_cast<uint4*>(bring + ((r + p + t) % L) * kDstate)[q] = v;
+  }
+  for (int idx = tid; idx < Tb * hpg * 8; idx += 256) {
+    const int t = idx / (hpg * 8), rem = idx % (hpg * 8), hh = rem >> 3, q = rem & 7;
+    const int h = g * hpg + hh;
+    const uint4 v = reinterpret_cast<const uint4*>(a.x + (static_cast<long long>(tok0 + t) * H + h) * kDim)[q];
+    uint16_t* dst = c.x_cache + static_cast<long long>(s) * c.x_stride + (static_cast<long long>(h) * L + (r + p + t) % L) * kDim;
+    reinterpret_cast<uint4*>(dst)[q] = v;
   }
   __syncthreads();
-  for (int idx = tid; idx < Tb * K; idx += 256) {
-    const int t = idx / K, k = idx % K;
+  // C.B contraction, one warp per (t, k) pair, lanes over dstate
+  for (int pr = warp; pr < Tb * K; pr += 8) {
+    const int t = pr / K, k = pr % K;
     float v = 0.0f;
     if (k <= p + t) {
-#pragma unroll 8
-      for (int n = 0; n < kDstate; ++n) v = fmaf(Cf[t][n], Bf[k][n], v);
+#pragma unroll
+      for (int n = lane; n < kDstate; n += 32) v = fmaf(Cf[t][n], Bf[k][n], v);
+#pragma unroll
+      for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
     }
-    CB[t][k] = v;
+    if (lane == 0) CB[t][k] = v;
+  }
+  // the f32 C block for the readout, 16-byte chunks swizzled
+  float* cfg = a.cf + (static_cast<long long>(b) * G + g) * TP * kDstate;
+  for (int idx = tid; idx < TP * 32; idx += 256) {
+    const int t = idx >> 5, m = idx & 31;
+    const float4 v = make_float4(Cf[t][4 * m], Cf[t][4 * m + 1], Cf[t][4 * m + 2], Cf[t][4 * m + 3]);
+    *reinterpret_cast<float4*>(cfg + t * kDstate + cswz(m) * 4) = v;
   }
   __syncthreads();
   const int KB = a.KB;
-  for (int hh = warp; hh < c.hpg; hh += 8) {
-    const int h = g * c.hpg + hh;
+  for (int hh = warp; hh < hpg; hh += 8) {
+    const int h = g * hpg + hh;
     const float Ah = a.A[h], Dh = a.D[h];
     float* dtrow = c.dt_cache + static_cast<long long>(s) * c.dt_stride + static_cast<long long>(h) * L;
     float dtp = 0.0f;
     if (lane < p) {
-      dtp = dtrow[(r + lane) % L];
+      dtp = hh < 16 ? dtl[hh][lane] : dtrow[(r + lane) % L];
     } else if (lane < K) {
       const int t = lane - p;
       const float v = __fadd_rn(a.dt[static_cast<long long>(tok0 + t) * H + h], a.dt_bias[h]);
@@ -150,10 +183,8 @@ struct ReadMeta {
 struct ReadLayout {
   int ns, KB;
   uint32_t s0_bytes, scale_off, c_off, coef_off, x_off, stage_bytes;
-  uint32_t stages_off, cf_off, xf_off, total;
+  uint32_t stages_off, total;
 };
-
-constexpr int kXfStride = kDim + 4;  // padded f32 row of the converted x ring (bank spread)
 
 __host__ __device__ inline ReadLayout read_layout(int dtype, int L, int TP, int ns) {
   ReadLayout f;
@@ -165,22 +196,16 @@ __host__ __device__ inline ReadLayout read_layout(int dtype, int L, int TP, int 
   f.scale_off = o;
   if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
   f.c_off = o;
-  o += TP * kDstate * 2;
+  o += TP * kDstate * 4;
   f.coef_off = o;
   o += ((f.KB + 1) * TP * 4 + 15) & ~15;
   f.x_off = o;
   o += f.KB * kDim * 2;
   f.stage_bytes = (o + 127) & ~127u;
   f.stages_off = 512;
-  f.cf_off = f.stages_off + ns * f.stage_bytes;
-  f.xf_off = f.cf_off + 2 * TP * kDstate * 4;
-  f.total = f.xf_off + 2 * f.KB * kXfStride * 4;
+  f.total = f.stages_off + ns * f.stage_bytes;
   return f;
 }
-
-// swizzled 16-byte chunk index of the converted C rows: keeps the lanes of a
-// quarter warp on distinct bank groups for all three state layouts
-__device__ __forceinline__ int cswz(int m) { return m ^ ((m >> 3) & 3); }
 
 template <int DT>
 struct RowChunk;  // 16 bytes of one state row -> float pairs
@@ -244,15 +269,16 @@ struct RowChunk<RSSM_E4M3> {
   }
 };
 
+// 96 registers: two 9-warp CTAs then fit the per-SMSP register files
 template <int DT, int TP>
-__global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns) {
+__global__ void __maxnreg__(96) readout_kernel(StepArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Cache& c = a.c;
   const ReadLayout lay = read_layout(DT, c.L, TP, ns);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
-  constexpr int kEPC = 16 / esz;            // elements per 16-byte chunk
-  constexpr int kRowChunks = 16 / kEPC;     // chunks per lane per row (16 elements per lane)
+  constexpr int kEPC = 16 / esz;         // state elements per 16-byte chunk
+  constexpr int kRowChunks = 16 / kEPC;  // chunks per lane per row (16 columns per lane)
   constexpr int kRowBytes = kDstate * esz;
   const int H = c.H;
 
@@ -264,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 8;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 192);
   ReadMeta* meta = reinterpret_cast<ReadMeta*>(smem + 256);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -273,14 +298,13 @@ __global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], kConsumerWarps);
     }
-    *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   const int KB = lay.KB;
   if (warp == kConsumerWarps) {
-    // ---------------- producer warp ----------------
+    // ---------------- producer: one lane issues all bulk copies ----------------
     if (lane != 0) return;
     int cur_b = -1;
     RowRec rr = {};
@@ -301,28 +325,25 @@ __global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns
       }
       meta[st] = ReadMeta{b, h, rr.s, rr.r, rr.p, rr.Tb, rr.tok0, rr.flags};
       if (rr.flags && rr.Tb > 0) {
-        const int s = rr.s, r = rr.r, p = rr.p, Tb = rr.Tb, tok0 = rr.tok0, g = h / c.hpg;
+        const int s = rr.s, r = rr.r, K = rr.p + rr.Tb, g = h / c.hpg;
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
         const uint32_t coef_bytes = (KB + 1) * TP * 4;
-        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + Tb * kDstate * 2 + coef_bytes + (p + Tb) * kDim * 2;
+        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + TP * kDstate * 4 + coef_bytes + K * kDim * 2;
         mbar_expect_tx(&full[st], bytes);
         bulk_g2s(sb, static_cast<const uint8_t*>(c.state) +
                          (static_cast<long long>(s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz,
                  lay.s0_bytes, &full[st]);
         if (k8bit)
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
-        for (int t = 0; t < Tb; ++t)
-          bulk_g2s(sb + lay.c_off + t * kDstate * 2, a.C + (static_cast<long long>(tok0 + t) * c.G + g) * kDstate,
-                   kDstate * 2, &full[st]);
+        bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * TP * kDstate, TP * kDstate * 4,
+                 &full[st]);
         bulk_g2s(sb + lay.coef_off, a.coef + (static_cast<long long>(b) * H + h) * (KB + 1) * TP, coef_bytes,
                  &full[st]);
+        // live ring + the new rows the precompute appended: logical 0..K-1
         const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * c.L * kDim;
-        const int n1 = min(p, c.L - r);
-        if (n1 > 0) bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
-        if (p > n1) bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (p - n1) * kDim * 2, &full[st]);
-        for (int t = 0; t < Tb; ++t)
-          bulk_g2s(sb + lay.x_off + (p + t) * kDim * 2, a.x + (static_cast<long long>(tok0 + t) * H + h) * kDim,
-                   kDim * 2, &full[st]);
+        const int n1 = min(K, c.L - r);
+        bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
+        if (K > n1) bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (K - n1) * kDim * 2, &full[st]);
       }
       mbar_arrive(&full[st]);
       issued = i + 1;
@@ -334,48 +355,19 @@ __global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns
     return;
   }
 
-  // ---------------- consumer warps ----------------
+  // ---------------- consumer warps (independent; stage barriers only) ----------------
   const int rg = lane >> 3, j = lane & 7;
   const int rho0 = 8 * warp + 2 * rg;
-  float* cfb = reinterpret_cast<float*>(smem + lay.cf_off);
-  float* xfb = reinterpret_cast<float*>(smem + lay.xf_off);
-  int nvalid = 0;
   for (int i = 0; i < nu; ++i) {
     const int st = i % ns;
     const uint32_t ph = (i / ns) & 1;
     if (!mbar_wait(&full[st], ph)) {
-      *abort_flag = 1;
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+      return;
     }
     const ReadMeta m = meta[st];
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
-    const bool valid = m.flags && m.Tb > 0;
-    const int K = m.p + m.Tb;
-    const int vb = nvalid & 1;
-    float* Cf = cfb + vb * TP * kDstate;
-    float* xf = xfb + vb * KB * kXfStride;
-    if (valid) {
-      const uint32_t* cs = reinterpret_cast<const uint32_t*>(sb + lay.c_off);
-      for (int idx = tid; idx < TP * (kDstate / 2); idx += kConsumerThreads) {
-        const int t = idx >> 6, pr = idx & 63, n = 2 * pr;
-        float2 v = make_float2(0.0f, 0.0f);
-        if (t < m.Tb) {
-          const uint32_t w = cs[t * 64 + pr];
-          v = make_float2(bf16lo(w), bf16hi(w));
-        }
-        const int mch = n >> 2;
-        *reinterpret_cast<float2*>(Cf + t * kDstate + cswz(mch) * 4 + (n & 3)) = v;
-      }
-      const uint32_t* xs = reinterpret_cast<const uint32_t*>(sb + lay.x_off);
-      for (int idx = tid; idx < K * (kDim / 2); idx += kConsumerThreads) {
-        const int k = idx >> 5, dp = idx & 31;
-        const uint32_t w = xs[idx];
-        *reinterpret_cast<float2*>(xf + k * kXfStride + 2 * dp) = make_float2(bf16lo(w), bf16hi(w));
-      }
-    }
-    consumer_sync();
-    if (*abort_flag) return;
-    if (!valid) {
+    if (!(m.flags && m.Tb > 0)) {
       // inactive or rejected row: zero outputs, no cache update
       for (int idx = tid; idx < m.Tb * (kDim / 2); idx += kConsumerThreads) {
         const int t = idx >> 5, dp = idx & 31;
@@ -385,14 +377,14 @@ __global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns
       if (lane == 0) mbar_arrive(&empty[st]);
       continue;
     }
-    ++nvalid;
+    const int K = m.p + m.Tb;
     // ---- S0 . C_t over this lane's 16 columns of rows rho0, rho0 + 1 ----
     float2 acc[2][TP];
 #pragma unroll
-    for (int rr = 0; rr < 2; ++rr)
+    for (int q2 = 0; q2 < 2; ++q2)
 #pragma unroll
-      for (int t = 0; t < TP; ++t) acc[rr][t] = make_float2(0.0f, 0.0f);
-    const float4* Cf4 = reinterpret_cast<const float4*>(Cf);
+      for (int t = 0; t < TP; ++t) acc[q2][t] = make_float2(0.0f, 0.0f);
+    const float4* Cf4 = reinterpret_cast<const float4*>(sb + lay.c_off);
 #pragma unroll
     for (int ch = 0; ch < kRowChunks; ++ch) {
       const int q = j + 8 * ch;  // 16-byte chunk within the row
@@ -430,32 +422,26 @@ __global__ void __launch_bounds__(kThreads, 1) readout_kernel(StepArgs a, int ns
       vals[t] = (acc[0][t].x + acc[0][t].y) * (dct * sc0);
       vals[TP + t] = (acc[1][t].x + acc[1][t].y) * (dct * sc1);
     }
-    // ---- ring terms: sum_k coef[k][t] x_k[d], k = j, j+8, ... ----
+    // ---- ring terms: sum_k coef[k][t] x_k[d], k = j, j+8, ... (x rows in bf16) ----
+    const uint32_t* xs = reinterpret_cast<const uint32_t*>(sb + lay.x_off);
     for (int k = j; k < K; k += 8) {
-      const float2 xk = *reinterpret_cast<const float2*>(xf + k * kXfStride + rho0);
+      const uint32_t xw = xs[k * (kDim / 2) + (rho0 >> 1)];
+      const float x0 = bf16lo(xw), x1 = bf16hi(xw);
 #pragma unroll
       for (int t4 = 0; t4 < TP; t4 += 4) {
         const float4 cv = *reinterpret_cast<const float4*>(coef + k * TP + t4);
-        vals[t4 + 0] = fmaf(cv.x, xk.x, vals[t4 + 0]);
-        vals[t4 + 1] = fmaf(cv.y, xk.x, vals[t4 + 1]);
-        vals[t4 + 2] = fmaf(cv.z, xk.x, vals[t4 + 2]);
-        vals[t4 + 3] = fmaf(cv.w, xk.x, vals[t4 + 3]);
-        vals[TP + t4 + 0] = fmaf(cv.x, xk.y, vals[TP + t4 + 0]);
-        vals[TP + t4 + 1] = fmaf(cv.y, xk.y, vals[TP + t4 + 1]);
-        vals[TP + t4 + 2] = fmaf(cv.z, xk.y, vals[TP + t4 + 2]);
-        vals[TP + t4 + 3] = fmaf(cv.w, xk.y, vals[TP + t4 + 3]);
+        vals[t4 + 0] = fmaf(cv.x, x0, vals[t4 + 0]);
+        vals[t4 + 1] = fmaf(cv.y, x0, vals[t4 + 1]);
+        vals[t4 + 2] = fmaf(cv.z, x0, vals[t4 + 2]);
+        vals[t4 + 3] = fmaf(cv.w, x0, vals[t4 + 3]);
+        vals[TP + t4 + 0] = fmaf(cv.x, x1, vals[TP + t4 + 0]);
+        vals[TP + t4 + 1] = fmaf(cv.y, x1, vals[TP + t4 + 1]);
+        vals[TP + t4 + 2] = fmaf(cv.z, x1, vals[TP + t4 + 2]);
+        vals[TP + t4 + 3] = fmaf(cv.w, x1, vals[TP + t4 + 3]);
       }
     }
-    // ---- append the new x rows after the live prefix ----
-    if (tid < m.Tb * 8) {
-      const int t = tid >> 3, qq = tid & 7;
-      const uint4 v = *reinterpret_cast<const uint4*>(sb + lay.x_off + (m.p + t) * kDim * 2 + qq * 16);
-      uint16_t* dst = c.x_cache + static_cast<long long>(m.s) * c.x_stride +
-                      (static_cast<long long>(m.h) * c.L + (m.r + m.p + t) % c.L) * kDim;
-      reinterpret_cast<uint4*>(dst)[qq] = v;
-    }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);  // stage fully read
+    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
     // ---- transpose-reduce the 2*TP partial sums over the 8 lanes of a row pair ----
     constexpr int V = 2 * TP;
 #pragma unroll
@@ -501,16 +487,19 @@ int launch_precompute(const StepArgs& a, void* stream) {
 template <int DT, int TP>
 static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 6
-  int ns = 6, ctas = 2;
+  int ns = 8, ctas = 2;
   for (; ns >= 3; --ns)
     if (read_layout(DT, a.c.L, TP, ns).total <= 113 * 1024) break;
   if (ns < 3) {
     ctas = 1;
-    for (ns = 6; ns > 2; --ns)
+    for (ns = 8; ns > 2; --ns)
       if (read_layout(DT, a.c.L, TP, ns).total <= 225 * 1024) break;
   }
   const ReadLayout lay = read_layout(DT, a.c.L, TP, ns);
   cudaError_t e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int occ = 0;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, readout_kernel<DT, TP>, kThreads, lay.total);
