@@ -9,8 +9,9 @@ checkpoints, window 16, T = 4 drafts.
                     [--config NAME] [--force-flush] [--no-e2e] [--no-cpu-baseline]
 
 Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
-on the launching stream; a 1 GiB buffer is written between steps (outside the
-events) so every step starts with a cold L2.  Under torchrun (N > 1) every
+on the launching stream; between steps (outside the events) a 1 GiB buffer is
+written and a 512 MiB buffer read, so every step starts with a cold L2 that
+holds no dirty lines.  Under torchrun (N > 1) every
 rank runs an independent replica (weak scaling, no data-path collective);
 the time is the max over ranks.  Prints one JSON line on rank 0.
 """
@@ -251,6 +252,14 @@ def run_gpu(args, rank, ws, local):
     scr_flush = api.alloc_scratch(gc, ids.size, wl.T)
     scr_step = api.alloc_scratch(gc, ids.size, wl.T)
     l2 = torch.empty(1 << 30, dtype=torch.uint8, device=dev)
+    l2r = torch.ones(1 << 27, dtype=torch.int32, device=dev)
+
+    def cold_l2():
+        """Write 1 GiB, then read 512 MiB: afterwards the L2 holds neither step
+        data nor dirty lines whose write-back the next step would pay for."""
+        l2.zero_()
+        l2r.max()
+
     force = 1 if args.force_flush else 0
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     cu = buf["cu"]
@@ -326,7 +335,7 @@ def run_gpu(args, rank, ws, local):
 
     for k in range(args.warmup):
         load_inputs(dev_inp[k])
-        l2.zero_()
+        cold_l2()
         one_step()
     torch.cuda.synchronize()
 
@@ -336,7 +345,7 @@ def run_gpu(args, rank, ws, local):
     clocks = ClockSampler(torch.cuda.current_device())
     for k in range(args.warmup, nsteps):
         load_inputs(dev_inp[k])
-        l2.zero_()
+        cold_l2()
         e0 = ev()
         e0.record(stream)
         e_f, e_r0, e_r1 = one_step()
@@ -373,7 +382,7 @@ def run_gpu(args, rank, ws, local):
         e2e_ms, e2e_units, h2d, d2h = [], 0, 0, 0
         for k in range(args.warmup, nsteps):
             hi = hin[k]
-            l2.zero_()
+            cold_l2()
             e0 = ev()
             e0.record(stream)
             load_inputs(hi, non_blocking=True)
@@ -399,7 +408,7 @@ def run_gpu(args, rank, ws, local):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
-        "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB buffer written between steps",
+        "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB written then 512 MiB read between steps (cold, clean L2)",
                        launch="one CUDA graph per launch group, replayed per step",
                        force_flush=bool(args.force_flush)),
         "roofline": {"bound": "hbm", "kernel": "readout_kernel", "achieved": achieved, "peak": peak,
