@@ -219,6 +219,32 @@ rssm_status rssm_eval_spec_math(const float *in, float *out_exp, float *out_soft
 
 const char *rssm_status_string(rssm_status status);
 
+/*
+ * rssm_step without a caller scratch buffer.  The pages have no counterpart
+ * to this entry point; it exists for callers that cannot allocate device
+ * memory -- an engine whose allocator has already reserved the GPU and hands
+ * out no per-call workspace, or a C/FFI host with no device allocator.
+ *
+ * Same arguments, semantics and results as rssm_step, minus scratch and
+ * scratch_bytes: the scratch is a fixed array of
+ * RSSM_STEP_STATIC_SCRATCH_BYTES bytes compiled into the library, present on
+ * every GPU that loads it until the process exits.  A step whose
+ * rssm_scratch_bytes() exceeds that size returns RSSM_ERR_SCRATCH_TOO_SMALL
+ * and launches nothing.  The call allocates and frees nothing.
+ *  - The first call on a device looks up the array's device address (once
+ *    per device, with that device current); make that first call before any
+ *    stream capture.
+ *  - Every call on a device shares the one array and leaves its contents
+ *    behind; nothing in it needs to start at zero.  Calls whose kernels
+ *    overlap on the GPU (different streams without ordering) race on the
+ *    array; order them.
+ */
+#define RSSM_STEP_STATIC_SCRATCH_BYTES (16u << 20)
+rssm_status rssm_step_static_scratch(const rssm_cache *cache, const void *x, const float *dt, const float *A,
+                                     const void *B, const void *C, const float *D, const float *dt_bias,
+                                     const int32_t *slot_idx, const int32_t *pnat, const int32_t *cu_seqlens,
+                                     int32_t batch, int32_t T, void *out, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

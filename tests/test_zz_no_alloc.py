@@ -1,0 +1,105 @@
+"""rssm_step_static_scratch: the step for callers that cannot allocate.
+
+Engines whose allocator owns all device memory, or FFI hosts without a device
+allocator, cannot hand rssm_step a scratch buffer; this entry point uses an
+array compiled into the library instead.  Called through the C ABI, it must
+give the same outputs and cache updates as rssm_step with a caller scratch,
+on consecutive calls (the array keeps the previous call's contents), and must
+refuse a step larger than the array.  Needs a GPU; collected last.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from speculative_state_replay_gb300 import _lib, api
+from speculative_state_replay_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+Y_ATOL, Y_RTOL = 2e-2, 1e-2
+
+
+def _entry():
+    from speculative_state_replay_gb300 import build
+
+    build.build()
+    lib = _lib.load()
+    f = lib.rssm_step_static_scratch
+    vp, i32 = ctypes.c_void_p, ctypes.c_int32
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.POINTER(_lib.RssmCacheStruct)] + [vp] * 10 + [i32, i32, vp, vp]
+    return f
+
+
+def _cache(wl, gen, dev):
+    gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
+                       device=dev)
+    ids = gen.slot_idx()
+    act = ids[ids > 0]
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    api.rssm_init_state(gc, t(gen.init_states(0, act.size)), t(act.astype(np.int32)))
+    return gc, ids
+
+
+def _bf16(t):
+    return (t.cpu().numpy().view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+
+
+def test_static_scratch_step_matches_rssm_step_twice():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    f = _entry()
+    dev = torch.device("cuda:0")
+    wl = W.config("mamba2_decode", batch=16)
+    gen = W.Generator(wl)
+    A, D, dtb = gen.params()
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
+    gA, gD, gb = t(A), t(D), t(dtb)
+    ref, ids = _cache(wl, gen, dev)
+    sut, _ = _cache(wl, gen, dev)
+    gids = t(ids)
+    p_ref = torch.zeros(ids.size, dtype=torch.int32, device=dev)
+    p_sut = p_ref.clone()
+    scratch = api.alloc_scratch(ref, ids.size, wl.T)
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    ptr = lambda x: ctypes.c_void_p(x.data_ptr())  # noqa: E731
+    for k in range(2):
+        inp = gen.step(k)
+        x, dt, B, C = t(inp.x.view(np.int16)), t(inp.dt), t(inp.B.view(np.int16)), t(inp.C.view(np.int16))
+        y_ref = torch.full((inp.ntok, wl.nheads, 64), 0x7FC0, dtype=torch.int16, device=dev)
+        y_sut = y_ref.clone()
+        api.rssm_step(ref, x, dt, gA, B, C, gD, gb, gids, p_ref, wl.T, y_ref, scratch)
+        rc = f(sut.struct(), ptr(x), ptr(dt), ptr(gA), ptr(B), ptr(C), ptr(gD), ptr(gb), ptr(gids), ptr(p_sut),
+               None, ids.size, wl.T, ptr(y_sut), stream)
+        assert rc == 0
+        torch.cuda.synchronize()
+        a, b = _bf16(y_sut), _bf16(y_ref)
+        assert np.all(np.abs(a - b) <= Y_ATOL + Y_RTOL * np.abs(b)), k
+        for name in ("x_cache", "B_cache", "dt_cache", "state", "ring_start", "error_word"):
+            assert torch.equal(getattr(sut, name), getattr(ref, name)), (k, name)
+        acc = t(inp.accepted)
+        api.rssm_accept(ref, gids, p_ref, acc, wl.T)
+        api.rssm_accept(sut, gids, p_sut, acc, wl.T)
+    torch.cuda.synchronize()
+    assert torch.equal(p_ref, p_sut)
+
+
+def test_static_scratch_refuses_steps_larger_than_the_array():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    f = _entry()
+    dev = torch.device("cuda:0")
+    wl = W.config("large_batch", batch=512, num_slots=2)  # needs ~43 MB of scratch
+    c = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
+                      device=dev)
+    assert api.rssm_scratch_bytes(c, wl.batch, wl.T) > (16 << 20)
+    buf = torch.zeros(1 << 20, dtype=torch.int32, device=dev)
+    p = ctypes.c_void_p(buf.data_ptr())
+    out = torch.full((8,), 7, dtype=torch.int32, device=dev)
+    rc = f(c.struct(), p, p, p, p, p, p, p, p, p, None, wl.batch, wl.T, ctypes.c_void_p(out.data_ptr()),
+           ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert rc == 3  # RSSM_ERR_SCRATCH_TOO_SMALL, nothing launched
+    torch.cuda.synchronize()
+    assert (out == 7).all()
