@@ -81,7 +81,7 @@ struct StepArgs {
   int KB;  // ring rows padded to a multiple of 4
   uint16_t* out;
   RowRec* rows;  // scratch [batch]
-  float* cf;     // scratch [batch][G][TP][128]: C rows as f32, chunk-swizzled for the readout
+  uint16_t* cf;  // scratch [batch][G][8][128]: C rows in the readout's MMA operand type
   float* coef;   // scratch [batch][H][KB+1][TP]
 };
 
@@ -101,7 +101,8 @@ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 inline size_t flush_scratch_bytes(int batch) { return 256 + align_up(sizeof(FlushRec) * (size_t)batch, 256); }
 inline size_t step_rows_bytes(int batch) { return align_up(sizeof(RowRec) * (size_t)batch, 256); }
 inline size_t step_cf_bytes(int batch, int G, int T) {
-  return align_up((size_t)batch * G * t_pad(T) * 128 * sizeof(float), 256);
+  (void)T;
+  return align_up((size_t)batch * G * 8 * 128 * 2, 256);
 }
 inline size_t step_scratch_bytes(int batch, int H, int G, int L, int T) {
   const size_t blk = (size_t)(ring_pad(L) + 1) * t_pad(T) * sizeof(float);

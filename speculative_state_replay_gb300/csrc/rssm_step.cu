@@ -11,10 +11,14 @@
 //   readout_kernel  persistent, one (row, head) unit at a time:
 //           y_t[d] = decay[t] (S0[d] . C_t) + sum_k coef[k][t] x_k[d]
 //       streaming S0 once through a multi-stage shared-memory ring filled by
-//       1-D bulk copies (producer warp + mbarriers); 8 consumer warps, 8 lanes
-//       per state row pair, packed f32x2 FMAs over dstate, warp-shuffle
-//       transpose-reduction over the 8 lanes.  Appends x.
+//       TMA (swizzled tensor boxes for S0, 1-D bulk copies for the rest) from
+//       a producer warp with mbarriers; 8 consumer warps contract on the
+//       tensor cores (mma.sync m16n8k16, f32 accumulation).
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
+
+#include <mutex>
 
 #include "rssm_device.cuh"
 
@@ -23,10 +27,6 @@ namespace rssm {
 // ---------------------------------------------------------------------------
 // precompute
 // ---------------------------------------------------------------------------
-// swizzled 16-byte chunk index of a converted f32 C row: keeps the lanes of a
-// quarter warp of the readout on distinct bank groups for every state layout
-__host__ __device__ __forceinline__ int cswz(int m) { return m ^ ((m >> 3) & 3); }
-
 template <int TP>
 __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
   __shared__ float Bf[kMaxL][kDstate + 4];
@@ -117,12 +117,26 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
     }
     if (lane == 0) CB[t][k] = v;
   }
-  // the f32 C block for the readout, 16-byte chunks swizzled
-  float* cfg = a.cf + (static_cast<long long>(b) * G + g) * TP * kDstate;
-  for (int idx = tid; idx < TP * 32; idx += 256) {
-    const int t = idx >> 5, m = idx & 31;
-    const float4 v = make_float4(Cf[t][4 * m], Cf[t][4 * m + 1], Cf[t][4 * m + 2], Cf[t][4 * m + 3]);
-    *reinterpret_cast<float4*>(cfg + t * kDstate + cswz(m) * 4) = v;
+  // the C block for the readout's tensor-core contraction: [8][128] in the
+  // MMA operand type (bf16 for f32/bf16 checkpoints, fp16 otherwise), rows
+  // t >= T_b zero, 32-byte quads of row t rotated by t
+  uint16_t* cbg = a.cf + (static_cast<long long>(b) * G + g) * 8 * kDstate;
+  const bool c_f16 = c.dtype == RSSM_F16 || c.dtype == RSSM_I8 || c.dtype == RSSM_E4M3;
+  for (int idx = tid; idx < 8 * (kDstate / 2); idx += 256) {
+    const int t = idx >> 6, q = idx & 63;
+    const float v0 = t < TP ? Cf[t][2 * q] : 0.0f, v1 = t < TP ? Cf[t][2 * q + 1] : 0.0f;
+    uint32_t w;
+    if (c_f16) {
+      const __half2 h = __floats2half2_rn(v0, v1);
+      w = *reinterpret_cast<const uint32_t*>(&h);
+    } else {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
+      w = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    // 32-byte quad j = n/16 of row t stored at quad j ^ t: the readout's
+    // per-row fragment loads then fall on distinct banks
+    const int n = 2 * q;
+    reinterpret_cast<uint32_t*>(cbg)[(t * kDstate + 16 * (((n >> 4) ^ t) & 7) + (n & 15)) >> 1] = w;
   }
   __syncthreads();
   const int KB = a.KB;
@@ -176,6 +190,17 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
 // ---------------------------------------------------------------------------
 // readout
 // ---------------------------------------------------------------------------
+// Per (row, head) unit the readout is two small dense contractions, done on
+// the tensor cores with mma.sync m16n8k16 (f32 accumulation):
+//     Y^T[t][d] = sum_n Cblk[t][n] S0[d][n]        (M = t, N = d, K = dstate)
+//     R^T[t][d] = sum_k coef[k][t] x_k[d]           (K = ring rows, coef split
+//                                                    into bf16 hi + lo)
+//     y_t[d]    = decay_t scale_d Y^T[t][d] + R^T[t][d]
+// Warp w owns the 8 state rows d = 8w..8w+7 (one n8 tile).  K is taken in a
+// permuted order inside each 16-wide step (physical 4c..4c+3 <-> logical
+// 2c, 2c+1, 2c+8, 2c+9 for lane group c), so every operand fragment is one
+// 64-bit shared load; the sum over k is unchanged.  S0 arrives by TMA tensor
+// copies with the 128-byte swizzle, which keeps those loads conflict-free.
 struct ReadMeta {
   int b, h, s, r, p, Tb, tok0, flags;
 };
@@ -191,95 +216,110 @@ __host__ __device__ inline ReadLayout read_layout(int dtype, int L, int TP, int 
   f.ns = ns;
   f.KB = (L + 3) & ~3;
   const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
-  f.s0_bytes = kHeadElems * esz;
+  f.s0_bytes = kHeadElems * esz;  // esz boxes of 64 rows x 128 bytes
   uint32_t o = f.s0_bytes;
   f.scale_off = o;
   if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
   f.c_off = o;
-  o += TP * kDstate * 4;
+  o += 8 * kDstate * 2;
   f.coef_off = o;
   o += ((f.KB + 1) * TP * 4 + 15) & ~15;
   f.x_off = o;
   o += f.KB * kDim * 2;
-  f.stage_bytes = (o + 127) & ~127u;
-  f.stages_off = 512;
-  f.total = f.stages_off + ns * f.stage_bytes;
+  f.stage_bytes = (o + 1023) & ~1023u;  // the swizzled boxes need 1024-byte alignment
+  f.stages_off = 1024;                  // barriers and per-stage metadata
+  f.total = f.stages_off + ns * f.stage_bytes + 1024;  // + slack to align the base
   return f;
 }
 
-template <int DT>
-struct RowChunk;  // 16 bytes of one state row -> float pairs
-
-template <>
-struct RowChunk<RSSM_F32> {
-  static constexpr int kPairs = 2;
-  __device__ __forceinline__ static void get(const uint4& q, float2 (&v)[2]) {
-    v[0] = make_float2(__uint_as_float(q.x), __uint_as_float(q.y));
-    v[1] = make_float2(__uint_as_float(q.z), __uint_as_float(q.w));
-  }
-};
-template <>
-struct RowChunk<RSSM_BF16> {
-  static constexpr int kPairs = 4;
-  __device__ __forceinline__ static void get(const uint4& q, float2 (&v)[4]) {
-    v[0] = make_float2(bf16lo(q.x), bf16hi(q.x));
-    v[1] = make_float2(bf16lo(q.y), bf16hi(q.y));
-    v[2] = make_float2(bf16lo(q.z), bf16hi(q.z));
-    v[3] = make_float2(bf16lo(q.w), bf16hi(q.w));
-  }
-};
-template <>
-struct RowChunk<RSSM_F16> {
-  static constexpr int kPairs = 4;
-  __device__ __forceinline__ static void get(const uint4& q, float2 (&v)[4]) {
-    v[0] = h2f2(q.x);
-    v[1] = h2f2(q.y);
-    v[2] = h2f2(q.z);
-    v[3] = h2f2(q.w);
-  }
-};
-__device__ __forceinline__ float i8f(uint32_t x, int k) {
-  // byte k of x (sign bit flipped) placed under exponent 2^23, minus 2^23 + 128
-  return __uint_as_float(__byte_perm(x, 0x4B000000u, k | (4 << 4) | (5 << 8) | (7 << 12))) - 8388736.0f;
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(smem_addr(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+      : "memory");
 }
-template <>
-struct RowChunk<RSSM_I8> {
-  static constexpr int kPairs = 8;
-  __device__ __forceinline__ static void get(const uint4& q, float2 (&v)[8]) {
-    const uint32_t w[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      v[2 * i] = make_float2(i8f(w[i], 0), i8f(w[i], 1));
-      v[2 * i + 1] = make_float2(i8f(w[i], 2), i8f(w[i], 3));
-    }
-  }
-};
-template <>
-struct RowChunk<RSSM_E4M3> {
-  static constexpr int kPairs = 8;
-  __device__ __forceinline__ static void get(const uint4& q, float2 (&v)[8]) {
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half2_raw lo = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] & 0xffffu), __NV_E4M3);
-      const __half2_raw hi = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w[i] >> 16), __NV_E4M3);
-      v[2 * i] = __half22float2(__half2(lo));
-      v[2 * i + 1] = __half22float2(__half2(hi));
-    }
-  }
-};
 
-// 96 registers: two 9-warp CTAs then fit the per-SMSP register files
+__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// byte offset of (row d, byte k) inside one 64-row x 128-byte swizzled box
+__device__ __forceinline__ uint32_t swz(int d, int kbyte) {
+  return static_cast<uint32_t>(d * 128 + ((((kbyte >> 4) ^ d) & 7) << 4) + (kbyte & 15));
+}
+
+// S0 . C over dstate for state rows d (lane's B column) of this warp
+template <int DT>
+__device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint16_t* cblk, int d, int g, int c,
+                                         float (&acc)[4]) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const uint2 av = *reinterpret_cast<const uint2*>(cblk + g * kDstate + 16 * ((ks ^ g) & 7) + 4 * c);
+    if constexpr (DT == RSSM_BF16 || DT == RSSM_F16) {
+      const int kb = (ks * 16 + 4 * c) * 2;  // byte within the 256-byte row
+      const uint2 bv = *reinterpret_cast<const uint2*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
+      if constexpr (DT == RSSM_BF16)
+        mma_bf16(acc, av.x, av.y, bv.x, bv.y);
+      else
+        mma_f16(acc, av.x, av.y, bv.x, bv.y);
+    } else if constexpr (DT == RSSM_F32) {
+      const int kb = (ks * 16 + 4 * c) * 4;
+      const float4 f = *reinterpret_cast<const float4*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
+      const uint32_t h01 = pack_bf16(f.x, f.y), h23 = pack_bf16(f.z, f.w);
+      const uint32_t l01 = pack_bf16(f.x - bf16_lo_f(h01), f.y - bf16_hi_f(h01));
+      const uint32_t l23 = pack_bf16(f.z - bf16_lo_f(h23), f.w - bf16_hi_f(h23));
+      mma_bf16(acc, av.x, av.y, h01, h23);
+      mma_bf16(acc, av.x, av.y, l01, l23);
+    } else {
+      const uint32_t w = *reinterpret_cast<const uint32_t*>(s0 + swz(d, ks * 16 + 4 * c));
+      uint32_t b0, b1;
+      if constexpr (DT == RSSM_I8) {
+        // int8 code q as fp16: (1024 + (q + 128)) - 1152, exact
+        const uint32_t u = w ^ 0x80808080u;
+        const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140), p23 = __byte_perm(u, 0x64646464u, 0x4342);
+        const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
+        const __half2 h01 = __hsub2(*reinterpret_cast<const __half2*>(&p01), off);
+        const __half2 h23 = __hsub2(*reinterpret_cast<const __half2*>(&p23), off);
+        b0 = *reinterpret_cast<const uint32_t*>(&h01);
+        b1 = *reinterpret_cast<const uint32_t*>(&h23);
+      } else {
+        const __half2_raw r01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
+        const __half2_raw r23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
+        b0 = static_cast<uint32_t>(r01.x) | (static_cast<uint32_t>(r01.y) << 16);
+        b1 = static_cast<uint32_t>(r23.x) | (static_cast<uint32_t>(r23.y) << 16);
+      }
+      mma_f16(acc, av.x, av.y, b0, b1);
+    }
+  }
+}
+
 template <int DT, int TP>
-__global__ void __maxnreg__(96) readout_kernel(StepArgs a, int ns) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Cache& c = a.c;
   const ReadLayout lay = read_layout(DT, c.L, TP, ns);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
-  constexpr int kEPC = 16 / esz;         // state elements per 16-byte chunk
-  constexpr int kRowChunks = 16 / kEPC;  // chunks per lane per row (16 columns per lane)
-  constexpr int kRowBytes = kDstate * esz;
   const int H = c.H;
 
   const long long units = static_cast<long long>(a.batch) * H;
@@ -304,7 +344,7 @@ __global__ void __maxnreg__(96) readout_kernel(StepArgs a, int ns) {
 
   const int KB = lay.KB;
   if (warp == kConsumerWarps) {
-    // ---------------- producer: one lane issues all bulk copies ----------------
+    // ---------------- producer: one lane issues all copies ----------------
     if (lane != 0) return;
     int cur_b = -1;
     RowRec rr = {};
@@ -328,14 +368,13 @@ __global__ void __maxnreg__(96) readout_kernel(StepArgs a, int ns) {
         const int s = rr.s, r = rr.r, K = rr.p + rr.Tb, g = h / c.hpg;
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
         const uint32_t coef_bytes = (KB + 1) * TP * 4;
-        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + TP * kDstate * 4 + coef_bytes + K * kDim * 2;
+        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + 8 * kDstate * 2 + coef_bytes + K * kDim * 2;
         mbar_expect_tx(&full[st], bytes);
-        bulk_g2s(sb, static_cast<const uint8_t*>(c.state) +
-                         (static_cast<long long>(s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz,
-                 lay.s0_bytes, &full[st]);
+#pragma unroll
+        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
         if (k8bit)
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
-        bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * TP * kDstate, TP * kDstate * 4,
+        bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
                  &full[st]);
         bulk_g2s(sb + lay.coef_off, a.coef + (static_cast<long long>(b) * H + h) * (KB + 1) * TP, coef_bytes,
                  &full[st]);
@@ -355,9 +394,10 @@ __global__ void __maxnreg__(96) readout_kernel(StepArgs a, int ns) {
     return;
   }
 
-  // ---------------- consumer warps (independent; stage barriers only) ----------------
-  const int rg = lane >> 3, j = lane & 7;
-  const int rho0 = 8 * warp + 2 * rg;
+  // ---------------- consumer warps: state rows 8*warp .. 8*warp+7 ----------------
+  const int g = lane >> 2, cq = lane & 3;
+  const int d = 8 * warp + g;        // B column (row of S0) this lane loads
+  const int dout = 8 * warp + 2 * cq;  // output rows this lane writes (dout, dout + 1)
   for (int i = 0; i < nu; ++i) {
     const int st = i % ns;
     const uint32_t ph = (i / ns) & 1;
@@ -369,104 +409,56 @@ __global__ void __maxnreg__(96) readout_kernel(StepArgs a, int ns) {
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
     if (!(m.flags && m.Tb > 0)) {
       // inactive or rejected row: zero outputs, no cache update
-      for (int idx = tid; idx < m.Tb * (kDim / 2); idx += kConsumerThreads) {
-        const int t = idx >> 5, dp = idx & 31;
-        reinterpret_cast<uint32_t*>(a.out + (static_cast<long long>(m.tok0 + t) * H + m.h) * kDim)[dp] = 0u;
+      for (int idx = lane; idx < m.Tb * 4; idx += 32) {
+        const int t = idx >> 2, q = idx & 3;
+        *reinterpret_cast<uint32_t*>(a.out + (static_cast<long long>(m.tok0 + t) * H + m.h) * kDim + 8 * warp +
+                                     2 * q) = 0u;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
       continue;
     }
     const int K = m.p + m.Tb;
-    // ---- S0 . C_t over this lane's 16 columns of rows rho0, rho0 + 1 ----
-    float2 acc[2][TP];
+    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    s0_dot_c<DT>(sb, reinterpret_cast<const uint16_t*>(sb + lay.c_off), d, g, cq, acc);
+    // ring terms: sum_k coef[k][t] x_k[d]
+    const float* coef = reinterpret_cast<const float*>(sb + lay.coef_off);
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
+    float accr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int q2 = 0; q2 < 2; ++q2)
+    for (int kb = 0; kb < 2; ++kb) {
+      if (kb * 16 < K) {
+        float v[4];
+        uint32_t xv[4];
 #pragma unroll
-      for (int t = 0; t < TP; ++t) acc[q2][t] = make_float2(0.0f, 0.0f);
-    const float4* Cf4 = reinterpret_cast<const float4*>(sb + lay.c_off);
-#pragma unroll
-    for (int ch = 0; ch < kRowChunks; ++ch) {
-      const int q = j + 8 * ch;  // 16-byte chunk within the row
-      const uint4 q0 = *reinterpret_cast<const uint4*>(sb + rho0 * kRowBytes + q * 16);
-      const uint4 q1 = *reinterpret_cast<const uint4*>(sb + (rho0 + 1) * kRowBytes + q * 16);
-      constexpr int NP = RowChunk<DT>::kPairs;
-      float2 v0[NP], v1[NP];
-      RowChunk<DT>::get(q0, v0);
-      RowChunk<DT>::get(q1, v1);
-      const int m0 = q * (kEPC / 4);  // first f32 chunk of C for these columns
-#pragma unroll
-      for (int t = 0; t < TP; ++t) {
-#pragma unroll
-        for (int k4 = 0; k4 < kEPC / 4; ++k4) {
-          const float4 cv = Cf4[t * (kDstate / 4) + cswz(m0 + k4)];
-          const float2 ca = make_float2(cv.x, cv.y), cb = make_float2(cv.z, cv.w);
-          acc[0][t] = __ffma2_rn(v0[2 * k4], ca, acc[0][t]);
-          acc[0][t] = __ffma2_rn(v0[2 * k4 + 1], cb, acc[0][t]);
-          acc[1][t] = __ffma2_rn(v1[2 * k4], ca, acc[1][t]);
-          acc[1][t] = __ffma2_rn(v1[2 * k4 + 1], cb, acc[1][t]);
+        for (int e = 0; e < 4; ++e) {
+          const int k = kb * 16 + 4 * cq + e;
+          const bool in = k < K;
+          v[e] = (in && g < TP) ? coef[k * TP + g] : 0.0f;
+          xv[e] = in ? static_cast<uint32_t>(xs[k * kDim + d]) : 0u;
         }
+        const uint32_t h01 = pack_bf16(v[0], v[1]), h23 = pack_bf16(v[2], v[3]);
+        const uint32_t l01 = pack_bf16(v[0] - bf16_lo_f(h01), v[1] - bf16_hi_f(h01));
+        const uint32_t l23 = pack_bf16(v[2] - bf16_lo_f(h23), v[3] - bf16_hi_f(h23));
+        const uint32_t b0 = xv[0] | (xv[1] << 16), b1 = xv[2] | (xv[3] << 16);
+        mma_bf16(accr, h01, h23, b0, b1);
+        mma_bf16(accr, l01, l23, b0, b1);
       }
     }
-    const float* coef = reinterpret_cast<const float*>(sb + lay.coef_off);
-    float vals[2 * TP];
+    const float dec = g < TP ? coef[KB * TP + g] : 0.0f;
     float sc0 = 1.0f, sc1 = 1.0f;
     if constexpr (k8bit) {
-      const float* scl = reinterpret_cast<const float*>(sb + lay.scale_off);
-      sc0 = scl[rho0];
-      sc1 = scl[rho0 + 1];
-    }
-#pragma unroll
-    for (int t = 0; t < TP; ++t) {
-      const float dct = coef[KB * TP + t];
-      vals[t] = (acc[0][t].x + acc[0][t].y) * (dct * sc0);
-      vals[TP + t] = (acc[1][t].x + acc[1][t].y) * (dct * sc1);
-    }
-    // ---- ring terms: sum_k coef[k][t] x_k[d], k = j, j+8, ... (x rows in bf16) ----
-    const uint32_t* xs = reinterpret_cast<const uint32_t*>(sb + lay.x_off);
-    for (int k = j; k < K; k += 8) {
-      const uint32_t xw = xs[k * (kDim / 2) + (rho0 >> 1)];
-      const float x0 = bf16lo(xw), x1 = bf16hi(xw);
-#pragma unroll
-      for (int t4 = 0; t4 < TP; t4 += 4) {
-        const float4 cv = *reinterpret_cast<const float4*>(coef + k * TP + t4);
-        vals[t4 + 0] = fmaf(cv.x, x0, vals[t4 + 0]);
-        vals[t4 + 1] = fmaf(cv.y, x0, vals[t4 + 1]);
-        vals[t4 + 2] = fmaf(cv.z, x0, vals[t4 + 2]);
-        vals[t4 + 3] = fmaf(cv.w, x0, vals[t4 + 3]);
-        vals[TP + t4 + 0] = fmaf(cv.x, x1, vals[TP + t4 + 0]);
-        vals[TP + t4 + 1] = fmaf(cv.y, x1, vals[TP + t4 + 1]);
-        vals[TP + t4 + 2] = fmaf(cv.z, x1, vals[TP + t4 + 2]);
-        vals[TP + t4 + 3] = fmaf(cv.w, x1, vals[TP + t4 + 3]);
-      }
+      const float2 scv = *reinterpret_cast<const float2*>(sb + lay.scale_off + dout * 4);
+      sc0 = scv.x;
+      sc1 = scv.y;
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
-    // ---- transpose-reduce the 2*TP partial sums over the 8 lanes of a row pair ----
-    constexpr int V = 2 * TP;
-#pragma unroll
-    for (int step = 0; step < 3; ++step) {
-      const int mask = 4 >> step;
-      const int half = V >> (step + 1);
-      const bool upper = (j & mask) != 0;
-#pragma unroll
-      for (int e = 0; e < half; ++e) {
-        const float send = upper ? vals[e] : vals[e + half];
-        const float keep = upper ? vals[e + half] : vals[e];
-        vals[e] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
-      }
-    }
-    // lane j now holds value index j * (V/8) + e: row rho0 + (j >> 2)
-    constexpr int PER = V / 8;
-#pragma unroll
-    for (int e = 0; e < PER; ++e) {
-      const int idx = j * PER + e;
-      const int rr = idx / TP, t = idx % TP;
-      if (t < m.Tb) {
-        const __nv_bfloat16 yv = __float2bfloat16_rn(vals[e]);
-        a.out[(static_cast<long long>(m.tok0 + t) * H + m.h) * kDim + rho0 + rr] =
-            *reinterpret_cast<const uint16_t*>(&yv);
-      }
+    const float y0 = fmaf(dec * sc0, acc[0], accr[0]);
+    const float y1 = fmaf(dec * sc1, acc[1], accr[1]);
+    if (g < m.Tb) {
+      const __nv_bfloat162 yv = __floats2bfloat162_rn(y0, y1);
+      *reinterpret_cast<__nv_bfloat162*>(a.out + (static_cast<long long>(m.tok0 + g) * H + m.h) * kDim + dout) = yv;
     }
   }
 }
@@ -484,9 +476,39 @@ int launch_precompute(const StepArgs& a, void* stream) {
   return cudaGetLastError();
 }
 
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// S0 of all slots as a 3-D tensor [slot][H*64 rows][128], boxes of 64 rows x 128 bytes, 128-byte swizzle
+static bool encode_state_map(const Cache& c, CUtensorMap* map) {
+  auto enc = tensor_map_encoder();
+  if (!enc) return false;
+  const int esz = c.dtype == RSSM_F32 ? 4 : (c.dtype == RSSM_BF16 || c.dtype == RSSM_F16) ? 2 : 1;
+  const CUtensorMapDataType dt = esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                          : (esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8);
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDstate), static_cast<cuuint64_t>(c.H) * kDim,
+                              static_cast<cuuint64_t>(c.S)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDstate) * esz, static_cast<cuuint64_t>(c.state_stride) * esz};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kDim), 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return enc(map, dt, 3, c.state, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int DT, int TP>
 static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
-  // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 6
+  // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 8
   int ns = 8, ctas = 2;
   for (; ns >= 3; --ns)
     if (read_layout(DT, a.c.L, TP, ns).total <= 113 * 1024) break;
@@ -496,6 +518,8 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
       if (read_layout(DT, a.c.L, TP, ns).total <= 225 * 1024) break;
   }
   const ReadLayout lay = read_layout(DT, a.c.L, TP, ns);
+  CUtensorMap map;
+  if (!encode_state_map(a.c, &map)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributePreferredSharedMemoryCarveout,
@@ -509,7 +533,7 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   const long long units = static_cast<long long>(a.batch) * a.c.H;
   const long long cap = static_cast<long long>(num_sms) * occ;
   const int grid = static_cast<int>(units < cap ? units : cap);
-  readout_kernel<DT, TP><<<grid, kThreads, lay.total, st>>>(a, ns);
+  readout_kernel<DT, TP><<<grid, kThreads, lay.total, st>>>(map, a, ns);
   return cudaGetLastError();
 }
 
