@@ -8,12 +8,15 @@ checkpoints, window 16, T = 4 drafts.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
                     [--config NAME] [--force-flush] [--no-e2e] [--no-cpu-baseline]
 
-Timing: W untimed warm-up steps, then K steps, each bracketed by CUDA events
-on the launching stream; between steps (outside the events) a 1 GiB buffer is
-written and a 512 MiB buffer read, so every step starts with a cold L2 that
-holds no dirty lines.  Under torchrun (N > 1) every
-rank runs an independent replica (weak scaling, no data-path collective);
-the time is the max over ranks.  Prints one JSON line on rank 0.
+Timing: W untimed warm-up steps, then K steps, each one CUDA graph (the
+library's kernels chained by programmatic dependent launch) bracketed by CUDA
+events on the launching stream -> `value`.  A second pass replays the same
+steps as one graph per launch group with events between the groups -> the
+per-kernel durations behind `roofline`.  Between steps (outside the events) a
+1 GiB buffer is written and a 512 MiB buffer read, so every step starts with a
+cold L2 that holds no dirty lines.  Under torchrun (N > 1) every rank runs an
+independent replica (weak scaling, no data-path collective); the time is the
+max over ranks.  Prints one JSON line on rank 0.
 """
 from __future__ import annotations
 
@@ -303,6 +306,11 @@ def run_gpu(args, rank, ws, local):
             with torch.cuda.graph(g, stream=side, capture_error_mode="thread_local"):
                 f()
             graphs.append(g)
+        # the whole step as one graph (kernels chained by programmatic launch)
+        g_step = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g_step, stream=side, capture_error_mode="thread_local"):
+            for f in groups:
+                f()
     torch.cuda.synchronize()
     # restart the workload from its initial state
     for i in range(0, active.size, chunk):
@@ -320,7 +328,44 @@ def run_gpu(args, rank, ws, local):
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
 
-    def one_step():
+    def step_units():
+        rr = scr_step[: ids.size * 32].view(torch.int32).view(ids.size, 8).cpu().numpy()
+        return rr, int(((rr[:, 5] == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
+
+    for k in range(args.warmup):
+        load_inputs(dev_inp[k])
+        cold_l2()
+        g_step.replay()
+    torch.cuda.synchronize()
+
+    # timed pass 1: whole steps (one graph each) -> value
+    step_ms, units = [], 0
+    barrier(ws)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    for k in range(args.warmup, nsteps):
+        load_inputs(dev_inp[k])
+        cold_l2()
+        e0 = ev()
+        e0.record(stream)
+        g_step.replay()
+        e1 = ev()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        step_ms.append(e0.elapsed_time(e1))
+        units += step_units()[1]
+    clk = clocks.stop()
+    barrier(ws)
+    torch.cuda.synchronize()
+
+    # timed pass 2: the same steps launched group by group with events between
+    # the groups -> per-kernel durations for the roofline
+    read_ms, flush_ms, read_bytes, fold_bytes = [], [], 0.0, 0.0
+    for k in range(args.warmup, nsteps):
+        load_inputs(dev_inp[k])
+        cold_l2()
+        e0 = ev()
+        e0.record(stream)
         graphs[0].replay()
         e_f = ev()
         e_f.record(stream)
@@ -331,39 +376,14 @@ def run_gpu(args, rank, ws, local):
         e_r1 = ev()
         e_r1.record(stream)
         graphs[3].replay()
-        return e_f, e_r0, e_r1
-
-    for k in range(args.warmup):
-        load_inputs(dev_inp[k])
-        cold_l2()
-        one_step()
-    torch.cuda.synchronize()
-
-    step_ms, read_ms, flush_ms, read_bytes, fold_bytes, units = [], [], [], 0.0, 0.0, 0
-    barrier(ws)
-    torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.current_device())
-    for k in range(args.warmup, nsteps):
-        load_inputs(dev_inp[k])
-        cold_l2()
-        e0 = ev()
-        e0.record(stream)
-        e_f, e_r0, e_r1 = one_step()
-        e1 = ev()
-        e1.record(stream)
         torch.cuda.synchronize()
-        step_ms.append(e0.elapsed_time(e1))
         flush_ms.append(e0.elapsed_time(e_f))
         read_ms.append(e_r0.elapsed_time(e_r1))
-        # per-row records the readout used, and the flagged rows of the flush
-        rr = scr_step[: ids.size * 32].view(torch.int32).view(ids.size, 8).cpu().numpy()
+        rr, _ = step_units()
         read_bytes += algorithmic_bytes(wl, [tuple(r[:6]) for r in rr], None, esz)
-        units += int(((rr[:, 5] == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
         cnt = int(scr_flush[:4].view(torch.int32).item())
         recs = scr_flush[256: 256 + cnt * 32].view(torch.int32).view(cnt, 8).cpu().numpy() if cnt else np.zeros((0, 8))
         fold_bytes += flush_bytes(wl, [int(r[3]) for r in recs], esz)
-    clk = clocks.stop()
-    barrier(ws)
     torch.cuda.synchronize()
     err = int(gc.error_word.item())
     if err:
@@ -386,14 +406,13 @@ def run_gpu(args, rank, ws, local):
             e0 = ev()
             e0.record(stream)
             load_inputs(hi, non_blocking=True)
-            one_step()
+            g_step.replay()
             yh[: hi["ntok"]].copy_(out[: hi["ntok"]], non_blocking=True)
             e1 = ev()
             e1.record(stream)
             torch.cuda.synchronize()
             e2e_ms.append(e0.elapsed_time(e1))
-            rr = scr_step[: ids.size * 32].view(torch.int32).view(ids.size, 8).cpu().numpy()
-            e2e_units += int(((rr[:, 5] == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
+            e2e_units += step_units()[1]
             h2d = sum(hi[key].numel() * hi[key].element_size() for key in ("x", "dt", "B", "C", "acc")) + (
                 0 if hi["cu"] is None else hi["cu"].numel() * 4)
             d2h = hi["ntok"] * wl.nheads * 64 * 2
@@ -409,7 +428,7 @@ def run_gpu(args, rank, ws, local):
         "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB written then 512 MiB read between steps (cold, clean L2)",
-                       launch="one CUDA graph per launch group, replayed per step",
+                       launch="one CUDA graph per step (kernels chained by programmatic dependent launch); kernel times from a second pass with one graph per launch group",
                        force_flush=bool(args.force_flush)),
         "roofline": {"bound": "hbm", "kernel": "readout_kernel", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
@@ -420,7 +439,7 @@ def run_gpu(args, rank, ws, local):
                            "avg_us": 1e3 * statistics.mean(flush_ms),
                            "algorithmic_bytes_per_step": fold_bytes / args.steps},
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,
+        "gpu_launches": 5 * args.steps,  # flag, fold, precompute, readout, accept per step
         "clocks": clk,
         "device_time_ms": {"step": statistics.mean(step_ms), "readout": statistics.mean(read_ms),
                            "flush": statistics.mean(flush_ms)},

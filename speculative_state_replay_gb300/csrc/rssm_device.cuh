@@ -83,6 +83,31 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// Programmatic dependent launch.  pdl_wait() returns once the preceding kernel
+// in the stream has completed and its writes are visible (immediately when the
+// kernel was launched without the attribute); every chain kernel calls it
+// before touching memory its predecessors may write.  pdl_trigger() lets the
+// next kernel start launching (it still waits before reading our results).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// launch with programmatic stream serialisation (the kernel must call pdl_wait)
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
+
 // named barrier over the consumer warps only (the producer warp never joins)
 __device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, %0;" ::"n"(kConsumerThreads) : "memory"); }
 
@@ -256,38 +281,48 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t c) {
 }
 
 // --------------------------------------------------------------------------
+// Round-to-nearest-even, saturating at the largest finite value, two at a time
+// (the PTX satfinite conversions: RNE first, then clamp to +-max finite).
+// --------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t cvt_f16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint32_t cvt_bf16x2_sat(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.satfinite.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// --------------------------------------------------------------------------
 // Checkpoint quantiser for one thread's 4 rows x 8 columns (rows r0..r0+3,
 // columns c0..c0+7 of a [64][128] head), the fragment the flush and init
 // kernels own.  Lanes sharing rows must be the 16 lanes with equal
 // (lane >> 4) of a warp (they hold the 128 columns of those rows).
 // 8-bit formats: per-row scale = amax/QMAX (1 for amax < 2^-100), v = acc *
-// (1/scale), then nearest or stochastic rounding.
+// (1/scale), then nearest or stochastic rounding.  Stochastic rounding draws
+// one Philox4x32-7 block per 4 consecutive elements of a row.
 // --------------------------------------------------------------------------
+__device__ __forceinline__ void row_random(uint32_t (&rnd)[8], int row, int c0, uint32_t h, uint32_t s,
+                                           uint32_t epoch, uint64_t seed) {
+  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const uint32_t elem = static_cast<uint32_t>(row * 128 + c0 + 4 * q);
+    const uint4 w = philox4x32_7(elem >> 2, h, s, epoch, k0, k1);
+    rnd[4 * q + 0] = w.x;
+    rnd[4 * q + 1] = w.y;
+    rnd[4 * q + 2] = w.z;
+    rnd[4 * q + 3] = w.w;
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c0, int lane, void* head_state,
                                                float* head_scale, int rounding, uint32_t h, uint32_t s,
                                                uint32_t epoch, uint64_t seed) {
   const bool sr = rounding == RSSM_ROUND_STOCHASTIC;
-  const uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
-  uint32_t rnd[4][8];
-  if (DT != RSSM_F32 && sr) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const uint32_t elem = static_cast<uint32_t>((r0 + i) * 128 + c0 + 4 * q);
-        const uint4 w = philox4x32_7(elem >> 2, h, s, epoch, k0, k1);
-        rnd[i][4 * q + 0] = w.x;
-        rnd[i][4 * q + 1] = w.y;
-        rnd[i][4 * q + 2] = w.z;
-        rnd[i][4 * q + 3] = w.w;
-      }
-  } else {
-#pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-      for (int q = 0; q < 8; ++q) rnd[i][q] = 0u;
-  }
   if constexpr (DT == RSSM_F32) {
     float* st = static_cast<float*>(head_state);
 #pragma unroll
@@ -301,17 +336,26 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       uint32_t wds[4];
+      if (!sr) {
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        uint16_t lo, hi;
-        if constexpr (DT == RSSM_BF16) {
-          lo = round_bf16(acc[i][2 * q], sr, rnd[i][2 * q]);
-          hi = round_bf16(acc[i][2 * q + 1], sr, rnd[i][2 * q + 1]);
-        } else {
-          lo = round_f16(acc[i][2 * q], sr, rnd[i][2 * q]);
-          hi = round_f16(acc[i][2 * q + 1], sr, rnd[i][2 * q + 1]);
+        for (int q = 0; q < 4; ++q)
+          wds[q] = DT == RSSM_BF16 ? cvt_bf16x2_sat(acc[i][2 * q], acc[i][2 * q + 1])
+                                   : cvt_f16x2_sat(acc[i][2 * q], acc[i][2 * q + 1]);
+      } else {
+        uint32_t rnd[8];
+        row_random(rnd, r0 + i, c0, h, s, epoch, seed);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          uint16_t lo, hi;
+          if constexpr (DT == RSSM_BF16) {
+            lo = round_bf16(acc[i][2 * q], true, rnd[2 * q]);
+            hi = round_bf16(acc[i][2 * q + 1], true, rnd[2 * q + 1]);
+          } else {
+            lo = round_f16(acc[i][2 * q], true, rnd[2 * q]);
+            hi = round_f16(acc[i][2 * q + 1], true, rnd[2 * q + 1]);
+          }
+          wds[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
         }
-        wds[q] = static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
       }
       *reinterpret_cast<uint4*>(st + (r0 + i) * 128 + c0) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
     }
@@ -335,25 +379,44 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
       if (mine == i) am = amax[i];
     const float sc = am < 7.888609052210118e-31f /* 2^-100 */ ? 1.0f : __fdiv_rn(am, qmax);
     const float iv = __frcp_rn(sc);
-    float scale[4], inv[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      scale[i] = __shfl_sync(0xffffffffu, sc, (lane & 16) | i);
-      inv[i] = __shfl_sync(0xffffffffu, iv, (lane & 16) | i);
-    }
+    float scale[4];
     uint8_t* st = static_cast<uint8_t*>(head_state);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
+      scale[i] = __shfl_sync(0xffffffffu, sc, (lane & 16) | i);
+      const float inv = __shfl_sync(0xffffffffu, iv, (lane & 16) | i);
       uint32_t wds[2] = {0u, 0u};
+      if (!sr) {
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {
-        const float v = __fmul_rn(acc[i][q], inv[i]);
-        uint32_t code;
-        if constexpr (DT == RSSM_I8)
-          code = static_cast<uint8_t>(round_i8(v, sr, rnd[i][q]));
-        else
-          code = round_e4m3(v, sr, rnd[i][q]);
-        wds[q >> 2] |= code << (8 * (q & 3));
+        for (int q = 0; q < 8; q += 2) {
+          const float v0 = __fmul_rn(acc[i][q], inv), v1 = __fmul_rn(acc[i][q + 1], inv);
+          uint32_t pair;
+          if constexpr (DT == RSSM_I8) {
+            // |v| <= amax / scale < 127.5, so round-to-nearest-even alone stays in -127..127
+            int i0, i1;
+            asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i0) : "f"(v0));
+            asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i1) : "f"(v1));
+            i0 = max(-127, min(127, i0));
+            i1 = max(-127, min(127, i1));
+            pair = (static_cast<uint32_t>(i0) & 0xffu) | ((static_cast<uint32_t>(i1) & 0xffu) << 8);
+          } else {
+            pair = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3));
+          }
+          wds[q >> 2] |= pair << (8 * (q & 3));
+        }
+      } else {
+        uint32_t rnd[8];
+        row_random(rnd, r0 + i, c0, h, s, epoch, seed);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const float v = __fmul_rn(acc[i][q], inv);
+          uint32_t code;
+          if constexpr (DT == RSSM_I8)
+            code = static_cast<uint8_t>(round_i8(v, true, rnd[q]));
+          else
+            code = round_e4m3(v, true, rnd[q]);
+          wds[q >> 2] |= code << (8 * (q & 3));
+        }
       }
       *reinterpret_cast<uint2*>(st + (r0 + i) * 128 + c0) = make_uint2(wds[0], wds[1]);
     }

@@ -10,7 +10,7 @@
 //   fold_kernel  persistent, one (flagged row, head) unit at a time:
 //                S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
 //                in fp32, canonical order, then rounding to the state format.
-// The fold streams S0 (and the live x/B rows) through a 3-stage shared-memory
+// The fold streams S0 (and the live x/B rows) through a 3-6 stage shared-memory
 // ring filled by 1-D bulk copies from a producer warp; 8 consumer warps own a
 // 4x8 fragment of the [64][128] state each and accumulate with packed f32x2
 // FMAs.  HBM traffic per unit: read + write of S0 (+ scales) and p rows of x
@@ -29,6 +29,8 @@ __global__ void __launch_bounds__(1024) flag_kernel(FlushArgs a) {
   __shared__ int base;
   const Cache& c = a.c;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  pdl_wait();
+  pdl_trigger();
   if (tid == 0) base = 0;
   __syncthreads();
   for (int b0 = 0; b0 < a.batch; b0 += 1024) {
@@ -101,9 +103,9 @@ struct FoldLayout {
   uint32_t meta_off, stages_off, uf_off, bf_off, total;
 };
 
-__host__ __device__ inline FoldLayout fold_layout(int dtype, int L) {
+__host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns) {
   FoldLayout f;
-  f.ns = 3;
+  f.ns = ns;
   f.KB = (L + 3) & ~3;
   const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
   f.s0_bytes = kHeadElems * esz;
@@ -126,13 +128,15 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 1) fold_kernel(FlushArgs a) {
+__global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Cache& c = a.c;
-  const FoldLayout lay = fold_layout(DT, c.L);
+  const FoldLayout lay = fold_layout(DT, c.L, ns);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
 
+  pdl_wait();  // the flag kernel's count and records
+  pdl_trigger();
   const long long units = static_cast<long long>(*a.count) * c.H;
   const long long per = units / gridDim.x, rem = units % gridDim.x;
   const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
@@ -140,7 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_kernel(FlushArgs a) {
   if (nu == 0) return;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
-  uint64_t* empty = full + 4;
+  uint64_t* empty = full + 8;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
   FoldMeta* meta = reinterpret_cast<FoldMeta*>(smem + lay.meta_off);
   float2* uf2 = reinterpret_cast<float2*>(smem + lay.uf_off);
@@ -159,25 +163,40 @@ __global__ void __launch_bounds__(kThreads, 1) fold_kernel(FlushArgs a) {
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
-    int cur = -1;
-    FlushRec rec = {};
-    float Ah = 0.0f;
+    // The live dt' values of unit i+1 are loaded while unit i is issued, so the
+    // load latency overlaps the wait for a free stage.
+    auto unit_of = [&](int i, int& li, int& h) {
+      const long long u = u0 + i;
+      li = static_cast<int>(u / c.H);
+      h = static_cast<int>(u % c.H);
+    };
+    auto load_dt = [&](const FlushRec& rc, int h) {
+      return lane < rc.p ? c.dt_cache[static_cast<long long>(rc.s) * c.dt_stride + static_cast<long long>(h) * c.L +
+                                      (rc.r + lane) % c.L]
+                         : 0.0f;
+    };
+    int li_n, h_n;
+    unit_of(0, li_n, h_n);
+    FlushRec rec_n = a.recs[li_n];
+    float dt_n = load_dt(rec_n, h_n), A_n = a.A[h_n];
     int issued = 0;
     bool ok = true;
-    for (int i = 0; i < nu && ok; ++i) {
+    for (int i = 0; i < nu; ++i) {
       const int st = i % lay.ns;
       const uint32_t ph = (i / lay.ns) & 1;
+      const FlushRec rec = rec_n;
+      const int h = h_n, li = li_n;
+      const float dtj = dt_n, Ah = A_n;
+      if (i + 1 < nu) {  // prefetch the next unit
+        unit_of(i + 1, li_n, h_n);
+        if (li_n != li) rec_n = a.recs[li_n];
+        dt_n = load_dt(rec_n, h_n);
+        A_n = a.A[h_n];
+      }
       if (i >= lay.ns && !mbar_wait(&empty[st], ph ^ 1)) {
         ok = false;
         break;
       }
-      const long long u = u0 + i;
-      const int li = static_cast<int>(u / c.H), h = static_cast<int>(u % c.H);
-      if (li != cur) {
-        rec = a.recs[li];
-        cur = li;
-      }
-      Ah = a.A[h];
       const int s = rec.s, r = rec.r, p = rec.p, g = h / c.hpg;
       uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
       if (lane == 0) {
@@ -201,11 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_kernel(FlushArgs a) {
         }
       }
       // canonical cumulative sums c_j (sequential fp32) and weights
-      float dtj = 0.0f, aj = 0.0f;
-      if (lane < p) {
-        dtj = c.dt_cache[static_cast<long long>(s) * c.dt_stride + static_cast<long long>(h) * c.L + (r + lane) % c.L];
-        aj = __fmul_rn(Ah, dtj);
-      }
+      const float aj = lane < p ? __fmul_rn(Ah, dtj) : 0.0f;
       float cj = 0.0f;
       for (int k = 0; k < p; ++k) {
         const float ak = __shfl_sync(0xffffffffu, aj, k);
@@ -221,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) fold_kernel(FlushArgs a) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
       issued = i + 1;
+      (void)li;
     }
     if (!ok) {
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
@@ -377,6 +393,8 @@ __global__ void __launch_bounds__(256) init_clear_kernel(InitArgs a) {
 __global__ void __launch_bounds__(256) accept_kernel(Cache c, const int* slot_idx, int* pnat, const int* accepted,
                                                      const int* cu, int batch, int T) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  pdl_wait();
+  pdl_trigger();
   if (b >= batch) return;
   const int s = slot_idx[b];
   if (s < 1 || s >= c.S) return;
@@ -412,21 +430,27 @@ __global__ void spec_math_kernel(const float* in, float* oexp, float* osp, long 
 // ---------------------------------------------------------------------------
 template <int DT>
 static int launch_fold_t(const FlushArgs& a, int num_sms, cudaStream_t st) {
-  const FoldLayout lay = fold_layout(DT, a.c.L);
+  // two CTAs per SM: as many stages (3..6) as fit 113 KB
+  int ns = 6;
+  while (ns > 2 && fold_layout(DT, a.c.L, ns).total > 113 * 1024) --ns;
+  const FoldLayout lay = fold_layout(DT, a.c.L, ns);
   cudaError_t e = cudaFuncSetAttribute(fold_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+  if (e != cudaSuccess) return e;
+  e = cudaFuncSetAttribute(fold_kernel<DT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   // the number of flagged rows is only known on the device: size the grid for
   // the worst case (every row flagged), capped at one CTA per SM
   const long long units = static_cast<long long>(a.batch) * a.c.H;
-  const int grid = static_cast<int>(units < num_sms ? (units > 0 ? units : 1) : num_sms);
-  fold_kernel<DT><<<grid, kThreads, lay.total, st>>>(a);
-  return cudaGetLastError();
+  const long long cap = 2LL * num_sms;
+  const int grid = static_cast<int>(units < cap ? (units > 0 ? units : 1) : cap);
+  e = launch_pdl(fold_kernel<DT>, dim3(grid), dim3(kThreads), lay.total, st, a, ns);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int launch_flush(const FlushArgs& a, int num_sms, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  flag_kernel<<<1, 1024, 0, st>>>(a);
-  cudaError_t e = cudaGetLastError();
+  cudaError_t e = launch_pdl(flag_kernel, dim3(1), dim3(1024), 0, st, a);
   if (e != cudaSuccess) return e;
   switch (a.c.dtype) {
     case RSSM_F32: return launch_fold_t<RSSM_F32>(a, num_sms, st);
@@ -455,9 +479,9 @@ int launch_init(const InitArgs& a, void* stream) {
 
 int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* accepted, const int* cu, int batch,
                   int T, void* stream) {
-  accept_kernel<<<(batch + 255) / 256, 256, 0, static_cast<cudaStream_t>(stream)>>>(c, slot_idx, pnat, accepted,
-                                                                                    cu, batch, T);
-  return cudaGetLastError();
+  cudaError_t e = launch_pdl(accept_kernel, dim3((batch + 255) / 256), dim3(256), 0, static_cast<cudaStream_t>(stream),
+                             c, slot_idx, pnat, accepted, cu, batch, T);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int launch_spec_math(const float* in, float* oexp, float* osp, long long n, void* stream) {

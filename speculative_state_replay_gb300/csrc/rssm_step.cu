@@ -33,10 +33,13 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
   __shared__ float Cf[TP][kDstate + 4];
   __shared__ float CB[TP][kMaxL];
   __shared__ float dtl[16][kMaxL];  // live dt' of up to 16 heads of the group
+  __shared__ float dtn[16][kMaxT];  // new dt + dt_bias of up to 16 heads
   __shared__ int meta[6];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  pdl_wait();  // the flush's bookkeeping and checkpoints are complete from here on
+  pdl_trigger();
   if (tid == 0) {
     const int s = a.slot_idx[b];
     int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
@@ -90,6 +93,10 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
     const int hh = idx / p, k = idx % p;
     dtl[hh][k] = c.dt_cache[static_cast<long long>(s) * c.dt_stride + static_cast<long long>(g * hpg + hh) * L +
                             (r + k) % L];
+  }
+  for (int idx = tid; idx < hl * Tb; idx += 256) {
+    const int hh = idx / Tb, t = idx % Tb, h = g * hpg + hh;
+    dtn[hh][t] = __fadd_rn(a.dt[static_cast<long long>(tok0 + t) * H + h], a.dt_bias[h]);
   }
   // ring appends: the new B rows (once per group) and the new x rows of the group's heads
   for (int idx = tid; idx < Tb * 16; idx += 256) {
@@ -149,15 +156,17 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
       dtp = hh < 16 ? dtl[hh][lane] : dtrow[(r + lane) % L];
     } else if (lane < K) {
       const int t = lane - p;
-      const float v = __fadd_rn(a.dt[static_cast<long long>(tok0 + t) * H + h], a.dt_bias[h]);
-      dtp = spec_softplus(v);
+      const float v = hh < 16 ? dtn[hh][t] : __fadd_rn(a.dt[static_cast<long long>(tok0 + t) * H + h], a.dt_bias[h]);
+      dtp = spec_softplus(v);  // the value stored in the ring: fixed-sequence softplus
       dtrow[(r + p + t) % L] = dtp;
     }
-    const float ak = __fmul_rn(Ah, dtp);
-    float cum = 0.0f;
-    for (int k = 0; k < K; ++k) {
-      const float x = __shfl_sync(0xffffffffu, ak, k);
-      if (lane >= k) cum = __fadd_rn(cum, x);
+    // inclusive prefix sum of A dt' over the lanes (these sums only feed the
+    // outputs, so any summation order is fine here)
+    float cum = lane < K ? Ah * dtp : 0.0f;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const float x = __shfl_up_sync(0xffffffffu, cum, off);
+      if (lane >= off) cum += x;
     }
     float cf[TP];
     float dec[TP];
@@ -346,6 +355,25 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   if (warp == kConsumerWarps) {
     // ---------------- producer: one lane issues all copies ----------------
     if (lane != 0) return;
+    // Before waiting for the precompute: request S0 of the first stages.  S0
+    // is final by now (the precompute waited for the flush before it let this
+    // kernel launch) and needs only the slot id, an input of the call.
+    const int npre = nu < ns ? nu : ns;
+    uint32_t pre = 0u;
+    for (int i = 0; i < npre; ++i) {
+      const long long u = u0 + i;
+      const int b = static_cast<int>(u / H), h = static_cast<int>(u % H);
+      const int s = a.slot_idx[b];
+      if (s >= 1 && s < c.S) {
+        uint8_t* sb = smem + lay.stages_off + i * lay.stage_bytes;
+        mbar_expect_tx(&full[i], lay.s0_bytes);
+#pragma unroll
+        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[i]);
+        pre |= 1u << i;
+      }
+    }
+    pdl_wait();  // row records, C blocks, coefficients, appended x rows
+    pdl_trigger();
     int cur_b = -1;
     RowRec rr = {};
     int issued = 0;
@@ -368,10 +396,14 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         const int s = rr.s, r = rr.r, K = rr.p + rr.Tb, g = h / c.hpg;
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
         const uint32_t coef_bytes = (KB + 1) * TP * 4;
-        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + 8 * kDstate * 2 + coef_bytes + K * kDim * 2;
+        const bool have_s0 = i < npre && ((pre >> i) & 1u);
+        const uint32_t bytes =
+            (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + 8 * kDstate * 2 + coef_bytes + K * kDim * 2;
         mbar_expect_tx(&full[st], bytes);
+        if (!have_s0) {
 #pragma unroll
-        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
+          for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
+        }
         if (k8bit)
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
         bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
@@ -469,11 +501,9 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
 int launch_precompute(const StepArgs& a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = a.batch * a.c.G;
-  if (a.TP == 4)
-    precompute_kernel<4><<<grid, 256, 0, st>>>(a);
-  else
-    precompute_kernel<8><<<grid, 256, 0, st>>>(a);
-  return cudaGetLastError();
+  const cudaError_t e = a.TP == 4 ? launch_pdl(precompute_kernel<4>, dim3(grid), dim3(256), 0, st, a)
+                                   : launch_pdl(precompute_kernel<8>, dim3(grid), dim3(256), 0, st, a);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
@@ -533,8 +563,8 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   const long long units = static_cast<long long>(a.batch) * a.c.H;
   const long long cap = static_cast<long long>(num_sms) * occ;
   const int grid = static_cast<int>(units < cap ? units : cap);
-  readout_kernel<DT, TP><<<grid, kThreads, lay.total, st>>>(map, a, ns);
-  return cudaGetLastError();
+  e = launch_pdl(readout_kernel<DT, TP>, dim3(grid), dim3(kThreads), lay.total, st, map, a, ns);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int launch_readout(const StepArgs& a, int num_sms, void* stream) {
