@@ -176,14 +176,14 @@ class ClockSampler:
 # --------------------------------------------------------------------------- #
 def algorithmic_bytes(wl, rows_rec, ntok_b, esz):
     """Algorithmic HBM bytes of one readout launch from its per-row records:
-    S0 (+ scales) once per (row, head), live x ring rows, new x, C per group,
-    y and the appended x; inactive rows only write zero outputs."""
+    S0 (+ scales) once per (row, head), the group's C rows shared by its heads,
+    and y; inactive rows only write zero outputs.  (The live x rows, the ring
+    term and the appends are the precompute's.)"""
     total = 0
     hpg = wl.hpg
     for (s, r, p, Tb, tok0, flags) in rows_rec:
         if flags and Tb > 0:
-            per_head = (64 * 128 * esz + (256 if esz == 1 else 0) + p * 128 + Tb * 128 + Tb * 256 / hpg
-                        + Tb * 128 + Tb * 128)
+            per_head = 64 * 128 * esz + (256 if esz == 1 else 0) + Tb * 256 / hpg + Tb * 128
             total += per_head * wl.nheads
         elif Tb > 0:
             total += Tb * 128 * wl.nheads
@@ -400,25 +400,35 @@ def run_gpu(args, rank, ws, local):
     if not args.no_e2e:
         yh = torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16).pin_memory()
         e2e_ms, e2e_units, h2d, d2h = [], 0, 0, 0
+        parts = {"h2d": [], "step": [], "d2h": []}
         for k in range(args.warmup, nsteps):
             hi = hin[k]
             cold_l2()
             e0 = ev()
             e0.record(stream)
             load_inputs(hi, non_blocking=True)
+            e_h = ev()
+            e_h.record(stream)
             g_step.replay()
+            e_g = ev()
+            e_g.record(stream)
             yh[: hi["ntok"]].copy_(out[: hi["ntok"]], non_blocking=True)
             e1 = ev()
             e1.record(stream)
             torch.cuda.synchronize()
             e2e_ms.append(e0.elapsed_time(e1))
+            parts["h2d"].append(e0.elapsed_time(e_h))
+            parts["step"].append(e_h.elapsed_time(e_g))
+            parts["d2h"].append(e_g.elapsed_time(e1))
             e2e_units += step_units()[1]
             h2d = sum(hi[key].numel() * hi[key].element_size() for key in ("x", "dt", "B", "C", "acc")) + (
                 0 if hi["cu"] is None else hi["cu"].numel() * 4)
             d2h = hi["ntok"] * wl.nheads * 64 * 2
         t_e2e = max_over_ranks(sum(e2e_ms), ws, dev)
         e2e = {"value": sum_over_ranks(e2e_units, ws, dev) / (t_e2e / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "breakdown_us": {k: 1e3 * statistics.median(v) for k, v in parts.items()},
+               "host_buffers_pinned": bool(hin[0]["x"].is_pinned() and yh.is_pinned())}
 
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (sum(read_ms) / 1e3) / 1e9
@@ -450,69 +460,76 @@ def run_gpu(args, rank, ws, local):
 # --------------------------------------------------------------------------- #
 # CPU oracle (baseline leg and reference arm)
 # --------------------------------------------------------------------------- #
-def oracle_sample(wl, seconds: float, max_steps: int, rows: int | None = None):
-    """Time the oracle as it stands on the workload: flush + step + accept per
-    step over `rows` rows, until `seconds` of wall time or max_steps."""
-    import oracle
+class OracleRun:
+    """The oracle as it stands on the workload, restricted to the first `rows`
+    rows (rows are independent); one decode step = flush + step + accept."""
 
-    oracle.build()
-    gen = W.Generator(wl)
-    A, D, dtb = gen.params()
-    ids = gen.slot_idx()
-    if rows is not None and rows < ids.size:
-        ids = ids[:rows]
-    oc = oracle.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
-                            wl.rounding, slot_pad_bytes=wl.slot_pad_bytes)
-    act = ids[ids > 0]
-    oc.init_state(gen.init_states(0, act.size), act, seed=wl.sr_seed)
-    pnat = np.zeros(ids.size, np.int32)
-    units, t_all, steps = 0, 0.0, 0
-    T = wl.T
-    for k in range(max_steps):
-        inp = gen.step(k)
-        # restrict the step inputs to the sampled rows
+    def __init__(self, wl, rows=None):
+        import oracle
+
+        oracle.build()
+        self.oracle, self.wl = oracle, wl
+        self.gen = W.Generator(wl)
+        self.A, self.D, self.dtb = self.gen.params()
+        ids = self.gen.slot_idx()
+        self.ids = ids[:rows] if rows is not None and rows < ids.size else ids
+        self.oc = oracle.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted,
+                                     wl.state_dtype, wl.rounding, slot_pad_bytes=wl.slot_pad_bytes)
+        act = self.ids[self.ids > 0]
+        self.oc.init_state(self.gen.init_states(0, act.size), act, seed=wl.sr_seed)
+        self.pnat = np.zeros(self.ids.size, np.int32)
+        self.k = 0
+
+    def step(self):
+        """Runs one decode step; returns (units, seconds)."""
+        wl, ids, T = self.wl, self.ids, self.wl.T
+        inp = self.gen.step(self.k)
+        self.k += 1
         if inp.cu_seqlens is None:
-            tok = np.arange(ids.size * T)
-            cu = None
+            tok, cu = np.arange(ids.size * T), None
         else:
             cu = inp.cu_seqlens[: ids.size + 1].copy()
             tok = np.arange(int(cu[-1]))
+        x, dt, B, C = inp.x[tok], inp.dt[tok], inp.B[tok], inp.C[tok]
         t0 = time.perf_counter()
-        oc.flush(A, ids, pnat, T, cu_seqlens=cu, seed=wl.sr_seed)
-        oc.step(inp.x[tok], inp.dt[tok], A, inp.B[tok], inp.C[tok], D, dtb, ids, pnat, T, cu_seqlens=cu)
-        oc.accept(ids, pnat, inp.accepted[: ids.size], T, cu_seqlens=cu)
-        t_all += time.perf_counter() - t0
-        units += int((ids > 0).sum()) * wl.nheads
-        steps += 1
-        if t_all >= seconds:
-            break
-    thr = oracle.openmp_threads() or 1
-    return units / t_all, thr, steps, ids.size, t_all
+        self.oc.flush(self.A, ids, self.pnat, T, cu_seqlens=cu, seed=wl.sr_seed)
+        self.oc.step(x, dt, self.A, B, C, self.D, self.dtb, ids, self.pnat, T, cu_seqlens=cu)
+        self.oc.accept(ids, self.pnat, inp.accepted[: ids.size], T, cu_seqlens=cu)
+        return int((ids > 0).sum()) * wl.nheads, time.perf_counter() - t0
+
+    @property
+    def threads(self):
+        return self.oracle.openmp_threads() or 1
 
 
 def cpu_baseline(wl, seconds):
-    v, thr, steps, rows, secs = oracle_sample(wl, seconds, max_steps=64)
-    return {"value": v, "unit": UNIT, "cores": thr, "kind": "oracle",
-            "sample": f"{steps} steps x {rows} rows x {wl.nheads} heads of {wl.name} "
-                      f"(flush+step+accept, {secs:.1f} s wall, OpenMP over (row, head))"}
+    run = OracleRun(wl)
+    units, secs, steps = 0, 0.0, 0
+    while secs < seconds and steps < 64:
+        u, dt = run.step()
+        units, secs, steps = units + u, secs + dt, steps + 1
+    return {"value": units / secs, "unit": UNIT, "cores": run.threads, "kind": "oracle",
+            "sample": f"{steps} consecutive decode steps x {run.ids.size} rows x {wl.nheads} heads of {wl.name} "
+                      f"(flush+step+accept, {secs:.1f} s of CPU wall time, OpenMP over (row, head))"}
 
 
 def run_reference(args, rank, ws):
     if rank != 0:
         return None
     wl = workload(args)
-    per_step = max(0.5, 60.0 / max(1, args.steps + args.warmup))
+    run = OracleRun(wl, rows=min(16, wl.batch))
     vals = []
     for k in range(args.warmup + args.steps):
-        v, thr, steps, rows, secs = oracle_sample(wl, per_step, max_steps=1, rows=min(16, wl.batch))
+        u, secs = run.step()
         if k >= args.warmup:
-            vals.append((v, secs, steps, rows))
-    value = statistics.mean(v for v, *_ in vals)
-    sample = f"each step: 1 decode step of {vals[0][3]} rows x {wl.nheads} heads of {wl.name} on the CPU oracle"
-    cb = {"value": value, "unit": UNIT, "cores": thr, "kind": "oracle", "sample": sample}
+            vals.append((u, secs))
+    value = sum(u for u, _ in vals) / sum(s for _, s in vals)
+    sample = (f"each step: one decode step (flush+step+accept) of the first {run.ids.size} rows x {wl.nheads} heads "
+              f"of {wl.name} on the CPU oracle, consecutive steps on one cache")
+    cb = {"value": value, "unit": UNIT, "cores": run.threads, "kind": "oracle", "sample": sample}
     return {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(s for _, s, *_ in vals),
+        "warmup": args.warmup, "ms_per_step": 1e3 * statistics.mean(s for _, s in vals),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(wl.describe(), parallelism=f"replicas{ws}"), "cpu_baseline": cb,
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -125,7 +125,7 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->out = static_cast<uint16_t*>(out);
   a->rows = static_cast<RowRec*>(scratch);
   a->cf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch));
-  a->coef = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch) +
+  a->rblk = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch) +
                                      step_cf_bytes(batch, cache->ngroups, T));
   return RSSM_OK;
 }

@@ -82,7 +82,7 @@ struct StepArgs {
   uint16_t* out;
   RowRec* rows;  // scratch [batch]
   uint16_t* cf;  // scratch [batch][G][8][128]: C rows in the readout's MMA operand type
-  float* coef;   // scratch [batch][H][KB+1][TP]
+  float* rblk;   // scratch [batch][H][TP*64 + TP]: ring term R[t][d], then decay[t]
 };
 
 struct InitArgs {
@@ -104,8 +104,10 @@ inline size_t step_cf_bytes(int batch, int G, int T) {
   (void)T;
   return align_up((size_t)batch * G * 8 * 128 * 2, 256);
 }
+inline size_t step_rblk_floats(int T) { return (size_t)t_pad(T) * 64 + t_pad(T); }
 inline size_t step_scratch_bytes(int batch, int H, int G, int L, int T) {
-  const size_t blk = (size_t)(ring_pad(L) + 1) * t_pad(T) * sizeof(float);
+  (void)L;
+  const size_t blk = step_rblk_floats(T) * sizeof(float);
   return step_rows_bytes(batch) + step_cf_bytes(batch, G, T) + align_up(blk * (size_t)batch * H, 256);
 }
 

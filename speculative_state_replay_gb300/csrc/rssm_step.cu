@@ -7,9 +7,12 @@
 //       cached: Description item 2), the C.B contraction CB[t][k] = C_t . B_k
 //       once per group, and per head the replay coefficients
 //           coef[k][t] = e^{c_{p+t} - c_k} dt'_k CB[t][k]  (+ D on k = p+t)
-//       plus decay[t] = e^{c_{p+t}}, written to scratch.  Appends B.
+//       which it applies at once to the head's x rows:
+//           R[t][d] = sum_k coef[k][t] x_k[d],   decay[t] = e^{c_{p+t}}
+//       written to scratch with the C rows (in the readout's MMA type).
+//       Appends B, x and dt'.
 //   readout_kernel  persistent, one (row, head) unit at a time:
-//           y_t[d] = decay[t] (S0[d] . C_t) + sum_k coef[k][t] x_k[d]
+//           y_t[d] = decay[t] (S0[d] . C_t) + R[t][d]
 //       streaming S0 once through a multi-stage shared-memory ring filled by
 //       TMA (swizzled tensor boxes for S0, 1-D bulk copies for the rest) from
 //       a producer warp with mbarriers; 8 consumer warps contract on the
@@ -28,12 +31,13 @@ namespace rssm {
 // precompute
 // ---------------------------------------------------------------------------
 template <int TP>
-__global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
+__global__ void __launch_bounds__(256, 4) precompute_kernel(StepArgs a) {
   __shared__ float Bf[kMaxL][kDstate + 4];
   __shared__ float Cf[TP][kDstate + 4];
   __shared__ float CB[TP][kMaxL];
   __shared__ float dtl[16][kMaxL];  // live dt' of up to 16 heads of the group
   __shared__ float dtn[16][kMaxT];  // new dt + dt_bias of up to 16 heads
+  __shared__ __align__(16) float cfs[8][kMaxL][TP];  // per warp: coef[k][t] of its current head
   __shared__ int meta[6];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
@@ -146,7 +150,6 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
     reinterpret_cast<uint32_t*>(cbg)[(t * kDstate + 16 * (((n >> 4) ^ t) & 7) + (n & 15)) >> 1] = w;
   }
   __syncthreads();
-  const int KB = a.KB;
   for (int hh = warp; hh < hpg; hh += 8) {
     const int h = g * hpg + hh;
     const float Ah = a.A[h], Dh = a.D[h];
@@ -182,16 +185,50 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
       cf[t] = v;
       dec[t] = t < Tb ? expf(cpt) : 0.0f;
     }
-    float* blk = a.coef + (static_cast<long long>(b) * H + h) * (KB + 1) * TP;
-    if (lane < KB) {
+    // ring term of this head: R[t][d] = sum_k coef[k][t] x_k[d] (lane k holds
+    // coef[k][.]); lane l accumulates d = 2l, 2l + 1.  The x rows of all K
+    // logical tokens are in the ring now (the new ones were appended above).
+    const uint32_t* xr = reinterpret_cast<const uint32_t*>(c.x_cache + static_cast<long long>(s) * c.x_stride +
+                                                           static_cast<long long>(h) * L * kDim);
+    float2 R[TP];
 #pragma unroll
-      for (int t4 = 0; t4 < TP; t4 += 4)
-        *reinterpret_cast<float4*>(blk + lane * TP + t4) = make_float4(cf[t4], cf[t4 + 1], cf[t4 + 2], cf[t4 + 3]);
+    for (int t = 0; t < TP; ++t) R[t] = make_float2(0.0f, 0.0f);
+    // coef[k][.] to shared memory, read back as broadcasts
+#pragma unroll
+    for (int t4 = 0; t4 < TP; t4 += 4)
+      *reinterpret_cast<float4*>(&cfs[warp][lane][t4]) = make_float4(cf[t4], cf[t4 + 1], cf[t4 + 2], cf[t4 + 3]);
+    __syncwarp();
+    for (int k0 = 0; k0 < K; k0 += 8) {
+      uint32_t xw[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) xw[e] = k0 + e < K ? xr[((r + k0 + e) % L) * (kDim / 2) + lane] : 0u;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        if (k0 + e < K) {
+          const float x0 = bf16lo(xw[e]), x1 = bf16hi(xw[e]);
+#pragma unroll
+          for (int t4 = 0; t4 < TP; t4 += 4) {
+            const float4 cv = *reinterpret_cast<const float4*>(&cfs[warp][k0 + e][t4]);
+            R[t4 + 0].x = fmaf(cv.x, x0, R[t4 + 0].x);
+            R[t4 + 0].y = fmaf(cv.x, x1, R[t4 + 0].y);
+            R[t4 + 1].x = fmaf(cv.y, x0, R[t4 + 1].x);
+            R[t4 + 1].y = fmaf(cv.y, x1, R[t4 + 1].y);
+            R[t4 + 2].x = fmaf(cv.z, x0, R[t4 + 2].x);
+            R[t4 + 2].y = fmaf(cv.z, x1, R[t4 + 2].y);
+            R[t4 + 3].x = fmaf(cv.w, x0, R[t4 + 3].x);
+            R[t4 + 3].y = fmaf(cv.w, x1, R[t4 + 3].y);
+          }
+        }
+      }
     }
+    __syncwarp();  // cfs is rewritten for the warp's next head
+    float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP);
+#pragma unroll
+    for (int t = 0; t < TP; ++t) reinterpret_cast<float2*>(blk + t * kDim)[lane] = R[t];
     if (lane == 0) {
 #pragma unroll
       for (int t4 = 0; t4 < TP; t4 += 4)
-        *reinterpret_cast<float4*>(blk + KB * TP + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
+        *reinterpret_cast<float4*>(blk + TP * kDim + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
     }
   }
 }
@@ -199,31 +236,30 @@ __global__ void __launch_bounds__(256) precompute_kernel(StepArgs a) {
 // ---------------------------------------------------------------------------
 // readout
 // ---------------------------------------------------------------------------
-// Per (row, head) unit the readout is two small dense contractions, done on
-// the tensor cores with mma.sync m16n8k16 (f32 accumulation):
+// Per (row, head) unit the readout is one small dense contraction on the
+// tensor cores, mma.sync m16n8k16 with f32 accumulation:
 //     Y^T[t][d] = sum_n Cblk[t][n] S0[d][n]        (M = t, N = d, K = dstate)
-//     R^T[t][d] = sum_k coef[k][t] x_k[d]           (K = ring rows, coef split
-//                                                    into bf16 hi + lo)
-//     y_t[d]    = decay_t scale_d Y^T[t][d] + R^T[t][d]
-// Warp w owns the 8 state rows d = 8w..8w+7 (one n8 tile).  K is taken in a
-// permuted order inside each 16-wide step (physical 4c..4c+3 <-> logical
-// 2c, 2c+1, 2c+8, 2c+9 for lane group c), so every operand fragment is one
-// 64-bit shared load; the sum over k is unchanged.  S0 arrives by TMA tensor
-// copies with the 128-byte swizzle, which keeps those loads conflict-free.
+//     y_t[d]    = decay_t scale_d Y^T[t][d] + R[t][d]
+// where the ring term R (live ring + new tokens) and decay_t come from the
+// precompute.  Warp w owns the 8 state rows d = 8w..8w+7 (one n8 tile).  K is
+// taken in a permuted order inside each 16-wide step (physical 4c..4c+3 <->
+// logical 2c, 2c+1, 2c+8, 2c+9 for lane group c), so every operand fragment is
+// one 64-bit shared load; the sum over k is unchanged.  S0 arrives by TMA
+// tensor copies with the 128-byte swizzle, which keeps those loads
+// conflict-free.
 struct ReadMeta {
   int b, h, s, r, p, Tb, tok0, flags;
 };
 
 struct ReadLayout {
-  int ns, KB;
-  uint32_t s0_bytes, scale_off, c_off, coef_off, x_off, stage_bytes;
+  int ns;
+  uint32_t s0_bytes, scale_off, c_off, r_off, r_bytes, stage_bytes;
   uint32_t stages_off, total;
 };
 
-__host__ __device__ inline ReadLayout read_layout(int dtype, int L, int TP, int ns) {
+__host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns) {
   ReadLayout f;
   f.ns = ns;
-  f.KB = (L + 3) & ~3;
   const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
   f.s0_bytes = kHeadElems * esz;  // esz boxes of 64 rows x 128 bytes
   uint32_t o = f.s0_bytes;
@@ -231,10 +267,9 @@ __host__ __device__ inline ReadLayout read_layout(int dtype, int L, int TP, int 
   if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
   f.c_off = o;
   o += 8 * kDstate * 2;
-  f.coef_off = o;
-  o += ((f.KB + 1) * TP * 4 + 15) & ~15;
-  f.x_off = o;
-  o += f.KB * kDim * 2;
+  f.r_off = o;
+  f.r_bytes = (TP * kDim + TP) * 4;
+  o += f.r_bytes;
   f.stage_bytes = (o + 1023) & ~1023u;  // the swizzled boxes need 1024-byte alignment
   f.stages_off = 1024;                  // barriers and per-stage metadata
   f.total = f.stages_off + ns * f.stage_bytes + 1024;  // + slack to align the base
@@ -326,7 +361,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Cache& c = a.c;
-  const ReadLayout lay = read_layout(DT, c.L, TP, ns);
+  const ReadLayout lay = read_layout(DT, TP, ns);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
   const int H = c.H;
@@ -351,7 +386,6 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   }
   __syncthreads();
 
-  const int KB = lay.KB;
   if (warp == kConsumerWarps) {
     // ---------------- producer: one lane issues all copies ----------------
     if (lane != 0) return;
@@ -372,7 +406,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         pre |= 1u << i;
       }
     }
-    pdl_wait();  // row records, C blocks, coefficients, appended x rows
+    pdl_wait();  // row records, C blocks, ring terms
     pdl_trigger();
     int cur_b = -1;
     RowRec rr = {};
@@ -393,12 +427,10 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       }
       meta[st] = ReadMeta{b, h, rr.s, rr.r, rr.p, rr.Tb, rr.tok0, rr.flags};
       if (rr.flags && rr.Tb > 0) {
-        const int s = rr.s, r = rr.r, K = rr.p + rr.Tb, g = h / c.hpg;
+        const int s = rr.s, g = h / c.hpg;
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
-        const uint32_t coef_bytes = (KB + 1) * TP * 4;
         const bool have_s0 = i < npre && ((pre >> i) & 1u);
-        const uint32_t bytes =
-            (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + 8 * kDstate * 2 + coef_bytes + K * kDim * 2;
+        const uint32_t bytes = (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + 8 * kDstate * 2 + lay.r_bytes;
         mbar_expect_tx(&full[st], bytes);
         if (!have_s0) {
 #pragma unroll
@@ -408,13 +440,8 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
         bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
                  &full[st]);
-        bulk_g2s(sb + lay.coef_off, a.coef + (static_cast<long long>(b) * H + h) * (KB + 1) * TP, coef_bytes,
+        bulk_g2s(sb + lay.r_off, a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP), lay.r_bytes,
                  &full[st]);
-        // live ring + the new rows the precompute appended: logical 0..K-1
-        const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * c.L * kDim;
-        const int n1 = min(K, c.L - r);
-        bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
-        if (K > n1) bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (K - n1) * kDim * 2, &full[st]);
       }
       mbar_arrive(&full[st]);
       issued = i + 1;
@@ -450,34 +477,11 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       if (lane == 0) mbar_arrive(&empty[st]);
       continue;
     }
-    const int K = m.p + m.Tb;
     float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
     s0_dot_c<DT>(sb, reinterpret_cast<const uint16_t*>(sb + lay.c_off), d, g, cq, acc);
-    // ring terms: sum_k coef[k][t] x_k[d]
-    const float* coef = reinterpret_cast<const float*>(sb + lay.coef_off);
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
-    float accr[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-#pragma unroll
-    for (int kb = 0; kb < 2; ++kb) {
-      if (kb * 16 < K) {
-        float v[4];
-        uint32_t xv[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int k = kb * 16 + 4 * cq + e;
-          const bool in = k < K;
-          v[e] = (in && g < TP) ? coef[k * TP + g] : 0.0f;
-          xv[e] = in ? static_cast<uint32_t>(xs[k * kDim + d]) : 0u;
-        }
-        const uint32_t h01 = pack_bf16(v[0], v[1]), h23 = pack_bf16(v[2], v[3]);
-        const uint32_t l01 = pack_bf16(v[0] - bf16_lo_f(h01), v[1] - bf16_hi_f(h01));
-        const uint32_t l23 = pack_bf16(v[2] - bf16_lo_f(h23), v[3] - bf16_hi_f(h23));
-        const uint32_t b0 = xv[0] | (xv[1] << 16), b1 = xv[2] | (xv[3] << 16);
-        mma_bf16(accr, h01, h23, b0, b1);
-        mma_bf16(accr, l01, l23, b0, b1);
-      }
-    }
-    const float dec = g < TP ? coef[KB * TP + g] : 0.0f;
+    const float* rb = reinterpret_cast<const float*>(sb + lay.r_off);
+    const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kDim + dout) : make_float2(0.0f, 0.0f);
+    const float dec = g < TP ? rb[TP * kDim + g] : 0.0f;
     float sc0 = 1.0f, sc1 = 1.0f;
     if constexpr (k8bit) {
       const float2 scv = *reinterpret_cast<const float2*>(sb + lay.scale_off + dout * 4);
@@ -486,8 +490,8 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
-    const float y0 = fmaf(dec * sc0, acc[0], accr[0]);
-    const float y1 = fmaf(dec * sc1, acc[1], accr[1]);
+    const float y0 = fmaf(dec * sc0, acc[0], rv.x);
+    const float y1 = fmaf(dec * sc1, acc[1], rv.y);
     if (g < m.Tb) {
       const __nv_bfloat162 yv = __floats2bfloat162_rn(y0, y1);
       *reinterpret_cast<__nv_bfloat162*>(a.out + (static_cast<long long>(m.tok0 + g) * H + m.h) * kDim + dout) = yv;
@@ -501,8 +505,14 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
 int launch_precompute(const StepArgs& a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = a.batch * a.c.G;
-  const cudaError_t e = a.TP == 4 ? launch_pdl(precompute_kernel<4>, dim3(grid), dim3(256), 0, st, a)
-                                   : launch_pdl(precompute_kernel<8>, dim3(grid), dim3(256), 0, st, a);
+  // four 256-thread CTAs per SM (64 registers); prefer shared memory over L1
+  cudaError_t e = a.TP == 4 ? cudaFuncSetAttribute(precompute_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                   cudaSharedmemCarveoutMaxShared)
+                            : cudaFuncSetAttribute(precompute_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                                   cudaSharedmemCarveoutMaxShared);
+  if (e != cudaSuccess) return e;
+  e = a.TP == 4 ? launch_pdl(precompute_kernel<4>, dim3(grid), dim3(256), 0, st, a)
+                : launch_pdl(precompute_kernel<8>, dim3(grid), dim3(256), 0, st, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -541,13 +551,13 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 8
   int ns = 8, ctas = 2;
   for (; ns >= 3; --ns)
-    if (read_layout(DT, a.c.L, TP, ns).total <= 113 * 1024) break;
+    if (read_layout(DT, TP, ns).total <= 113 * 1024) break;
   if (ns < 3) {
     ctas = 1;
     for (ns = 8; ns > 2; --ns)
-      if (read_layout(DT, a.c.L, TP, ns).total <= 225 * 1024) break;
+      if (read_layout(DT, TP, ns).total <= 225 * 1024) break;
   }
-  const ReadLayout lay = read_layout(DT, a.c.L, TP, ns);
+  const ReadLayout lay = read_layout(DT, TP, ns);
   CUtensorMap map;
   if (!encode_state_map(a.c, &map)) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
