@@ -246,7 +246,7 @@ def run_gpu(args, rank, ws, local):
                C=torch.zeros((max_tok, wl.ngroups, 128), dtype=torch.int16, device=dev),
                acc=torch.zeros(ids.size, dtype=torch.int32, device=dev),
                cu=torch.zeros(ids.size + 1, dtype=torch.int32, device=dev) if wl.varlen else None)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()  # noqa: E731
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a))  # noqa: E731  (host copies of the inputs)
     hin = [dict(x=pin(i.x.view(np.int16)), dt=pin(i.dt), B=pin(i.B.view(np.int16)), C=pin(i.C.view(np.int16)),
                 acc=pin(i.accepted), cu=None if i.cu_seqlens is None else pin(i.cu_seqlens), ntok=i.ntok)
            for i in host]
@@ -398,21 +398,35 @@ def run_gpu(args, rank, ws, local):
     # host memory and y goes back to it, inside the timed region
     e2e = None
     if not args.no_e2e:
+        # one set of pinned staging buffers, reused every step (as a serving
+        # engine does); the host fills it with the step's inputs before the
+        # timed region, which then holds H2D copy -> step -> D2H copy of y
+        stg = {key: torch.empty_like(buf[key], device="cpu").pin_memory() for key in ("x", "dt", "B", "C", "acc")}
+        if cu is not None:
+            stg["cu"] = torch.empty_like(cu, device="cpu").pin_memory()
         yh = torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16).pin_memory()
         e2e_ms, e2e_units, h2d, d2h = [], 0, 0, 0
         parts = {"h2d": [], "step": [], "d2h": []}
         for k in range(args.warmup, nsteps):
             hi = hin[k]
+            n = hi["ntok"]
+            for key in ("x", "dt", "B", "C"):
+                stg[key][:n].copy_(hi[key])
+            stg["acc"].copy_(hi["acc"])
+            if cu is not None:
+                stg["cu"].copy_(hi["cu"])
+            src = {key: (stg[key][:n] if key in ("x", "dt", "B", "C") else stg[key]) for key in stg}
+            src["ntok"] = n
             cold_l2()
             e0 = ev()
             e0.record(stream)
-            load_inputs(hi, non_blocking=True)
+            load_inputs(src, non_blocking=True)
             e_h = ev()
             e_h.record(stream)
             g_step.replay()
             e_g = ev()
             e_g.record(stream)
-            yh[: hi["ntok"]].copy_(out[: hi["ntok"]], non_blocking=True)
+            yh[:n].copy_(out[:n], non_blocking=True)
             e1 = ev()
             e1.record(stream)
             torch.cuda.synchronize()
@@ -421,14 +435,14 @@ def run_gpu(args, rank, ws, local):
             parts["step"].append(e_h.elapsed_time(e_g))
             parts["d2h"].append(e_g.elapsed_time(e1))
             e2e_units += step_units()[1]
-            h2d = sum(hi[key].numel() * hi[key].element_size() for key in ("x", "dt", "B", "C", "acc")) + (
-                0 if hi["cu"] is None else hi["cu"].numel() * 4)
-            d2h = hi["ntok"] * wl.nheads * 64 * 2
+            h2d = sum(src[key].numel() * src[key].element_size() for key in ("x", "dt", "B", "C", "acc")) + (
+                0 if cu is None else src["cu"].numel() * 4)
+            d2h = n * wl.nheads * 64 * 2
         t_e2e = max_over_ranks(sum(e2e_ms), ws, dev)
         e2e = {"value": sum_over_ranks(e2e_units, ws, dev) / (t_e2e / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "breakdown_us": {k: 1e3 * statistics.median(v) for k, v in parts.items()},
-               "host_buffers_pinned": bool(hin[0]["x"].is_pinned() and yh.is_pinned())}
+               "breakdown_us": {key: 1e3 * statistics.median(v) for key, v in parts.items()},
+               "staging": "pinned host buffers reused every step"}
 
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (sum(read_ms) / 1e3) / 1e9

@@ -66,12 +66,24 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase of an mbarrier: gives up after roughly a second.
+// Suspending test: the thread sleeps in hardware until the phase completes or
+// about `hint_ns` nanoseconds pass.
+__device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait on a phase of an mbarrier: gives up after about two seconds.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kWaitSpins; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (i >= 64) __nanosleep(256);
-  }
+  if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitTries; ++i)
+    if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
   return false;
 }
 // 1-D bulk copy global -> shared, completion counted in bytes on `bar`.

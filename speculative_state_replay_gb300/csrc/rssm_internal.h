@@ -17,7 +17,7 @@ constexpr int kMaxT = 8;      // draft tokens per step
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
-constexpr uint32_t kWaitSpins = 1u << 22;        // ~1 s of bounded mbarrier polling
+constexpr uint32_t kWaitTries = 2000;            // x 1 ms suspend hint: ~2 s bound on an mbarrier wait
 
 // device view of an rssm_cache
 struct Cache {
