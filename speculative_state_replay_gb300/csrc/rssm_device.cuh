@@ -95,6 +95,15 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// Per-thread asynchronous copies global -> shared (16 bytes through L2 only,
+// or 4 bytes), all of a thread's copies completed by cp_async_wait_all().
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // Programmatic dependent launch.  pdl_wait() returns once the preceding kernel
 // in the stream has completed and its writes are visible (immediately when the
 // kernel was launched without the attribute); every chain kernel calls it

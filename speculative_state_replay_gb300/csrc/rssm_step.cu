@@ -30,205 +30,231 @@ namespace rssm {
 // ---------------------------------------------------------------------------
 // precompute
 // ---------------------------------------------------------------------------
+// The precompute's inputs all come in through shared memory in one round of
+// asynchronous copies, issued as soon as the row's ring start is known; the
+// kernel is a short chain of dependent steps per CTA (every CTA of a step fits
+// in one wave), so its time is the latency of that chain.  Dynamic shared
+// memory, one (row, group):
+//   xs [hcm][L][64]        bf16  x rows of a chunk of hcm = min(hpg, 16) of
+//                                the group's heads by logical token k (live
+//                                ring rows, then new)
+//   bs [L][128]            bf16  B rows by logical token k
+//   cs [8][128]            bf16  C rows of the new tokens
+constexpr int kHeadChunk = 16;
+__host__ __device__ inline int head_chunk(int hpg) { return hpg < kHeadChunk ? hpg : kHeadChunk; }
+inline size_t precompute_smem(int hpg, int L) {
+  return static_cast<size_t>(head_chunk(hpg)) * L * kDim * 2 + static_cast<size_t>(L) * kDstate * 2 + 8 * kDstate * 2;
+}
+
 template <int TP>
-__global__ void __launch_bounds__(256, 4) precompute_kernel(StepArgs a) {
-  __shared__ float Bf[kMaxL][kDstate + 4];
-  __shared__ float Cf[TP][kDstate + 4];
+__global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepArgs a) {
+  extern __shared__ __align__(16) unsigned char psm[];
   __shared__ float CB[TP][kMaxL];
-  __shared__ float dtl[16][kMaxL];  // live dt' of up to 16 heads of the group
-  __shared__ float dtn[16][kMaxT];  // new dt + dt_bias of up to 16 heads
+  __shared__ float dts[kHeadChunk][kMaxL];  // dt' of the live tokens; dt of the new ones (before bias, softplus)
+  __shared__ float hp[3][kHeadChunk];       // A, D, dt_bias of the chunk's heads
   __shared__ __align__(16) float cfs[8][kMaxL][TP];  // per warp: coef[k][t] of its current head
   __shared__ int meta[6];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int L = c.L, H = c.H, G = c.G, hpg = c.hpg;
+  uint16_t* xs = reinterpret_cast<uint16_t*>(psm);
+  uint16_t* bs = xs + head_chunk(hpg) * L * kDim;
+  uint16_t* cs = bs + L * kDstate;
   pdl_wait();  // the flush's bookkeeping and checkpoints are complete from here on
   pdl_trigger();
-  if (tid == 0) {
-    const int s = a.slot_idx[b];
-    int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
-    const int tok0 = a.cu ? a.cu[b] : b * a.T;
-    int flags = 0, p = 0, r = 0;
-    const bool tb_ok = Tb >= 0 && Tb <= a.T;
-    if (s >= 1 && s < c.S) {
-      if (!tb_ok) {
-        if (g == 0) set_error(c.err, RSSM_ERRBIT_SEQLEN);
-      } else {
-        p = a.pnat[b];
-        if (p < 0 || p + Tb > c.L) {
+  if (warp == 0) {
+    // the row's scalars in one round trip, then its ring start
+    int v = 0;
+    if (lane == 0) v = a.slot_idx[b];
+    else if (lane == 1) v = a.pnat[b];
+    else if (lane == 2) v = a.cu ? a.cu[b] : b * a.T;
+    else if (lane == 3) v = a.cu ? a.cu[b + 1] : (b + 1) * a.T;
+    const int s = __shfl_sync(0xffffffffu, v, 0), pn = __shfl_sync(0xffffffffu, v, 1);
+    const int tok0 = __shfl_sync(0xffffffffu, v, 2), tok1 = __shfl_sync(0xffffffffu, v, 3);
+    if (lane == 0) {
+      int Tb = tok1 - tok0, flags = 0, p = 0, r = 0;
+      const bool tb_ok = Tb >= 0 && Tb <= a.T;
+      if (s >= 1 && s < c.S) {
+        if (!tb_ok) {
+          if (g == 0) set_error(c.err, RSSM_ERRBIT_SEQLEN);
+        } else if (pn < 0 || pn + Tb > L) {
           if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);
         } else {
+          p = pn;
           r = c.ring_start[s];
           flags = 1;
         }
       }
+      if (!tb_ok) Tb = 0;
+      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags;
+      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, {0, 0}};
     }
-    if (!tb_ok) Tb = 0;
-    meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags;
-    if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, {0, 0}};
   }
   __syncthreads();
   const int s = meta[0], r = meta[1], p = meta[2], Tb = meta[3], tok0 = meta[4];
   if (!meta[5] || Tb == 0) return;
-  const int K = p + Tb, L = c.L, H = c.H, G = c.G, hpg = c.hpg;
+  const int K = p + Tb;  // logical tokens: p live ring rows, then the Tb new ones
+  auto ring = [&](int k) {  // ring slot of logical token k < L
+    const int q = r + k;
+    return q >= L ? q - L : q;
+  };
   uint16_t* bring = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
-  // independent loads first: B rows (live ring + new), C rows, live dt' of the group's heads
-  for (int idx = tid; idx < K * (kDstate / 2); idx += 256) {
-    const int k = idx >> 6, q = idx & 63;
-    const uint16_t* src = k < p ? bring + ((r + k) % L) * kDstate
+  uint16_t* xslot = c.x_cache + static_cast<long long>(s) * c.x_stride;
+  float* dslot = c.dt_cache + static_cast<long long>(s) * c.dt_stride;
+  // B and C rows of the group
+  for (int idx = tid; idx < K * 16; idx += 256) {
+    const int k = idx >> 4, q = idx & 15;
+    const uint16_t* src = k < p ? bring + ring(k) * kDstate
                                 : a.B + (static_cast<long long>(tok0 + k - p) * G + g) * kDstate;
-    const uint32_t w = reinterpret_cast<const uint32_t*>(src)[q];
-    Bf[k][2 * q] = bf16lo(w);
-    Bf[k][2 * q + 1] = bf16hi(w);
+    cp_async16(bs + k * kDstate + q * 8, src + q * 8);
   }
-  for (int idx = tid; idx < TP * (kDstate / 2); idx += 256) {
-    const int t = idx >> 6, q = idx & 63;
-    float2 v = make_float2(0.0f, 0.0f);
-    if (t < Tb) {
-      const uint32_t w =
-          reinterpret_cast<const uint32_t*>(a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate)[q];
-      v = make_float2(bf16lo(w), bf16hi(w));
-    }
-    Cf[t][2 * q] = v.x;
-    Cf[t][2 * q + 1] = v.y;
+  if (tid < Tb * 16) {
+    const int t = tid >> 4, q = tid & 15;
+    cp_async16(cs + t * kDstate + q * 8, a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate + q * 8);
   }
-  const int hl = hpg < 16 ? hpg : 16;
-  for (int idx = tid; idx < hl * p; idx += 256) {
-    const int hh = idx / p, k = idx % p;
-    dtl[hh][k] = c.dt_cache[static_cast<long long>(s) * c.dt_stride + static_cast<long long>(g * hpg + hh) * L +
-                            (r + k) % L];
-  }
-  for (int idx = tid; idx < hl * Tb; idx += 256) {
-    const int hh = idx / Tb, t = idx % Tb, h = g * hpg + hh;
-    dtn[hh][t] = __fadd_rn(a.dt[static_cast<long long>(tok0 + t) * H + h], a.dt_bias[h]);
-  }
-  // ring appends: the new B rows (once per group) and the new x rows of the group's heads
-  for (int idx = tid; idx < Tb * 16; idx += 256) {
-    const int t = idx >> 4, q = idx & 15;
-    const uint4 v = reinterpret_cast<const uint4*>(a.B + (static_cast<long long>(tok0 + t) * G + g) * kDstate)[q];
-    reinterpret_cast<uint4*>(bring + ((r + p + t) % L) * kDstate)[q] = v;
-  }
-  for (int idx = tid; idx < Tb * hpg * 8; idx += 256) {
-    const int t = idx / (hpg * 8), rem = idx % (hpg * 8), hh = rem >> 3, q = rem & 7;
-    const int h = g * hpg + hh;
-    const uint4 v = reinterpret_cast<const uint4*>(a.x + (static_cast<long long>(tok0 + t) * H + h) * kDim)[q];
-    uint16_t* dst = c.x_cache + static_cast<long long>(s) * c.x_stride + (static_cast<long long>(h) * L + (r + p + t) % L) * kDim;
-    reinterpret_cast<uint4*>(dst)[q] = v;
-  }
-  __syncthreads();
-  // C.B contraction, one warp per (t, k) pair, lanes over dstate
-  for (int pr = warp; pr < Tb * K; pr += 8) {
-    const int t = pr / K, k = pr % K;
-    float v = 0.0f;
-    if (k <= p + t) {
-#pragma unroll
-      for (int n = lane; n < kDstate; n += 32) v = fmaf(Cf[t][n], Bf[k][n], v);
-#pragma unroll
-      for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
-    }
-    if (lane == 0) CB[t][k] = v;
-  }
-  // the C block for the readout's tensor-core contraction: [8][128] in the
-  // MMA operand type (bf16 for f32/bf16 checkpoints, fp16 otherwise), rows
-  // t >= T_b zero, 32-byte quads of row t rotated by t
-  uint16_t* cbg = a.cf + (static_cast<long long>(b) * G + g) * 8 * kDstate;
   const bool c_f16 = c.dtype == RSSM_F16 || c.dtype == RSSM_I8 || c.dtype == RSSM_E4M3;
-  for (int idx = tid; idx < 8 * (kDstate / 2); idx += 256) {
-    const int t = idx >> 6, q = idx & 63;
-    const float v0 = t < TP ? Cf[t][2 * q] : 0.0f, v1 = t < TP ? Cf[t][2 * q + 1] : 0.0f;
-    uint32_t w;
-    if (c_f16) {
-      const __half2 h = __floats2half2_rn(v0, v1);
-      w = *reinterpret_cast<const uint32_t*>(&h);
-    } else {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(v0, v1);
-      w = *reinterpret_cast<const uint32_t*>(&h);
-    }
-    // 32-byte quad j = n/16 of row t stored at quad j ^ t: the readout's
-    // per-row fragment loads then fall on distinct banks
-    const int n = 2 * q;
-    reinterpret_cast<uint32_t*>(cbg)[(t * kDstate + 16 * (((n >> 4) ^ t) & 7) + (n & 15)) >> 1] = w;
-  }
-  __syncthreads();
-  for (int hh = warp; hh < hpg; hh += 8) {
-    const int h = g * hpg + hh;
-    const float Ah = a.A[h], Dh = a.D[h];
-    float* dtrow = c.dt_cache + static_cast<long long>(s) * c.dt_stride + static_cast<long long>(h) * L;
-    float dtp = 0.0f;
-    if (lane < p) {
-      dtp = hh < 16 ? dtl[hh][lane] : dtrow[(r + lane) % L];
-    } else if (lane < K) {
-      const int t = lane - p;
-      const float v = hh < 16 ? dtn[hh][t] : __fadd_rn(a.dt[static_cast<long long>(tok0 + t) * H + h], a.dt_bias[h]);
-      dtp = spec_softplus(v);  // the value stored in the ring: fixed-sequence softplus
-      dtrow[(r + p + t) % L] = dtp;
-    }
-    // inclusive prefix sum of A dt' over the lanes (these sums only feed the
-    // outputs, so any summation order is fine here)
-    float cum = lane < K ? Ah * dtp : 0.0f;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const float x = __shfl_up_sync(0xffffffffu, cum, off);
-      if (lane >= off) cum += x;
-    }
-    float cf[TP];
-    float dec[TP];
-#pragma unroll
-    for (int t = 0; t < TP; ++t) {
-      const int kt = p + t < 31 ? p + t : 31;
-      const float cpt = __shfl_sync(0xffffffffu, cum, kt);
-      float v = 0.0f;
-      if (t < Tb && lane <= p + t) {
-        v = expf(cpt - cum) * dtp * CB[t][lane];
-        if (lane == p + t) v += Dh;
+  for (int h0 = 0; h0 < hpg; h0 += kHeadChunk) {
+    const int hc = hpg - h0 < kHeadChunk ? hpg - h0 : kHeadChunk, hb = g * hpg + h0;
+    if (h0) __syncthreads();  // every warp is done with the previous chunk's rows
+    // x rows of the chunk's heads: one 16-byte piece per thread and head (K * 8 <= 256)
+    if (tid < K * 8) {
+      const int k = tid >> 3, q = tid & 7;
+      for (int hh = 0; hh < hc; ++hh) {
+        const uint16_t* src = k < p ? xslot + (static_cast<long long>(hb + hh) * L + ring(k)) * kDim
+                                    : a.x + (static_cast<long long>(tok0 + k - p) * H + hb + hh) * kDim;
+        cp_async16(xs + (hh * L + k) * kDim + q * 8, src + q * 8);
       }
-      cf[t] = v;
-      dec[t] = t < Tb ? expf(cpt) : 0.0f;
     }
-    // ring term of this head: R[t][d] = sum_k coef[k][t] x_k[d] (lane k holds
-    // coef[k][.]); lane l accumulates d = 2l, 2l + 1.  The x rows of all K
-    // logical tokens are in the ring now (the new ones were appended above).
-    const uint32_t* xr = reinterpret_cast<const uint32_t*>(c.x_cache + static_cast<long long>(s) * c.x_stride +
-                                                           static_cast<long long>(h) * L * kDim);
-    float2 R[TP];
+    for (int idx = tid; idx < hc * 32; idx += 256) {
+      const int hh = idx >> 5, k = idx & 31;
+      if (k < K) {
+        const float* src = k < p ? dslot + static_cast<long long>(hb + hh) * L + ring(k)
+                                 : a.dt + static_cast<long long>(tok0 + k - p) * H + hb + hh;
+        cp_async4(&dts[hh][k], src);
+      }
+    }
+    if (tid < hc) {
+      cp_async4(&hp[0][tid], a.A + hb + tid);
+      cp_async4(&hp[1][tid], a.D + hb + tid);
+      cp_async4(&hp[2][tid], a.dt_bias + hb + tid);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    if (h0 == 0) {
+      // ring append of the new B rows
+      if (tid < Tb * 16) {
+        const int t = tid >> 4, q = tid & 15;
+        reinterpret_cast<uint4*>(bring + ring(p + t) * kDstate)[q] =
+            reinterpret_cast<const uint4*>(bs + (p + t) * kDstate)[q];
+      }
+      // C.B contraction, one warp per (t, k) pair with k <= p + t, 4 dstate entries a lane
+      for (int pr = warp; pr < Tb * K; pr += 8) {
+        const int t = pr / K, k = pr % K;
+        float v = 0.0f;
+        if (k <= p + t) {
+          const uint2 cw = reinterpret_cast<const uint2*>(cs + t * kDstate)[lane];
+          const uint2 bw = reinterpret_cast<const uint2*>(bs + k * kDstate)[lane];
+          v = fmaf(bf16lo(cw.x), bf16lo(bw.x), v);
+          v = fmaf(bf16hi(cw.x), bf16hi(bw.x), v);
+          v = fmaf(bf16lo(cw.y), bf16lo(bw.y), v);
+          v = fmaf(bf16hi(cw.y), bf16hi(bw.y), v);
 #pragma unroll
-    for (int t = 0; t < TP; ++t) R[t] = make_float2(0.0f, 0.0f);
-    // coef[k][.] to shared memory, read back as broadcasts
-#pragma unroll
-    for (int t4 = 0; t4 < TP; t4 += 4)
-      *reinterpret_cast<float4*>(&cfs[warp][lane][t4]) = make_float4(cf[t4], cf[t4 + 1], cf[t4 + 2], cf[t4 + 3]);
-    __syncwarp();
-    for (int k0 = 0; k0 < K; k0 += 8) {
-      uint32_t xw[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) xw[e] = k0 + e < K ? xr[((r + k0 + e) % L) * (kDim / 2) + lane] : 0u;
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        if (k0 + e < K) {
-          const float x0 = bf16lo(xw[e]), x1 = bf16hi(xw[e]);
-#pragma unroll
-          for (int t4 = 0; t4 < TP; t4 += 4) {
-            const float4 cv = *reinterpret_cast<const float4*>(&cfs[warp][k0 + e][t4]);
-            R[t4 + 0].x = fmaf(cv.x, x0, R[t4 + 0].x);
-            R[t4 + 0].y = fmaf(cv.x, x1, R[t4 + 0].y);
-            R[t4 + 1].x = fmaf(cv.y, x0, R[t4 + 1].x);
-            R[t4 + 1].y = fmaf(cv.y, x1, R[t4 + 1].y);
-            R[t4 + 2].x = fmaf(cv.z, x0, R[t4 + 2].x);
-            R[t4 + 2].y = fmaf(cv.z, x1, R[t4 + 2].y);
-            R[t4 + 3].x = fmaf(cv.w, x0, R[t4 + 3].x);
-            R[t4 + 3].y = fmaf(cv.w, x1, R[t4 + 3].y);
-          }
+          for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
         }
+        if (lane == 0) CB[t][k] = v;
       }
+      // the C block for the readout's tensor-core contraction: [8][128] in the
+      // MMA operand type (bf16 for f32/bf16 checkpoints, fp16 otherwise), rows
+      // t >= T_b zero; 32-byte quad j of row t is stored at quad j ^ t, so the
+      // readout's per-row fragment loads fall on distinct banks
+      uint16_t* cbg = a.cf + (static_cast<long long>(b) * G + g) * 8 * kDstate;
+      for (int idx = tid; idx < 8 * (kDstate / 2); idx += 256) {
+        const int t = idx >> 6, q = idx & 63, n = 2 * q;
+        uint32_t w = t < Tb ? reinterpret_cast<const uint32_t*>(cs + t * kDstate)[q] : 0u;
+        if (c_f16) {
+          const __half2 hv = __floats2half2_rn(bf16lo(w), bf16hi(w));
+          w = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        reinterpret_cast<uint32_t*>(cbg)[(t * kDstate + 16 * (((n >> 4) ^ t) & 7) + (n & 15)) >> 1] = w;
+      }
+      __syncthreads();
     }
-    __syncwarp();  // cfs is rewritten for the warp's next head
-    float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP);
+    // ring appends of the chunk's new x rows
+    for (int idx = tid; idx < hc * 64; idx += 256) {
+      const int hh = idx >> 6, t = (idx >> 3) & 7, q = idx & 7;
+      if (t < Tb)
+        reinterpret_cast<uint4*>(xslot + (static_cast<long long>(hb + hh) * L + ring(p + t)) * kDim)[q] =
+            reinterpret_cast<const uint4*>(xs + (hh * L + p + t) * kDim)[q];
+    }
+    for (int hh = warp; hh < hc; hh += 8) {
+      const int h = hb + hh;
+      const float Ah = hp[0][hh], Dh = hp[1][hh];
+      float dtp = 0.0f;
+      if (lane < p) {
+        dtp = dts[hh][lane];
+      } else if (lane < K) {
+        dtp = spec_softplus(__fadd_rn(dts[hh][lane], hp[2][hh]));  // the value stored in the ring
+        dslot[static_cast<long long>(h) * L + ring(lane)] = dtp;
+      }
+      // inclusive prefix sum of A dt' over the lanes (these sums only feed the
+      // outputs, so any summation order is fine here)
+      float cum = lane < K ? Ah * dtp : 0.0f;
 #pragma unroll
-    for (int t = 0; t < TP; ++t) reinterpret_cast<float2*>(blk + t * kDim)[lane] = R[t];
-    if (lane == 0) {
+      for (int off = 1; off < 32; off <<= 1) {
+        const float x = __shfl_up_sync(0xffffffffu, cum, off);
+        if (lane >= off) cum += x;
+      }
+      float cf[TP];
+      float dec[TP];
+#pragma unroll
+      for (int t = 0; t < TP; ++t) {
+        const int kt = p + t < 31 ? p + t : 31;
+        const float cpt = __shfl_sync(0xffffffffu, cum, kt);
+        float v = 0.0f;
+        if (t < Tb && lane <= p + t) {
+          v = expf(cpt - cum) * dtp * CB[t][lane];
+          if (lane == p + t) v += Dh;
+        }
+        cf[t] = v;
+        dec[t] = t < Tb ? expf(cpt) : 0.0f;
+      }
+      // ring term of this head: R[t][d] = sum_k coef[k][t] x_k[d]; lane k
+      // holds coef[k][.], shared through cfs; lane l accumulates d = 2l, 2l + 1
 #pragma unroll
       for (int t4 = 0; t4 < TP; t4 += 4)
-        *reinterpret_cast<float4*>(blk + TP * kDim + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
+        *reinterpret_cast<float4*>(&cfs[warp][lane][t4]) = make_float4(cf[t4], cf[t4 + 1], cf[t4 + 2], cf[t4 + 3]);
+      __syncwarp();
+      float2 R[TP];
+#pragma unroll
+      for (int t = 0; t < TP; ++t) R[t] = make_float2(0.0f, 0.0f);
+      const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + hh * L * kDim) + lane;
+#pragma unroll 4
+      for (int k = 0; k < K; ++k) {
+        const uint32_t w = xr[k * (kDim / 2)];
+        const float x0 = bf16lo(w), x1 = bf16hi(w);
+#pragma unroll
+        for (int t4 = 0; t4 < TP; t4 += 4) {
+          const float4 cv = *reinterpret_cast<const float4*>(&cfs[warp][k][t4]);
+          R[t4 + 0].x = fmaf(cv.x, x0, R[t4 + 0].x);
+          R[t4 + 0].y = fmaf(cv.x, x1, R[t4 + 0].y);
+          R[t4 + 1].x = fmaf(cv.y, x0, R[t4 + 1].x);
+          R[t4 + 1].y = fmaf(cv.y, x1, R[t4 + 1].y);
+          R[t4 + 2].x = fmaf(cv.z, x0, R[t4 + 2].x);
+          R[t4 + 2].y = fmaf(cv.z, x1, R[t4 + 2].y);
+          R[t4 + 3].x = fmaf(cv.w, x0, R[t4 + 3].x);
+          R[t4 + 3].y = fmaf(cv.w, x1, R[t4 + 3].y);
+        }
+      }
+      __syncwarp();  // cfs is rewritten for the warp's next head
+      float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP);
+#pragma unroll
+      for (int t = 0; t < TP; ++t) reinterpret_cast<float2*>(blk + t * kDim)[lane] = R[t];
+      if (lane == 0) {
+#pragma unroll
+        for (int t4 = 0; t4 < TP; t4 += 4)
+          *reinterpret_cast<float4*>(blk + TP * kDim + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
+      }
     }
   }
 }
@@ -286,14 +312,14 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
 }
 
 __device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
 }
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
@@ -311,28 +337,37 @@ __device__ __forceinline__ uint32_t swz(int d, int kbyte) {
   return static_cast<uint32_t>(d * 128 + ((((kbyte >> 4) ^ d) & 7) << 4) + (kbyte & 15));
 }
 
-// S0 . C over dstate for state rows d (lane's B column) of this warp
+// A fragments of the C block for lane (g, c): row t = g, logical k = 16 ks +
+// {2c, 2c+1, 2c+8, 2c+9} (physical 16 ks + 4c .. 4c+3), one 64-bit load per k step
+__device__ __forceinline__ void load_c_frags(const uint16_t* cblk, int g, int c, uint2 (&af)[8]) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) af[ks] = *reinterpret_cast<const uint2*>(cblk + g * kDstate + 16 * ((ks ^ g) & 7) + 4 * c);
+}
+
+// S0 . C over dstate for state rows d (lane's B column) of this warp; even and
+// odd k steps accumulate in separate chains, added at the end
 template <int DT>
-__device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint16_t* cblk, int d, int g, int c,
-                                         float (&acc)[4]) {
+__device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8], int d, int c, float (&acc)[4]) {
+  float a2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
-    const uint2 av = *reinterpret_cast<const uint2*>(cblk + g * kDstate + 16 * ((ks ^ g) & 7) + 4 * c);
+    const uint2 av = af[ks];
+    float(&ac)[4] = a2[ks & 1];
     if constexpr (DT == RSSM_BF16 || DT == RSSM_F16) {
       const int kb = (ks * 16 + 4 * c) * 2;  // byte within the 256-byte row
       const uint2 bv = *reinterpret_cast<const uint2*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
       if constexpr (DT == RSSM_BF16)
-        mma_bf16(acc, av.x, av.y, bv.x, bv.y);
+        mma_bf16(ac, av.x, av.y, bv.x, bv.y);
       else
-        mma_f16(acc, av.x, av.y, bv.x, bv.y);
+        mma_f16(ac, av.x, av.y, bv.x, bv.y);
     } else if constexpr (DT == RSSM_F32) {
       const int kb = (ks * 16 + 4 * c) * 4;
       const float4 f = *reinterpret_cast<const float4*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
       const uint32_t h01 = pack_bf16(f.x, f.y), h23 = pack_bf16(f.z, f.w);
       const uint32_t l01 = pack_bf16(f.x - bf16_lo_f(h01), f.y - bf16_hi_f(h01));
       const uint32_t l23 = pack_bf16(f.z - bf16_lo_f(h23), f.w - bf16_hi_f(h23));
-      mma_bf16(acc, av.x, av.y, h01, h23);
-      mma_bf16(acc, av.x, av.y, l01, l23);
+      mma_bf16(a2[0], av.x, av.y, h01, h23);
+      mma_bf16(a2[1], av.x, av.y, l01, l23);
     } else {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(s0 + swz(d, ks * 16 + 4 * c));
       uint32_t b0, b1;
@@ -351,9 +386,11 @@ __device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint16_t* cblk
         b0 = static_cast<uint32_t>(r01.x) | (static_cast<uint32_t>(r01.y) << 16);
         b1 = static_cast<uint32_t>(r23.x) | (static_cast<uint32_t>(r23.y) << 16);
       }
-      mma_f16(acc, av.x, av.y, b0, b1);
+      mma_f16(ac, av.x, av.y, b0, b1);
     }
   }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) acc[j] = a2[0][j] + a2[1][j];
 }
 
 template <int DT, int TP>
@@ -408,7 +445,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     }
     pdl_wait();  // row records, C blocks, ring terms
     pdl_trigger();
-    int cur_b = -1;
+    int cur_b = -1, cur_bg = -1;
     RowRec rr = {};
     int issued = 0;
     bool ok = true;
@@ -425,12 +462,19 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         rr = a.rows[b];
         cur_b = b;
       }
-      meta[st] = ReadMeta{b, h, rr.s, rr.r, rr.p, rr.Tb, rr.tok0, rr.flags};
-      if (rr.flags && rr.Tb > 0) {
-        const int s = rr.s, g = h / c.hpg;
+      const bool active = rr.flags && rr.Tb > 0;
+      const int g = h / c.hpg, bg = b * c.G + g;
+      // the C block is copied only when the (row, group) changes: consumers
+      // keep its fragments in registers (flags bit 1 tells them to reload)
+      const bool newc = active && bg != cur_bg;
+      if (active) cur_bg = bg;
+      meta[st] = ReadMeta{b, h, rr.s, rr.r, rr.p, rr.Tb, rr.tok0, (active ? 1 : 0) | (newc ? 2 : 0)};
+      if (active) {
+        const int s = rr.s;
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
         const bool have_s0 = i < npre && ((pre >> i) & 1u);
-        const uint32_t bytes = (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + 8 * kDstate * 2 + lay.r_bytes;
+        const uint32_t bytes =
+            (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + (newc ? 8u * kDstate * 2 : 0u) + lay.r_bytes;
         mbar_expect_tx(&full[st], bytes);
         if (!have_s0) {
 #pragma unroll
@@ -438,8 +482,9 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         }
         if (k8bit)
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
-        bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
-                 &full[st]);
+        if (newc)
+          bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
+                   &full[st]);
         bulk_g2s(sb + lay.r_off, a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP), lay.r_bytes,
                  &full[st]);
       }
@@ -457,6 +502,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   const int g = lane >> 2, cq = lane & 3;
   const int d = 8 * warp + g;        // B column (row of S0) this lane loads
   const int dout = 8 * warp + 2 * cq;  // output rows this lane writes (dout, dout + 1)
+  uint2 af[8];                          // C block fragments of the current (row, group)
   for (int i = 0; i < nu; ++i) {
     const int st = i % ns;
     const uint32_t ph = (i / ns) & 1;
@@ -466,7 +512,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     }
     const ReadMeta m = meta[st];
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
-    if (!(m.flags && m.Tb > 0)) {
+    if (!(m.flags & 1)) {
       // inactive or rejected row: zero outputs, no cache update
       for (int idx = lane; idx < m.Tb * 4; idx += 32) {
         const int t = idx >> 2, q = idx & 3;
@@ -477,8 +523,9 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       if (lane == 0) mbar_arrive(&empty[st]);
       continue;
     }
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    s0_dot_c<DT>(sb, reinterpret_cast<const uint16_t*>(sb + lay.c_off), d, g, cq, acc);
+    if (m.flags & 2) load_c_frags(reinterpret_cast<const uint16_t*>(sb + lay.c_off), g, cq, af);
+    float acc[4];
+    s0_dot_c<DT>(sb, af, d, cq, acc);
     const float* rb = reinterpret_cast<const float*>(sb + lay.r_off);
     const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kDim + dout) : make_float2(0.0f, 0.0f);
     const float dec = g < TP ? rb[TP * kDim + g] : 0.0f;
@@ -505,14 +552,14 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
 int launch_precompute(const StepArgs& a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const int grid = a.batch * a.c.G;
-  // four 256-thread CTAs per SM (64 registers); prefer shared memory over L1
-  cudaError_t e = a.TP == 4 ? cudaFuncSetAttribute(precompute_kernel<4>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                   cudaSharedmemCarveoutMaxShared)
-                            : cudaFuncSetAttribute(precompute_kernel<8>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                                   cudaSharedmemCarveoutMaxShared);
-  if (e != cudaSuccess) return e;
-  e = a.TP == 4 ? launch_pdl(precompute_kernel<4>, dim3(grid), dim3(256), 0, st, a)
-                : launch_pdl(precompute_kernel<8>, dim3(grid), dim3(256), 0, st, a);
+  const size_t smem = precompute_smem(a.c.hpg, a.c.L);
+  // 256-thread CTAs, four per SM at T <= 4 (64 registers, ~55 KB of shared
+  // memory at L = 20), three at T <= 8
+  auto kern = a.TP == 4 ? precompute_kernel<4> : precompute_kernel<8>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(precompute_smem(kHeadChunk, kMaxL)));
+  if (e == cudaSuccess) e = launch_pdl(kern, dim3(grid), dim3(256), smem, st, a);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
