@@ -1,12 +1,15 @@
 """Benchmark: one decode step of the ReplaySSM checkpointing SSU on GB300.
 
-A step = rssm_flush (classify + fold) -> rssm_step (precompute + readout) ->
-rssm_accept over one batch of synthetic decode inputs.  Default workload:
+A step = flush + step + accept over one batch of synthetic decode inputs:
+by default (--path split) rssm_flush (classify + fold) -> rssm_step
+(precompute + readout) -> rssm_accept; with --path fused, rssm_flush_step
+(flush decision + precompute, then the fused fold + readout) -> rssm_accept.  Default workload:
 Mamba-2-style decode, batch 64 of 256 slots, 128 heads, 8 groups, bf16
 checkpoints, window 16, T = 4 drafts.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config NAME] [--force-flush] [--no-e2e] [--no-cpu-baseline]
+                    [--config NAME] [--path fused|split] [--force-flush] [--no-e2e]
+                    [--no-cpu-baseline]
 
 Timing: W untimed warm-up steps, then K steps, each one CUDA graph (the
 library's kernels chained by programmatic dependent launch) bracketed by CUDA
@@ -49,6 +52,8 @@ def parse():
     ap.add_argument("--config", default="mamba2_decode")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--force-flush", action="store_true", help="flush every active row every step")
+    ap.add_argument("--path", default="split", choices=["fused", "split"],
+                    help="fused: rssm_flush_step; split: rssm_flush then rssm_step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU budget of the oracle baseline sample")
@@ -182,11 +187,33 @@ def algorithmic_bytes(wl, rows_rec, ntok_b, esz):
     total = 0
     hpg = wl.hpg
     for (s, r, p, Tb, tok0, flags) in rows_rec:
-        if flags and Tb > 0:
+        if (flags & 1) and Tb > 0:
             per_head = 64 * 128 * esz + (256 if esz == 1 else 0) + Tb * 256 / hpg + Tb * 128
             total += per_head * wl.nheads
         elif Tb > 0:
             total += Tb * 128 * wl.nheads
+    return total
+
+
+def fused_bytes(wl, rows_rec, esz):
+    """Algorithmic HBM bytes of one fused fold + readout launch from its
+    per-row records (s, r, p, Tb, tok0, flags, p_old, epoch): S0 (+ scales)
+    read once per (row, head) that is read out or folded; for rows read out the
+    group's C rows shared by its heads and y; for folded rows the new S0 (+
+    scales) written and the live x rows, dt' and the group's live B rows; rows
+    without outputs write zeros."""
+    total = 0
+    hpg = wl.hpg
+    s0 = 64 * 128 * esz + (256 if esz == 1 else 0)
+    for (s, r, p, Tb, tok0, flags, p_old, ep) in rows_rec:
+        out_ok, fo = (flags & 1) and Tb > 0, flags & 2
+        per_head = 0
+        if out_ok or fo:
+            per_head += s0
+        per_head += (Tb * 256 / hpg + Tb * 128) if out_ok else Tb * 128
+        if fo:
+            per_head += s0 + p_old * (128 + 4) + p_old * 256 / hpg
+        total += per_head * wl.nheads
     return total
 
 
@@ -290,7 +317,20 @@ def run_gpu(args, rank, ws, local):
     def g_acc():
         api.rssm_accept(gc, gids, pnat, buf["acc"], wl.T, cu_seqlens=cu)
 
-    groups = [g_flush, g_pre, g_read, g_acc]
+    def g_fpre():
+        api.rssm_flush_step_precompute(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
+                                       scr_step, cu_seqlens=cu, force=force, seed=wl.sr_seed)
+
+    def g_fread():
+        api.rssm_flush_step_readout(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
+                                    scr_step, cu_seqlens=cu, force=force, seed=wl.sr_seed)
+
+    fused = args.path == "fused"
+    # the launch groups of one step; `rg` is the dominant kernel's group
+    if fused:
+        groups, names, rg = [g_fpre, g_fread, g_acc], ["precompute", "fused_readout", "accept"], 1
+    else:
+        groups, names, rg = [g_flush, g_pre, g_read, g_acc], ["flush", "precompute", "readout", "accept"], 2
     # one eager step (sets kernel attributes), then capture on a snapshot of the
     # cache that is restored afterwards so capture has no side effects
     load_inputs(dev_inp[0])
@@ -330,7 +370,7 @@ def run_gpu(args, rank, ws, local):
 
     def step_units():
         rr = scr_step[: ids.size * 32].view(torch.int32).view(ids.size, 8).cpu().numpy()
-        return rr, int(((rr[:, 5] == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
+        return rr, int((((rr[:, 5] & 1) == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
 
     for k in range(args.warmup):
         load_inputs(dev_inp[k])
@@ -360,30 +400,34 @@ def run_gpu(args, rank, ws, local):
 
     # timed pass 2: the same steps launched group by group with events between
     # the groups -> per-kernel durations for the roofline
-    read_ms, flush_ms, read_bytes, fold_bytes = [], [], 0.0, 0.0
+    grp_ms = [[] for _ in groups]
+    read_bytes, fold_bytes, fold_units = 0.0, 0.0, 0
     for k in range(args.warmup, nsteps):
         load_inputs(dev_inp[k])
         cold_l2()
-        e0 = ev()
-        e0.record(stream)
-        graphs[0].replay()
-        e_f = ev()
-        e_f.record(stream)
-        graphs[1].replay()
-        e_r0 = ev()
-        e_r0.record(stream)
-        graphs[2].replay()
-        e_r1 = ev()
-        e_r1.record(stream)
-        graphs[3].replay()
+        evs = [ev()]
+        evs[0].record(stream)
+        for g in graphs:
+            g.replay()
+            e = ev()
+            e.record(stream)
+            evs.append(e)
         torch.cuda.synchronize()
-        flush_ms.append(e0.elapsed_time(e_f))
-        read_ms.append(e_r0.elapsed_time(e_r1))
+        for j in range(len(groups)):
+            grp_ms[j].append(evs[j].elapsed_time(evs[j + 1]))
         rr, _ = step_units()
-        read_bytes += algorithmic_bytes(wl, [tuple(r[:6]) for r in rr], None, esz)
-        cnt = int(scr_flush[:4].view(torch.int32).item())
-        recs = scr_flush[256: 256 + cnt * 32].view(torch.int32).view(cnt, 8).cpu().numpy() if cnt else np.zeros((0, 8))
-        fold_bytes += flush_bytes(wl, [int(r[3]) for r in recs], esz)
+        if fused:
+            read_bytes += fused_bytes(wl, [tuple(int(v) for v in r) for r in rr], esz)
+            fold_units += int(((rr[:, 5] & 2) != 0).sum()) * wl.nheads
+        else:
+            read_bytes += algorithmic_bytes(wl, [tuple(r[:6]) for r in rr], None, esz)
+            cnt = int(scr_flush[:4].view(torch.int32).item())
+            recs = (scr_flush[256: 256 + cnt * 32].view(torch.int32).view(cnt, 8).cpu().numpy() if cnt
+                    else np.zeros((0, 8)))
+            fold_bytes += flush_bytes(wl, [int(r[3]) for r in recs], esz)
+            fold_units += cnt * wl.nheads
+    read_ms = grp_ms[rg]
+    flush_ms = grp_ms[0] if not fused else []
     torch.cuda.synchronize()
     err = int(gc.error_word.item())
     if err:
@@ -447,26 +491,31 @@ def run_gpu(args, rank, ws, local):
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (sum(read_ms) / 1e3) / 1e9
     fold_achieved = fold_bytes / (sum(flush_ms) / 1e3) / 1e9 if sum(flush_ms) > 0 else 0.0
+    flush_roofline = None
+    if not fused:
+        flush_roofline = {"bound": "hbm", "kernel": "flag_kernel+fold_kernel", "achieved": fold_achieved,
+                          "peak": peak, "unit": "GB/s", "frac": fold_achieved / peak,
+                          "avg_us": 1e3 * statistics.mean(flush_ms),
+                          "algorithmic_bytes_per_step": fold_bytes / args.steps}
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic",
         "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB written then 512 MiB read between steps (cold, clean L2)",
                        launch="one CUDA graph per step (kernels chained by programmatic dependent launch); kernel times from a second pass with one graph per launch group",
-                       force_flush=bool(args.force_flush)),
-        "roofline": {"bound": "hbm", "kernel": "readout_kernel", "achieved": achieved, "peak": peak,
-                     "unit": "GB/s", "frac": achieved / peak, "traffic": None, "peak_source": peak_kind,
-                     "avg_launch_us": 1e3 * statistics.mean(read_ms),
-                     "algorithmic_bytes_per_launch": read_bytes / args.steps},
-        "flush_roofline": {"bound": "hbm", "kernel": "flag_kernel+fold_kernel", "achieved": fold_achieved,
-                           "peak": peak, "unit": "GB/s", "frac": fold_achieved / peak,
-                           "avg_us": 1e3 * statistics.mean(flush_ms),
-                           "algorithmic_bytes_per_step": fold_bytes / args.steps},
+                       force_flush=bool(args.force_flush), path=args.path),
+        "roofline": {"bound": "hbm", "kernel": "flush_readout_kernel" if fused else "readout_kernel",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "peak_source": peak_kind, "avg_launch_us": 1e3 * statistics.mean(read_ms),
+                     "algorithmic_bytes_per_launch": read_bytes / args.steps,
+                     "folded_units_per_launch": fold_units / args.steps},
+        "flush_roofline": flush_roofline,
         "e2e": e2e,
-        "gpu_launches": 5 * args.steps,  # flag, fold, precompute, readout, accept per step
+        # per step: precompute, fused readout, accept (split: flag, fold, precompute, readout, accept)
+        "gpu_launches": (3 if fused else 5) * args.steps,
         "clocks": clk,
-        "device_time_ms": {"step": statistics.mean(step_ms), "readout": statistics.mean(read_ms),
-                           "flush": statistics.mean(flush_ms)},
+        "device_time_ms": dict({"step": statistics.mean(step_ms)},
+                               **{n: statistics.mean(v) for n, v in zip(names, grp_ms)}),
     }
     return res, wl
 

@@ -155,6 +155,32 @@ def rssm_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out,
           stream)
 
 
+def _flush_step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, force, seed,
+                stream):
+    f = getattr(_lib.load(), fn)
+    _check(fn, f(cache.struct(), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                 _ptr(slot_idx), _ptr(pnat), _ptr(cu_seqlens), slot_idx.numel(), T, force, seed, _ptr(out),
+                 _ptr(scratch), scratch.numel(), _stream(stream)))
+
+
+def rssm_flush_step(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None, force=0,
+                    seed=0, stream=None):
+    _flush_step("rssm_flush_step", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens,
+                force, seed, stream)
+
+
+def rssm_flush_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
+                               force=0, seed=0, stream=None):
+    _flush_step("rssm_flush_step_precompute", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch,
+                cu_seqlens, force, seed, stream)
+
+
+def rssm_flush_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
+                            force=0, seed=0, stream=None):
+    _flush_step("rssm_flush_step_readout", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch,
+                cu_seqlens, force, seed, stream)
+
+
 def rssm_accept(cache, slot_idx, pnat, accepted, T, cu_seqlens=None, stream=None):
     _check("rssm_accept", _lib.load().rssm_accept(cache.struct(), _ptr(slot_idx), _ptr(pnat), _ptr(accepted),
                                                   _ptr(cu_seqlens), slot_idx.numel(), T, _stream(stream)))

@@ -339,18 +339,38 @@ __device__ __forceinline__ void row_random(uint32_t (&rnd)[8], int row, int c0, 
   }
 }
 
-template <int DT>
+// Byte offset of state element (row, col) in shared memory laid out as the
+// readout's TMA boxes: 64 rows x 128 bytes per box, boxes 8 KiB apart, the
+// 16-byte chunk index within a row XOR-ed with (row & 7) (the 128-byte swizzle).
+template <int ESZ>
+__device__ __forceinline__ uint32_t swizzled_offset(int row, int col) {
+  const int byte = col * ESZ;
+  return static_cast<uint32_t>((byte >> 7) * 8192 + row * 128 + ((((byte >> 4) & 7) ^ (row & 7)) << 4) + (byte & 15));
+}
+
+// Round the lane's 4 x 8 accumulators (rows r0..r0+3, columns c0..c0+7) to
+// the state format and store them to the head's checkpoint (and the row
+// scales for 8-bit formats).  With kMirror the same bits also go to a
+// shared-memory copy of the head in the swizzled box layout (and its scales).
+template <int DT, bool kMirror = false>
 __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c0, int lane, void* head_state,
                                                float* head_scale, int rounding, uint32_t h, uint32_t s,
-                                               uint32_t epoch, uint64_t seed) {
+                                               uint32_t epoch, uint64_t seed, uint8_t* mirror = nullptr,
+                                               float* mirror_scale = nullptr) {
   const bool sr = rounding == RSSM_ROUND_STOCHASTIC;
   if constexpr (DT == RSSM_F32) {
     float* st = static_cast<float*>(head_state);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       float4* dst = reinterpret_cast<float4*>(st + (r0 + i) * 128 + c0);
-      dst[0] = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
-      dst[1] = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+      const float4 v0 = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+      const float4 v1 = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+      dst[0] = v0;
+      dst[1] = v1;
+      if constexpr (kMirror) {
+        *reinterpret_cast<float4*>(mirror + swizzled_offset<4>(r0 + i, c0)) = v0;
+        *reinterpret_cast<float4*>(mirror + swizzled_offset<4>(r0 + i, c0 + 4)) = v1;
+      }
     }
   } else if constexpr (DT == RSSM_BF16 || DT == RSSM_F16) {
     uint16_t* st = static_cast<uint16_t*>(head_state);
@@ -379,6 +399,8 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
         }
       }
       *reinterpret_cast<uint4*>(st + (r0 + i) * 128 + c0) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
+      if constexpr (kMirror)
+        *reinterpret_cast<uint4*>(mirror + swizzled_offset<2>(r0 + i, c0)) = make_uint4(wds[0], wds[1], wds[2], wds[3]);
     }
   } else {
     constexpr float qmax = (DT == RSSM_I8) ? 127.0f : 448.0f;
@@ -440,9 +462,14 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
         }
       }
       *reinterpret_cast<uint2*>(st + (r0 + i) * 128 + c0) = make_uint2(wds[0], wds[1]);
+      if constexpr (kMirror)
+        *reinterpret_cast<uint2*>(mirror + swizzled_offset<1>(r0 + i, c0)) = make_uint2(wds[0], wds[1]);
     }
-    if ((lane & 15) == 0)
+    if ((lane & 15) == 0) {
       *reinterpret_cast<float4*>(head_scale + r0) = make_float4(scale[0], scale[1], scale[2], scale[3]);
+      if constexpr (kMirror)
+        *reinterpret_cast<float4*>(mirror_scale + r0) = make_float4(scale[0], scale[1], scale[2], scale[3]);
+    }
   }
 }
 

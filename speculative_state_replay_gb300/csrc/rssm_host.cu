@@ -123,6 +123,11 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->TP = t_pad(T);
   a->KB = ring_pad(a->c.L);
   a->out = static_cast<uint16_t*>(out);
+  a->flush_mode = 0;
+  a->seed = 0;
+  a->pnat_rw = nullptr;
+  a->work = nullptr;
+  a->gdone = nullptr;
   a->rows = static_cast<RowRec*>(scratch);
   a->cf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch));
   a->rblk = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch) +
@@ -137,7 +142,7 @@ extern "C" {
 size_t rssm_scratch_bytes(const rssm_cache* cache, int32_t batch, int32_t T) {
   Cache c;
   if (check_cache(cache, &c) != RSSM_OK || batch < 0 || T < 1 || T > kMaxT) return 0;
-  const size_t f = flush_scratch_bytes(batch), s = step_scratch_bytes(batch, c.H, c.G, c.L, T);
+  const size_t f = flush_scratch_bytes(batch), s = flush_step_scratch_bytes(batch, c.H, c.G, c.L, T);
   return f > s ? f : s;
 }
 
@@ -217,6 +222,68 @@ rssm_status rssm_step(const rssm_cache* cache, const void* x, const float* dt, c
   if (st != RSSM_OK) return st;
   return rssm_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out, scratch,
                            scratch_bytes, stream);
+}
+
+namespace {
+// validation and arguments of the flush+step call (and of its two halves)
+rssm_status flush_step_args(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
+                            const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
+                            int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force,
+                            uint64_t seed, void* out, void* scratch, size_t scratch_bytes, StepArgs* a, int* sms) {
+  if (force != 0 && force != 1) return RSSM_ERR_INVALID_ARGUMENT;
+  rssm_status st = step_common(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out, scratch,
+                               scratch_bytes, a);
+  if (st != RSSM_OK || batch == 0) return st;
+  if (scratch_bytes < flush_step_scratch_bytes(batch, cache->nheads, cache->ngroups, a->c.L, T))
+    return RSSM_ERR_SCRATCH_TOO_SMALL;
+  if (static_cast<long long>(batch) * a->c.H > (1LL << 30)) return RSSM_ERR_UNSUPPORTED;
+  *sms = num_sms();
+  if (*sms <= 0) return RSSM_ERR_CUDA;
+  a->flush_mode = 1 + force;
+  a->seed = seed;
+  a->pnat_rw = pnat;
+  a->work = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(scratch) +
+                                        step_scratch_bytes(batch, cache->nheads, cache->ngroups, a->c.L, T));
+  a->gdone = a->work + 64;  // 256 bytes past the work counter
+  return RSSM_OK;
+}
+}  // namespace
+
+rssm_status rssm_flush_step_precompute(const rssm_cache* cache, const void* x, const float* dt, const float* A,
+                                       const void* B, const void* C, const float* D, const float* dt_bias,
+                                       const int32_t* slot_idx, int32_t* pnat, const int32_t* cu_seqlens,
+                                       int32_t batch, int32_t T, int32_t force, uint64_t seed, void* out,
+                                       void* scratch, size_t scratch_bytes, void* stream) {
+  StepArgs a;
+  int sms = 0;
+  rssm_status st = flush_step_args(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force,
+                                   seed, out, scratch, scratch_bytes, &a, &sms);
+  if (st != RSSM_OK || batch == 0) return st;
+  return launch_precompute(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_flush_step_readout(const rssm_cache* cache, const void* x, const float* dt, const float* A,
+                                    const void* B, const void* C, const float* D, const float* dt_bias,
+                                    const int32_t* slot_idx, int32_t* pnat, const int32_t* cu_seqlens, int32_t batch,
+                                    int32_t T, int32_t force, uint64_t seed, void* out, void* scratch,
+                                    size_t scratch_bytes, void* stream) {
+  StepArgs a;
+  int sms = 0;
+  rssm_status st = flush_step_args(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force,
+                                   seed, out, scratch, scratch_bytes, &a, &sms);
+  if (st != RSSM_OK || batch == 0) return st;
+  return launch_flush_readout(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_flush_step(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
+                            const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
+                            int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force,
+                            uint64_t seed, void* out, void* scratch, size_t scratch_bytes, void* stream) {
+  rssm_status st = rssm_flush_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T,
+                                              force, seed, out, scratch, scratch_bytes, stream);
+  if (st != RSSM_OK) return st;
+  return rssm_flush_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force, seed,
+                                 out, scratch, scratch_bytes, stream);
 }
 
 rssm_status rssm_accept(const rssm_cache* cache, const int32_t* slot_idx, int32_t* pnat, const int32_t* accepted,

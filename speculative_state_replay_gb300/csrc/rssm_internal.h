@@ -14,6 +14,7 @@ constexpr int kDstate = 128;  // state dim
 constexpr int kHeadElems = kDim * kDstate;
 constexpr int kMaxL = 32;     // ring length the kernels are built for (one lane per ring slot)
 constexpr int kMaxT = 8;      // draft tokens per step
+constexpr int kRStride = 72;  // row stride (floats) of the ring-term block R[t][64]: rows 8 banks apart
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
@@ -45,11 +46,15 @@ struct FlushRec {
   int pad[3];
 };
 
-// one row of a step (written by the precompute, read by the readout), 32 bytes
+// one row of a step (written by the precompute, read by the readout), 32 bytes.
+// r and p are the ring start and live count the step works on (after the
+// flush when the flush is part of the call).
 struct RowRec {
   int s, r, p, Tb, tok0;
-  int flags;  // 1: compute; 0: write zeros for Tb tokens
-  int pad[2];
+  int flags;           // bit 0: compute the row's outputs (else zeros for Tb tokens); bit 1: fold it first;
+                       // bit 2: the appends overlap the live prefix the fold reads (the fused readout appends)
+  int p_old;           // live count before the flush (bit 1 set)
+  unsigned epoch_new;  // epoch of the checkpoint the fold writes (bit 1 set)
 };
 
 struct FlushArgs {
@@ -80,9 +85,14 @@ struct StepArgs {
   int TP;  // T padded to 4 or 8
   int KB;  // ring rows padded to a multiple of 4
   uint16_t* out;
+  int flush_mode;            // 0: step only; 1: flush rows with p + T_b > W first; 2: flush every active row first
+  unsigned long long seed;   // stochastic-rounding key of the fold (flush_mode != 0)
+  int* pnat_rw;              // pnat, written by the fold's bookkeeping (flush_mode != 0)
+  unsigned* work;            // scratch: dynamic work counter of the fused readout (flush_mode != 0)
+  unsigned* gdone;           // scratch [batch][G]: heads of a (row, group) whose live rows have landed
   RowRec* rows;  // scratch [batch]
   uint16_t* cf;  // scratch [batch][G][8][128]: C rows in the readout's MMA operand type
-  float* rblk;   // scratch [batch][H][TP*64 + TP]: ring term R[t][d], then decay[t]
+  float* rblk;   // scratch [batch][H][TP*kRStride + TP]: ring term R[t][d] (rows padded), then decay[t]
 };
 
 struct InitArgs {
@@ -104,17 +114,23 @@ inline size_t step_cf_bytes(int batch, int G, int T) {
   (void)T;
   return align_up((size_t)batch * G * 8 * 128 * 2, 256);
 }
-inline size_t step_rblk_floats(int T) { return (size_t)t_pad(T) * 64 + t_pad(T); }
+inline size_t step_rblk_floats(int T) { return (size_t)t_pad(T) * kRStride + t_pad(T); }
 inline size_t step_scratch_bytes(int batch, int H, int G, int L, int T) {
   (void)L;
   const size_t blk = step_rblk_floats(T) * sizeof(float);
   return step_rows_bytes(batch) + step_cf_bytes(batch, G, T) + align_up(blk * (size_t)batch * H, 256);
+}
+// the flush+step call: the step's scratch, then the work counter, then the
+// per-(row, group) landed-head counters
+inline size_t flush_step_scratch_bytes(int batch, int H, int G, int L, int T) {
+  return step_scratch_bytes(batch, H, G, L, T) + 256 + align_up((size_t)batch * G * 4, 256);
 }
 
 // launchers (defined in the .cu files); return a cudaError_t as int
 int launch_flush(const FlushArgs& a, int num_sms, void* stream);
 int launch_precompute(const StepArgs& a, void* stream);
 int launch_readout(const StepArgs& a, int num_sms, void* stream);
+int launch_flush_readout(const StepArgs& a, int num_sms, void* stream);
 int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* accepted, const int* cu, int batch,
                   int T, void* stream);
 int launch_init(const InitArgs& a, void* stream);

@@ -17,13 +17,7 @@
 //       TMA (swizzled tensor boxes for S0, 1-D bulk copies for the rest) from
 //       a producer warp with mbarriers; 8 consumer warps contract on the
 //       tensor cores (mma.sync m16n8k16, f32 accumulation).
-#include <cuda.h>
-#include <cudaTypedefs.h>
-#include <cuda_runtime.h>
-
-#include <mutex>
-
-#include "rssm_device.cuh"
+#include "rssm_readout.cuh"
 
 namespace rssm {
 
@@ -53,7 +47,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   __shared__ float dts[kHeadChunk][kMaxL];  // dt' of the live tokens; dt of the new ones (before bias, softplus)
   __shared__ float hp[3][kHeadChunk];       // A, D, dt_bias of the chunk's heads
   __shared__ __align__(16) float cfs[8][kMaxL][TP];  // per warp: coef[k][t] of its current head
-  __shared__ int meta[6];
+  __shared__ int meta[7];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -74,26 +68,49 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
     const int tok0 = __shfl_sync(0xffffffffu, v, 2), tok1 = __shfl_sync(0xffffffffu, v, 3);
     if (lane == 0) {
       int Tb = tok1 - tok0, flags = 0, p = 0, r = 0;
+      unsigned ep = 0u;
       const bool tb_ok = Tb >= 0 && Tb <= a.T;
       if (s >= 1 && s < c.S) {
         if (!tb_ok) {
           if (g == 0) set_error(c.err, RSSM_ERRBIT_SEQLEN);
-        } else if (pn < 0 || pn + Tb > L) {
-          if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);
+        } else if (a.flush_mode && (pn < 0 || pn > L)) {
+          if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);  // the flush's own check
         } else {
-          p = pn;
-          r = c.ring_start[s];
-          flags = 1;
+          // with the flush in the same call: decide it here (the flush rule),
+          // then work on the ring as the flush leaves it
+          const int r0 = c.ring_start[s];
+          const bool fl = a.flush_mode == 2 || (a.flush_mode == 1 && pn + Tb > c.W);
+          p = fl ? 0 : pn;
+          r = fl ? (r0 + pn >= L ? r0 + pn - L : r0 + pn) : r0;
+          if (fl) {
+            ep = c.epoch[s] + 1u;
+            flags = 2;
+          }
+          // the step's check; with the flush in the call, new tokens that would
+          // land on live slots the fold still has to read are appended by
+          // the fused readout after the fold has its copy (bit 2)
+          if (p < 0 || p + Tb > L) {
+            if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);
+          } else {
+            flags |= 1;
+            if (fl && pn + Tb > L) flags |= 4;
+          }
         }
       }
       if (!tb_ok) Tb = 0;
-      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags;
-      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, {0, 0}};
+      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags & 1;
+      meta[6] = (flags >> 2) & 1;
+      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, pn, ep};
+    }
+    if (a.work && lane == 0) {  // the fused readout's counters
+      if (blockIdx.x == 0) *a.work = 0u;
+      a.gdone[blockIdx.x] = 0u;
     }
   }
   __syncthreads();
   const int s = meta[0], r = meta[1], p = meta[2], Tb = meta[3], tok0 = meta[4];
   if (!meta[5] || Tb == 0) return;
+  const bool app = !meta[6];  // appends here (else by the fused readout, after its fold)
   const int K = p + Tb;  // logical tokens: p live ring rows, then the Tb new ones
   auto ring = [&](int k) {  // ring slot of logical token k < L
     const int q = r + k;
@@ -117,13 +134,13 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   for (int h0 = 0; h0 < hpg; h0 += kHeadChunk) {
     const int hc = hpg - h0 < kHeadChunk ? hpg - h0 : kHeadChunk, hb = g * hpg + h0;
     if (h0) __syncthreads();  // every warp is done with the previous chunk's rows
-    // x rows of the chunk's heads: one 16-byte piece per thread and head (K * 8 <= 256)
-    if (tid < K * 8) {
-      const int k = tid >> 3, q = tid & 7;
-      for (int hh = 0; hh < hc; ++hh) {
+    // x rows: warp w brings the rows of the heads it works on (w, w + 8), 16 bytes a lane
+    for (int hh = warp; hh < hc; hh += 8) {
+      for (int q = lane; q < K * 8; q += 32) {
+        const int k = q >> 3, part = q & 7;
         const uint16_t* src = k < p ? xslot + (static_cast<long long>(hb + hh) * L + ring(k)) * kDim
                                     : a.x + (static_cast<long long>(tok0 + k - p) * H + hb + hh) * kDim;
-        cp_async16(xs + (hh * L + k) * kDim + q * 8, src + q * 8);
+        cp_async16(xs + (hh * L + k) * kDim + part * 8, src + part * 8);
       }
     }
     for (int idx = tid; idx < hc * 32; idx += 256) {
@@ -141,28 +158,42 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
     }
     cp_async_wait_all();
     __syncthreads();
+    // dt' = softplus(dt + dt_bias) of every (head, new token) of the chunk at
+    // once (the exact sequence: these values go into the ring), in place
+    if (tid < hc * 8) {
+      const int hh = tid >> 3, t = tid & 7;
+      if (t < Tb) {
+        const float v = spec_softplus(__fadd_rn(dts[hh][p + t], hp[2][hh]));
+        dts[hh][p + t] = v;
+        if (app) dslot[static_cast<long long>(hb + hh) * L + ring(p + t)] = v;
+      }
+    }
     if (h0 == 0) {
       // ring append of the new B rows
-      if (tid < Tb * 16) {
+      if (app && tid < Tb * 16) {
         const int t = tid >> 4, q = tid & 15;
         reinterpret_cast<uint4*>(bring + ring(p + t) * kDstate)[q] =
             reinterpret_cast<const uint4*>(bs + (p + t) * kDstate)[q];
       }
-      // C.B contraction, one warp per (t, k) pair with k <= p + t, 4 dstate entries a lane
-      for (int pr = warp; pr < Tb * K; pr += 8) {
-        const int t = pr / K, k = pr % K;
-        float v = 0.0f;
-        if (k <= p + t) {
-          const uint2 cw = reinterpret_cast<const uint2*>(cs + t * kDstate)[lane];
-          const uint2 bw = reinterpret_cast<const uint2*>(bs + k * kDstate)[lane];
-          v = fmaf(bf16lo(cw.x), bf16lo(bw.x), v);
-          v = fmaf(bf16hi(cw.x), bf16hi(bw.x), v);
-          v = fmaf(bf16lo(cw.y), bf16lo(bw.y), v);
-          v = fmaf(bf16hi(cw.y), bf16hi(bw.y), v);
+      // C.B contraction on the tensor cores: CB[t][k] = sum_n C[t][n] B[k][n]
+      // as mma.sync m16n8k16 (M = t, rows >= T_b zero; N = k, one 8-token
+      // tile per warp; K = dstate in 8 steps), f32 accumulation of exact bf16
+      // products.  Entries with k > p + t are never used.
+      if (warp * 8 < K) {
+        const int g8 = lane >> 2, c4 = lane & 3;
+        const int kr = warp * 8 + g8 < K ? warp * 8 + g8 : K - 1;  // B row (token) of this lane
+        const uint32_t* crow = reinterpret_cast<const uint32_t*>(cs + g8 * kDstate);
+        const uint32_t* brow = reinterpret_cast<const uint32_t*>(bs + kr * kDstate);
+        float d4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-          for (int off = 16; off; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t a0 = g8 < Tb ? crow[8 * ks + c4] : 0u, a2 = g8 < Tb ? crow[8 * ks + 4 + c4] : 0u;
+          mma_bf16(d4, a0, a2, brow[8 * ks + c4], brow[8 * ks + 4 + c4]);
         }
-        if (lane == 0) CB[t][k] = v;
+        if (g8 < TP) {
+          CB[g8][warp * 8 + 2 * c4] = d4[0];
+          CB[g8][warp * 8 + 2 * c4 + 1] = d4[1];
+        }
       }
       // the C block for the readout's tensor-core contraction: [8][128] in the
       // MMA operand type (bf16 for f32/bf16 checkpoints, fp16 otherwise), rows
@@ -181,22 +212,17 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       __syncthreads();
     }
     // ring appends of the chunk's new x rows
-    for (int idx = tid; idx < hc * 64; idx += 256) {
+    for (int idx = tid; app && idx < hc * 64; idx += 256) {
       const int hh = idx >> 6, t = (idx >> 3) & 7, q = idx & 7;
       if (t < Tb)
         reinterpret_cast<uint4*>(xslot + (static_cast<long long>(hb + hh) * L + ring(p + t)) * kDim)[q] =
             reinterpret_cast<const uint4*>(xs + (hh * L + p + t) * kDim)[q];
     }
+    if (h0) __syncthreads();  // the chunk's dt' (the first chunk synchronised above)
     for (int hh = warp; hh < hc; hh += 8) {
       const int h = hb + hh;
       const float Ah = hp[0][hh], Dh = hp[1][hh];
-      float dtp = 0.0f;
-      if (lane < p) {
-        dtp = dts[hh][lane];
-      } else if (lane < K) {
-        dtp = spec_softplus(__fadd_rn(dts[hh][lane], hp[2][hh]));  // the value stored in the ring
-        dslot[static_cast<long long>(h) * L + ring(lane)] = dtp;
-      }
+      const float dtp = lane < K ? dts[hh][lane] : 0.0f;
       // inclusive prefix sum of A dt' over the lanes (these sums only feed the
       // outputs, so any summation order is fine here)
       float cum = lane < K ? Ah * dtp : 0.0f;
@@ -213,11 +239,11 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
         const float cpt = __shfl_sync(0xffffffffu, cum, kt);
         float v = 0.0f;
         if (t < Tb && lane <= p + t) {
-          v = expf(cpt - cum) * dtp * CB[t][lane];
+          v = __expf(cpt - cum) * dtp * CB[t][lane];
           if (lane == p + t) v += Dh;
         }
         cf[t] = v;
-        dec[t] = t < Tb ? expf(cpt) : 0.0f;
+        dec[t] = t < Tb ? __expf(cpt) : 0.0f;
       }
       // ring term of this head: R[t][d] = sum_k coef[k][t] x_k[d]; lane k
       // holds coef[k][.], shared through cfs; lane l accumulates d = 2l, 2l + 1
@@ -232,28 +258,24 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 #pragma unroll 4
       for (int k = 0; k < K; ++k) {
         const uint32_t w = xr[k * (kDim / 2)];
-        const float x0 = bf16lo(w), x1 = bf16hi(w);
+        const float2 xv = make_float2(bf16lo(w), bf16hi(w));
 #pragma unroll
         for (int t4 = 0; t4 < TP; t4 += 4) {
           const float4 cv = *reinterpret_cast<const float4*>(&cfs[warp][k][t4]);
-          R[t4 + 0].x = fmaf(cv.x, x0, R[t4 + 0].x);
-          R[t4 + 0].y = fmaf(cv.x, x1, R[t4 + 0].y);
-          R[t4 + 1].x = fmaf(cv.y, x0, R[t4 + 1].x);
-          R[t4 + 1].y = fmaf(cv.y, x1, R[t4 + 1].y);
-          R[t4 + 2].x = fmaf(cv.z, x0, R[t4 + 2].x);
-          R[t4 + 2].y = fmaf(cv.z, x1, R[t4 + 2].y);
-          R[t4 + 3].x = fmaf(cv.w, x0, R[t4 + 3].x);
-          R[t4 + 3].y = fmaf(cv.w, x1, R[t4 + 3].y);
+          R[t4 + 0] = __ffma2_rn(make_float2(cv.x, cv.x), xv, R[t4 + 0]);
+          R[t4 + 1] = __ffma2_rn(make_float2(cv.y, cv.y), xv, R[t4 + 1]);
+          R[t4 + 2] = __ffma2_rn(make_float2(cv.z, cv.z), xv, R[t4 + 2]);
+          R[t4 + 3] = __ffma2_rn(make_float2(cv.w, cv.w), xv, R[t4 + 3]);
         }
       }
       __syncwarp();  // cfs is rewritten for the warp's next head
-      float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP);
+      float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (TP * kRStride + TP);
 #pragma unroll
-      for (int t = 0; t < TP; ++t) reinterpret_cast<float2*>(blk + t * kDim)[lane] = R[t];
+      for (int t = 0; t < TP; ++t) reinterpret_cast<float2*>(blk + t * kRStride)[lane] = R[t];
       if (lane == 0) {
 #pragma unroll
         for (int t4 = 0; t4 < TP; t4 += 4)
-          *reinterpret_cast<float4*>(blk + TP * kDim + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
+          *reinterpret_cast<float4*>(blk + TP * kRStride + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
       }
     }
   }
@@ -262,137 +284,6 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 // ---------------------------------------------------------------------------
 // readout
 // ---------------------------------------------------------------------------
-// Per (row, head) unit the readout is one small dense contraction on the
-// tensor cores, mma.sync m16n8k16 with f32 accumulation:
-//     Y^T[t][d] = sum_n Cblk[t][n] S0[d][n]        (M = t, N = d, K = dstate)
-//     y_t[d]    = decay_t scale_d Y^T[t][d] + R[t][d]
-// where the ring term R (live ring + new tokens) and decay_t come from the
-// precompute.  Warp w owns the 8 state rows d = 8w..8w+7 (one n8 tile).  K is
-// taken in a permuted order inside each 16-wide step (physical 4c..4c+3 <->
-// logical 2c, 2c+1, 2c+8, 2c+9 for lane group c), so every operand fragment is
-// one 64-bit shared load; the sum over k is unchanged.  S0 arrives by TMA
-// tensor copies with the 128-byte swizzle, which keeps those loads
-// conflict-free.
-struct ReadMeta {
-  int b, h, s, r, p, Tb, tok0, flags;
-};
-
-struct ReadLayout {
-  int ns;
-  uint32_t s0_bytes, scale_off, c_off, r_off, r_bytes, stage_bytes;
-  uint32_t stages_off, total;
-};
-
-__host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns) {
-  ReadLayout f;
-  f.ns = ns;
-  const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
-  f.s0_bytes = kHeadElems * esz;  // esz boxes of 64 rows x 128 bytes
-  uint32_t o = f.s0_bytes;
-  f.scale_off = o;
-  if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
-  f.c_off = o;
-  o += 8 * kDstate * 2;
-  f.r_off = o;
-  f.r_bytes = (TP * kDim + TP) * 4;
-  o += f.r_bytes;
-  f.stage_bytes = (o + 1023) & ~1023u;  // the swizzled boxes need 1024-byte alignment
-  f.stages_off = 1024;                  // barriers and per-stage metadata
-  f.total = f.stages_off + ns * f.stage_bytes + 1024;  // + slack to align the base
-  return f;
-}
-
-__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(smem_addr(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
-      : "memory");
-}
-
-__device__ __forceinline__ void mma_bf16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-  asm(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-      "{%0,%1,%2,%3};"
-      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-      : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
-  return *reinterpret_cast<const uint32_t*>(&h);
-}
-__device__ __forceinline__ float bf16_lo_f(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi_f(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
-
-// byte offset of (row d, byte k) inside one 64-row x 128-byte swizzled box
-__device__ __forceinline__ uint32_t swz(int d, int kbyte) {
-  return static_cast<uint32_t>(d * 128 + ((((kbyte >> 4) ^ d) & 7) << 4) + (kbyte & 15));
-}
-
-// A fragments of the C block for lane (g, c): row t = g, logical k = 16 ks +
-// {2c, 2c+1, 2c+8, 2c+9} (physical 16 ks + 4c .. 4c+3), one 64-bit load per k step
-__device__ __forceinline__ void load_c_frags(const uint16_t* cblk, int g, int c, uint2 (&af)[8]) {
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) af[ks] = *reinterpret_cast<const uint2*>(cblk + g * kDstate + 16 * ((ks ^ g) & 7) + 4 * c);
-}
-
-// S0 . C over dstate for state rows d (lane's B column) of this warp; even and
-// odd k steps accumulate in separate chains, added at the end
-template <int DT>
-__device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8], int d, int c, float (&acc)[4]) {
-  float a2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const uint2 av = af[ks];
-    float(&ac)[4] = a2[ks & 1];
-    if constexpr (DT == RSSM_BF16 || DT == RSSM_F16) {
-      const int kb = (ks * 16 + 4 * c) * 2;  // byte within the 256-byte row
-      const uint2 bv = *reinterpret_cast<const uint2*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
-      if constexpr (DT == RSSM_BF16)
-        mma_bf16(ac, av.x, av.y, bv.x, bv.y);
-      else
-        mma_f16(ac, av.x, av.y, bv.x, bv.y);
-    } else if constexpr (DT == RSSM_F32) {
-      const int kb = (ks * 16 + 4 * c) * 4;
-      const float4 f = *reinterpret_cast<const float4*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
-      const uint32_t h01 = pack_bf16(f.x, f.y), h23 = pack_bf16(f.z, f.w);
-      const uint32_t l01 = pack_bf16(f.x - bf16_lo_f(h01), f.y - bf16_hi_f(h01));
-      const uint32_t l23 = pack_bf16(f.z - bf16_lo_f(h23), f.w - bf16_hi_f(h23));
-      mma_bf16(a2[0], av.x, av.y, h01, h23);
-      mma_bf16(a2[1], av.x, av.y, l01, l23);
-    } else {
-      const uint32_t w = *reinterpret_cast<const uint32_t*>(s0 + swz(d, ks * 16 + 4 * c));
-      uint32_t b0, b1;
-      if constexpr (DT == RSSM_I8) {
-        // int8 code q as fp16: (1024 + (q + 128)) - 1152, exact
-        const uint32_t u = w ^ 0x80808080u;
-        const uint32_t p01 = __byte_perm(u, 0x64646464u, 0x4140), p23 = __byte_perm(u, 0x64646464u, 0x4342);
-        const __half2 off = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));
-        const __half2 h01 = __hsub2(*reinterpret_cast<const __half2*>(&p01), off);
-        const __half2 h23 = __hsub2(*reinterpret_cast<const __half2*>(&p23), off);
-        b0 = *reinterpret_cast<const uint32_t*>(&h01);
-        b1 = *reinterpret_cast<const uint32_t*>(&h23);
-      } else {
-        const __half2_raw r01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w & 0xffffu), __NV_E4M3);
-        const __half2_raw r23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(w >> 16), __NV_E4M3);
-        b0 = static_cast<uint32_t>(r01.x) | (static_cast<uint32_t>(r01.y) << 16);
-        b1 = static_cast<uint32_t>(r23.x) | (static_cast<uint32_t>(r23.y) << 16);
-      }
-      mma_f16(ac, av.x, av.y, b0, b1);
-    }
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) acc[j] = a2[0][j] + a2[1][j];
-}
-
 template <int DT, int TP>
 __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -462,7 +353,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         rr = a.rows[b];
         cur_b = b;
       }
-      const bool active = rr.flags && rr.Tb > 0;
+      const bool active = (rr.flags & 1) && rr.Tb > 0;
       const int g = h / c.hpg, bg = b * c.G + g;
       // the C block is copied only when the (row, group) changes: consumers
       // keep its fragments in registers (flags bit 1 tells them to reload)
@@ -485,7 +376,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         if (newc)
           bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
                    &full[st]);
-        bulk_g2s(sb + lay.r_off, a.rblk + (static_cast<long long>(b) * H + h) * (TP * kDim + TP), lay.r_bytes,
+        bulk_g2s(sb + lay.r_off, a.rblk + (static_cast<long long>(b) * H + h) * (TP * kRStride + TP), lay.r_bytes,
                  &full[st]);
       }
       mbar_arrive(&full[st]);
@@ -527,8 +418,8 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     float acc[4];
     s0_dot_c<DT>(sb, af, d, cq, acc);
     const float* rb = reinterpret_cast<const float*>(sb + lay.r_off);
-    const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kDim + dout) : make_float2(0.0f, 0.0f);
-    const float dec = g < TP ? rb[TP * kDim + g] : 0.0f;
+    const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kRStride + dout) : make_float2(0.0f, 0.0f);
+    const float dec = g < TP ? rb[TP * kRStride + g] : 0.0f;
     float sc0 = 1.0f, sc1 = 1.0f;
     if constexpr (k8bit) {
       const float2 scv = *reinterpret_cast<const float2*>(sb + lay.scale_off + dout * 4);
@@ -561,36 +452,6 @@ int launch_precompute(const StepArgs& a, void* stream) {
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(precompute_smem(kHeadChunk, kMaxL)));
   if (e == cudaSuccess) e = launch_pdl(kern, dim3(grid), dim3(256), smem, st, a);
   return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link)
-static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    cudaDriverEntryPointQueryResult q;
-    void* p = nullptr;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// S0 of all slots as a 3-D tensor [slot][H*64 rows][128], boxes of 64 rows x 128 bytes, 128-byte swizzle
-static bool encode_state_map(const Cache& c, CUtensorMap* map) {
-  auto enc = tensor_map_encoder();
-  if (!enc) return false;
-  const int esz = c.dtype == RSSM_F32 ? 4 : (c.dtype == RSSM_BF16 || c.dtype == RSSM_F16) ? 2 : 1;
-  const CUtensorMapDataType dt = esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                          : (esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8);
-  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDstate), static_cast<cuuint64_t>(c.H) * kDim,
-                              static_cast<cuuint64_t>(c.S)};
-  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDstate) * esz, static_cast<cuuint64_t>(c.state_stride) * esz};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kDim), 1};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  return enc(map, dt, 3, c.state, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int DT, int TP>

@@ -66,7 +66,8 @@ def state_close(dtype, g, o):
 class Pair:
     """Oracle + GPU replicas of one workload."""
 
-    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None):
+    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False):
+        self.fused = fused  # GPU side through rssm_flush_step instead of rssm_flush + rssm_step
         self.orc, self.wl, self.oc = orc, wl, oc
         self.ids, self.pnat = ids, pnat.copy()
         self.device = device
@@ -92,10 +93,14 @@ class Pair:
         oc.accept(self.ids, self.pnat, inp.accepted, wl.T, cu_seqlens=inp.cu_seqlens)
         # gpu
         out = torch.full((max(inp.ntok, 1), wl.nheads, 64), 0x7FC0, dtype=torch.int16, device=self.device)
-        api.rssm_flush(gc, self.gA, self.gids, self.gpnat, wl.T, self.scratch, cu_seqlens=cu, force=force,
-                       seed=self.seed)
-        api.rssm_step(gc, d(inp.x), d(inp.dt), self.gA, d(inp.B), d(inp.C), self.gD, self.gb, self.gids,
-                      self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu)
+        if self.fused:
+            api.rssm_flush_step(gc, d(inp.x), d(inp.dt), self.gA, d(inp.B), d(inp.C), self.gD, self.gb, self.gids,
+                                self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu, force=force, seed=self.seed)
+        else:
+            api.rssm_flush(gc, self.gA, self.gids, self.gpnat, wl.T, self.scratch, cu_seqlens=cu, force=force,
+                           seed=self.seed)
+            api.rssm_step(gc, d(inp.x), d(inp.dt), self.gA, d(inp.B), d(inp.C), self.gD, self.gb, self.gids,
+                          self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu)
         api.rssm_accept(gc, self.gids, self.gpnat, d(inp.accepted), wl.T, cu_seqlens=cu)
         torch.cuda.synchronize()
         y_g = out[: inp.ntok].cpu().numpy().view(np.uint16)
