@@ -196,12 +196,14 @@ def algorithmic_bytes(wl, rows_rec, ntok_b, esz):
 
 
 def fused_bytes(wl, rows_rec, esz):
-    """Algorithmic HBM bytes of one fused fold + readout launch from its
-    per-row records (s, r, p, Tb, tok0, flags, p_old, epoch): S0 (+ scales)
-    read once per (row, head) that is read out or folded; for rows read out the
-    group's C rows shared by its heads and y; for folded rows the new S0 (+
-    scales) written and the live x rows, dt' and the group's live B rows; rows
-    without outputs write zeros."""
+    """Algorithmic HBM bytes of one step-kernel launch (rssm_flush_step) from its
+    per-row records (s, r, p, Tb, tok0, flags, p_old, epoch), per (row, head):
+    S0 (+ scales) read once if the row is read out or folded; for a folded row
+    the new S0 (+ scales) written and its pre-flush live x rows, dt' and (the
+    group's share of) B rows read; for a row read out its live and new x rows
+    and dt, the group's share of its live and new B rows and of its C rows, y
+    written, and the appended x rows, dt' and B rows written; rows without
+    outputs write zero y."""
     total = 0
     hpg = wl.hpg
     s0 = 64 * 128 * esz + (256 if esz == 1 else 0)
@@ -210,9 +212,14 @@ def fused_bytes(wl, rows_rec, esz):
         per_head = 0
         if out_ok or fo:
             per_head += s0
-        per_head += (Tb * 256 / hpg + Tb * 128) if out_ok else Tb * 128
         if fo:
             per_head += s0 + p_old * (128 + 4) + p_old * 256 / hpg
+        if out_ok:
+            k = p + Tb
+            per_head += k * (128 + 4) + k * 256 / hpg + Tb * 256 / hpg  # x, dt, B, C read
+            per_head += Tb * 128 + Tb * (128 + 4) + Tb * 256 / hpg      # y, appends written
+        elif Tb > 0:
+            per_head += Tb * 128
         total += per_head * wl.nheads
     return total
 
@@ -318,17 +325,17 @@ def run_gpu(args, rank, ws, local):
         api.rssm_accept(gc, gids, pnat, buf["acc"], wl.T, cu_seqlens=cu)
 
     def g_fpre():
-        api.rssm_flush_step_precompute(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
+        api.rssm_flush_step_classify(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
                                        scr_step, cu_seqlens=cu, force=force, seed=wl.sr_seed)
 
     def g_fread():
-        api.rssm_flush_step_readout(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
+        api.rssm_flush_step_main(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
                                     scr_step, cu_seqlens=cu, force=force, seed=wl.sr_seed)
 
     fused = args.path == "fused"
     # the launch groups of one step; `rg` is the dominant kernel's group
     if fused:
-        groups, names, rg = [g_fpre, g_fread, g_acc], ["precompute", "fused_readout", "accept"], 1
+        groups, names, rg = [g_fpre, g_fread, g_acc], ["classify", "step_main", "accept"], 1
     else:
         groups, names, rg = [g_flush, g_pre, g_read, g_acc], ["flush", "precompute", "readout", "accept"], 2
     # one eager step (sets kernel attributes), then capture on a snapshot of the
@@ -504,14 +511,14 @@ def run_gpu(args, rank, ws, local):
         "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB written then 512 MiB read between steps (cold, clean L2)",
                        launch="one CUDA graph per step (kernels chained by programmatic dependent launch); kernel times from a second pass with one graph per launch group",
                        force_flush=bool(args.force_flush), path=args.path),
-        "roofline": {"bound": "hbm", "kernel": "flush_readout_kernel" if fused else "readout_kernel",
+        "roofline": {"bound": "hbm", "kernel": "step_kernel" if fused else "readout_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
                      "peak_source": peak_kind, "avg_launch_us": 1e3 * statistics.mean(read_ms),
                      "algorithmic_bytes_per_launch": read_bytes / args.steps,
                      "folded_units_per_launch": fold_units / args.steps},
         "flush_roofline": flush_roofline,
         "e2e": e2e,
-        # per step: precompute, fused readout, accept (split: flag, fold, precompute, readout, accept)
+        # per step: classify, step kernel, accept (split: flag, fold, precompute, readout, accept)
         "gpu_launches": (3 if fused else 5) * args.steps,
         "clocks": clk,
         "device_time_ms": dict({"step": statistics.mean(step_ms)},

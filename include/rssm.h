@@ -187,15 +187,15 @@ rssm_status rssm_step(const rssm_cache *cache, const void *x, const float *dt, c
  * (bit for bit: the fold's arithmetic and quantiser are the flush's), rings,
  * ring_start, pnat, flush_epoch and error bits.  The pages keep the flush and
  * the step as separate kernels ([FI] Description items 1-2: precompute +
- * persistent main); here the flush decision is taken in the step's
- * precompute and each flagged head is folded in the same shared-memory stage
- * its readout contracts, so its checkpoint is read from HBM once.
+ * persistent main; the flush in its own kernels); here one persistent kernel
+ * takes each (row, head) once: it folds a flushed head in the shared-memory
+ * stage its checkpoint arrived in, forms the step's replay terms for it and
+ * reads the outputs out of the same stage, so each checkpoint is read from
+ * HBM once per decode iteration.
  *   pnat     [batch] i32 (device, in/out): set to 0 for flushed rows
  *   force, seed as in rssm_flush; scratch of at least rssm_scratch_bytes().
- * Where a flushed row's new tokens land on ring slots of the live prefix
- * the fold reads (pnat + T_b > L, which happens whenever max_window < T),
- * those appends are made after the fold has read the prefix; the result is
- * the same.
+ * Ring appends are made after the live prefix they may land on has been read,
+ * so rows with pnat + T_b > L (whenever max_window < T) give the same result.
  */
 rssm_status rssm_flush_step(const rssm_cache *cache, const void *x, const float *dt, const float *A, const void *B,
                             const void *C, const float *D, const float *dt_bias, const int32_t *slot_idx,
@@ -204,23 +204,23 @@ rssm_status rssm_flush_step(const rssm_cache *cache, const void *x, const float 
 
 /*
  * The two halves of rssm_flush_step, exposed for profiling: rssm_flush_step
- * == rssm_flush_step_precompute followed by rssm_flush_step_readout with the
- * same arguments and scratch.
- *   precompute: per (row, group): the flush decision, then as
- *               rssm_step_precompute on the ring the flush leaves.
- *   readout:    per (row, head): folds flushed heads, the flush's
- *               bookkeeping, streams S0 once, forms y.
+ * == rssm_flush_step_classify followed by rssm_flush_step_main with the same
+ * arguments and scratch.
+ *   classify: per row: the flush decision and the ring the step works on.
+ *   main:     per (row, head): folds flushed heads, the flush's bookkeeping,
+ *             the step's replay terms and ring appends, streams S0 once,
+ *             forms y.
  */
-rssm_status rssm_flush_step_precompute(const rssm_cache *cache, const void *x, const float *dt, const float *A,
-                                       const void *B, const void *C, const float *D, const float *dt_bias,
-                                       const int32_t *slot_idx, int32_t *pnat, const int32_t *cu_seqlens,
-                                       int32_t batch, int32_t T, int32_t force, uint64_t seed, void *out,
-                                       void *scratch, size_t scratch_bytes, void *stream);
-rssm_status rssm_flush_step_readout(const rssm_cache *cache, const void *x, const float *dt, const float *A,
-                                    const void *B, const void *C, const float *D, const float *dt_bias,
-                                    const int32_t *slot_idx, int32_t *pnat, const int32_t *cu_seqlens, int32_t batch,
-                                    int32_t T, int32_t force, uint64_t seed, void *out, void *scratch,
-                                    size_t scratch_bytes, void *stream);
+rssm_status rssm_flush_step_classify(const rssm_cache *cache, const void *x, const float *dt, const float *A,
+                                     const void *B, const void *C, const float *D, const float *dt_bias,
+                                     const int32_t *slot_idx, int32_t *pnat, const int32_t *cu_seqlens, int32_t batch,
+                                     int32_t T, int32_t force, uint64_t seed, void *out, void *scratch,
+                                     size_t scratch_bytes, void *stream);
+rssm_status rssm_flush_step_main(const rssm_cache *cache, const void *x, const float *dt, const float *A,
+                                 const void *B, const void *C, const float *D, const float *dt_bias,
+                                 const int32_t *slot_idx, int32_t *pnat, const int32_t *cu_seqlens, int32_t batch,
+                                 int32_t T, int32_t force, uint64_t seed, void *out, void *scratch,
+                                 size_t scratch_bytes, void *stream);
 
 /*
  * The two halves of rssm_step, exposed for profiling and for callers that

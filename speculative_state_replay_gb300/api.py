@@ -169,15 +169,15 @@ def rssm_flush_step(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, s
                 force, seed, stream)
 
 
-def rssm_flush_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
+def rssm_flush_step_classify(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
                                force=0, seed=0, stream=None):
-    _flush_step("rssm_flush_step_precompute", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch,
+    _flush_step("rssm_flush_step_classify", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch,
                 cu_seqlens, force, seed, stream)
 
 
-def rssm_flush_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
+def rssm_flush_step_main(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
                             force=0, seed=0, stream=None):
-    _flush_step("rssm_flush_step_readout", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch,
+    _flush_step("rssm_flush_step_main", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch,
                 cu_seqlens, force, seed, stream)
 
 

@@ -104,6 +104,12 @@ __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) 
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_addr(smem_dst)), "l"(gmem_src) : "memory");
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Arrive on `bar` once every cp.async this thread has issued so far has
+// landed, without adding to the barrier's expected count (the barrier is
+// initialised to expect this arrival).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
 // Programmatic dependent launch.  pdl_wait() returns once the preceding kernel
 // in the stream has completed and its writes are visible (immediately when the
 // kernel was launched without the attribute); every chain kernel calls it

@@ -249,41 +249,41 @@ rssm_status flush_step_args(const rssm_cache* cache, const void* x, const float*
 }
 }  // namespace
 
-rssm_status rssm_flush_step_precompute(const rssm_cache* cache, const void* x, const float* dt, const float* A,
-                                       const void* B, const void* C, const float* D, const float* dt_bias,
-                                       const int32_t* slot_idx, int32_t* pnat, const int32_t* cu_seqlens,
-                                       int32_t batch, int32_t T, int32_t force, uint64_t seed, void* out,
-                                       void* scratch, size_t scratch_bytes, void* stream) {
+rssm_status rssm_flush_step_classify(const rssm_cache* cache, const void* x, const float* dt, const float* A,
+                                     const void* B, const void* C, const float* D, const float* dt_bias,
+                                     const int32_t* slot_idx, int32_t* pnat, const int32_t* cu_seqlens, int32_t batch,
+                                     int32_t T, int32_t force, uint64_t seed, void* out, void* scratch,
+                                     size_t scratch_bytes, void* stream) {
   StepArgs a;
   int sms = 0;
   rssm_status st = flush_step_args(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force,
                                    seed, out, scratch, scratch_bytes, &a, &sms);
   if (st != RSSM_OK || batch == 0) return st;
-  return launch_precompute(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+  return launch_classify(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
-rssm_status rssm_flush_step_readout(const rssm_cache* cache, const void* x, const float* dt, const float* A,
-                                    const void* B, const void* C, const float* D, const float* dt_bias,
-                                    const int32_t* slot_idx, int32_t* pnat, const int32_t* cu_seqlens, int32_t batch,
-                                    int32_t T, int32_t force, uint64_t seed, void* out, void* scratch,
-                                    size_t scratch_bytes, void* stream) {
+rssm_status rssm_flush_step_main(const rssm_cache* cache, const void* x, const float* dt, const float* A,
+                                 const void* B, const void* C, const float* D, const float* dt_bias,
+                                 const int32_t* slot_idx, int32_t* pnat, const int32_t* cu_seqlens, int32_t batch,
+                                 int32_t T, int32_t force, uint64_t seed, void* out, void* scratch,
+                                 size_t scratch_bytes, void* stream) {
   StepArgs a;
   int sms = 0;
   rssm_status st = flush_step_args(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force,
                                    seed, out, scratch, scratch_bytes, &a, &sms);
   if (st != RSSM_OK || batch == 0) return st;
-  return launch_flush_readout(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+  return launch_flush_step(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
 rssm_status rssm_flush_step(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
                             const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
                             int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force,
                             uint64_t seed, void* out, void* scratch, size_t scratch_bytes, void* stream) {
-  rssm_status st = rssm_flush_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T,
-                                              force, seed, out, scratch, scratch_bytes, stream);
+  rssm_status st = rssm_flush_step_classify(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T,
+                                            force, seed, out, scratch, scratch_bytes, stream);
   if (st != RSSM_OK) return st;
-  return rssm_flush_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force, seed,
-                                 out, scratch, scratch_bytes, stream);
+  return rssm_flush_step_main(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force, seed, out,
+                              scratch, scratch_bytes, stream);
 }
 
 rssm_status rssm_accept(const rssm_cache* cache, const int32_t* slot_idx, int32_t* pnat, const int32_t* accepted,

@@ -51,8 +51,7 @@ struct FlushRec {
 // flush when the flush is part of the call).
 struct RowRec {
   int s, r, p, Tb, tok0;
-  int flags;           // bit 0: compute the row's outputs (else zeros for Tb tokens); bit 1: fold it first;
-                       // bit 2: the appends overlap the live prefix the fold reads (the fused readout appends)
+  int flags;           // bit 0: compute the row's outputs (else zeros for Tb tokens); bit 1: fold it first
   int p_old;           // live count before the flush (bit 1 set)
   unsigned epoch_new;  // epoch of the checkpoint the fold writes (bit 1 set)
 };
@@ -85,11 +84,11 @@ struct StepArgs {
   int TP;  // T padded to 4 or 8
   int KB;  // ring rows padded to a multiple of 4
   uint16_t* out;
-  int flush_mode;            // 0: step only; 1: flush rows with p + T_b > W first; 2: flush every active row first
+  int flush_mode;            // rssm_flush_step: 1 flush rows with p + T_b > W first; 2 every active row
   unsigned long long seed;   // stochastic-rounding key of the fold (flush_mode != 0)
   int* pnat_rw;              // pnat, written by the fold's bookkeeping (flush_mode != 0)
-  unsigned* work;            // scratch: dynamic work counter of the fused readout (flush_mode != 0)
-  unsigned* gdone;           // scratch [batch][G]: heads of a (row, group) whose live rows have landed
+  unsigned* work;            // scratch: dynamic work counter of the step kernel (rssm_flush_step)
+  unsigned* gdone;           // scratch [batch][G]: heads of a (row, group) whose ring rows have landed
   RowRec* rows;  // scratch [batch]
   uint16_t* cf;  // scratch [batch][G][8][128]: C rows in the readout's MMA operand type
   float* rblk;   // scratch [batch][H][TP*kRStride + TP]: ring term R[t][d] (rows padded), then decay[t]
@@ -130,7 +129,8 @@ inline size_t flush_step_scratch_bytes(int batch, int H, int G, int L, int T) {
 int launch_flush(const FlushArgs& a, int num_sms, void* stream);
 int launch_precompute(const StepArgs& a, void* stream);
 int launch_readout(const StepArgs& a, int num_sms, void* stream);
-int launch_flush_readout(const StepArgs& a, int num_sms, void* stream);
+int launch_classify(const StepArgs& a, void* stream);
+int launch_flush_step(const StepArgs& a, int num_sms, void* stream);
 int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* accepted, const int* cu, int batch,
                   int T, void* stream);
 int launch_init(const InitArgs& a, void* stream);

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   __shared__ float dts[kHeadChunk][kMaxL];  // dt' of the live tokens; dt of the new ones (before bias, softplus)
   __shared__ float hp[3][kHeadChunk];       // A, D, dt_bias of the chunk's heads
   __shared__ __align__(16) float cfs[8][kMaxL][TP];  // per warp: coef[k][t] of its current head
-  __shared__ int meta[7];
+  __shared__ int meta[6];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -68,49 +68,26 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
     const int tok0 = __shfl_sync(0xffffffffu, v, 2), tok1 = __shfl_sync(0xffffffffu, v, 3);
     if (lane == 0) {
       int Tb = tok1 - tok0, flags = 0, p = 0, r = 0;
-      unsigned ep = 0u;
       const bool tb_ok = Tb >= 0 && Tb <= a.T;
       if (s >= 1 && s < c.S) {
         if (!tb_ok) {
           if (g == 0) set_error(c.err, RSSM_ERRBIT_SEQLEN);
-        } else if (a.flush_mode && (pn < 0 || pn > L)) {
-          if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);  // the flush's own check
+        } else if (pn < 0 || pn + Tb > L) {
+          if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);
         } else {
-          // with the flush in the same call: decide it here (the flush rule),
-          // then work on the ring as the flush leaves it
-          const int r0 = c.ring_start[s];
-          const bool fl = a.flush_mode == 2 || (a.flush_mode == 1 && pn + Tb > c.W);
-          p = fl ? 0 : pn;
-          r = fl ? (r0 + pn >= L ? r0 + pn - L : r0 + pn) : r0;
-          if (fl) {
-            ep = c.epoch[s] + 1u;
-            flags = 2;
-          }
-          // the step's check; with the flush in the call, new tokens that would
-          // land on live slots the fold still has to read are appended by
-          // the fused readout after the fold has its copy (bit 2)
-          if (p < 0 || p + Tb > L) {
-            if (g == 0) set_error(c.err, RSSM_ERRBIT_PNAT);
-          } else {
-            flags |= 1;
-            if (fl && pn + Tb > L) flags |= 4;
-          }
+          p = pn;
+          r = c.ring_start[s];
+          flags = 1;
         }
       }
       if (!tb_ok) Tb = 0;
-      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags & 1;
-      meta[6] = (flags >> 2) & 1;
-      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, pn, ep};
-    }
-    if (a.work && lane == 0) {  // the fused readout's counters
-      if (blockIdx.x == 0) *a.work = 0u;
-      a.gdone[blockIdx.x] = 0u;
+      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags;
+      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, p, 0u};
     }
   }
   __syncthreads();
   const int s = meta[0], r = meta[1], p = meta[2], Tb = meta[3], tok0 = meta[4];
   if (!meta[5] || Tb == 0) return;
-  const bool app = !meta[6];  // appends here (else by the fused readout, after its fold)
   const int K = p + Tb;  // logical tokens: p live ring rows, then the Tb new ones
   auto ring = [&](int k) {  // ring slot of logical token k < L
     const int q = r + k;
@@ -165,12 +142,12 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       if (t < Tb) {
         const float v = spec_softplus(__fadd_rn(dts[hh][p + t], hp[2][hh]));
         dts[hh][p + t] = v;
-        if (app) dslot[static_cast<long long>(hb + hh) * L + ring(p + t)] = v;
+        dslot[static_cast<long long>(hb + hh) * L + ring(p + t)] = v;
       }
     }
     if (h0 == 0) {
       // ring append of the new B rows
-      if (app && tid < Tb * 16) {
+      if (tid < Tb * 16) {
         const int t = tid >> 4, q = tid & 15;
         reinterpret_cast<uint4*>(bring + ring(p + t) * kDstate)[q] =
             reinterpret_cast<const uint4*>(bs + (p + t) * kDstate)[q];
@@ -212,7 +189,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       __syncthreads();
     }
     // ring appends of the chunk's new x rows
-    for (int idx = tid; app && idx < hc * 64; idx += 256) {
+    for (int idx = tid; idx < hc * 64; idx += 256) {
       const int hh = idx >> 6, t = (idx >> 3) & 7, q = idx & 7;
       if (t < Tb)
         reinterpret_cast<uint4*>(xslot + (static_cast<long long>(hb + hh) * L + ring(p + t)) * kDim)[q] =
