@@ -11,10 +11,11 @@
 //                S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
 //                in fp32, canonical order, then rounding to the state format.
 // The fold streams S0 (and the live x/B rows) through a 3-6 stage shared-memory
-// ring filled by 1-D bulk copies from a producer warp; 8 consumer warps own a
-// 4x8 fragment of the [64][128] state each and accumulate with packed f32x2
-// FMAs.  HBM traffic per unit: read + write of S0 (+ scales) and p rows of x
-// and B.
+// ring filled by a producer warp (1-D bulk copies; the dt' values by cp.async);
+// each of 8 consumer warps forms the weights itself and owns 8 rows of the
+// [64][128] state (a 4x8 fragment per lane), accumulating with packed f32x2
+// FMAs straight from the stage, with no barrier between the warps.  HBM
+// traffic per unit: read + write of S0 (+ scales) and p rows of x and B.
 #include <cuda_runtime.h>
 
 #include "rssm_device.cuh"
@@ -99,10 +100,12 @@ struct FoldMeta {
 
 struct FoldLayout {
   int ns, KB;
-  uint32_t s0_bytes, scale_off, x_off, b_off, w_off, stage_bytes;
-  uint32_t meta_off, stages_off, uf_off, bf_off, total;
+  uint32_t s0_bytes, scale_off, x_off, b_off, dt_off, sc_off, stage_bytes;
+  uint32_t meta_off, stages_off, total;
 };
 
+// one stage: S0 (as stored) | 8-bit scales | live x rows | live B rows | live
+// dt' | A of the head
 __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns) {
   FoldLayout f;
   f.ns = ns;
@@ -116,14 +119,14 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns) {
   o += f.KB * kDim * 2;
   f.b_off = o;
   o += f.KB * kDstate * 2;
-  f.w_off = o;
-  o += (f.KB + 4) * 4;
+  f.dt_off = o;
+  o += f.KB * 4;
+  f.sc_off = o;
+  o += 16;
   f.stage_bytes = (o + 127) & ~127u;
   f.meta_off = 256;  // after the barriers
   f.stages_off = 512;
-  f.uf_off = f.stages_off + f.ns * f.stage_bytes;
-  f.bf_off = f.uf_off + f.KB * kDim * 8;
-  f.total = f.bf_off + f.KB * kDstate * 4;
+  f.total = f.stages_off + f.ns * f.stage_bytes;
   return f;
 }
 
@@ -134,10 +137,11 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
   const FoldLayout lay = fold_layout(DT, c.L, ns);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
+  const int L = c.L, H = c.H;
 
   pdl_wait();  // the flag kernel's count and records
   pdl_trigger();
-  const long long units = static_cast<long long>(*a.count) * c.H;
+  const long long units = static_cast<long long>(*a.count) * H;
   const long long per = units / gridDim.x, rem = units % gridDim.x;
   const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
   const int nu = static_cast<int>(per + (blockIdx.x < rem ? 1 : 0));
@@ -145,53 +149,41 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 8;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 128);
   FoldMeta* meta = reinterpret_cast<FoldMeta*>(smem + lay.meta_off);
-  float2* uf2 = reinterpret_cast<float2*>(smem + lay.uf_off);
-  float* bfv = reinterpret_cast<float*>(smem + lay.bf_off);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
     for (int st = 0; st < lay.ns; ++st) {
-      mbar_init(&full[st], 1);
+      mbar_init(&full[st], 1 + 32);  // producer lane 0 + one cp.async arrival per producer lane
       mbar_init(&empty[st], kConsumerWarps);
     }
-    *abort_flag = 0;
     fence_barrier_init();
   }
   __syncthreads();
 
   if (warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
-    // The live dt' values of unit i+1 are loaded while unit i is issued, so the
-    // load latency overlaps the wait for a free stage.
-    auto unit_of = [&](int i, int& li, int& h) {
-      const long long u = u0 + i;
-      li = static_cast<int>(u / c.H);
-      h = static_cast<int>(u % c.H);
-    };
-    auto load_dt = [&](const FlushRec& rc, int h) {
-      return lane < rc.p ? c.dt_cache[static_cast<long long>(rc.s) * c.dt_stride + static_cast<long long>(h) * c.L +
-                                      (rc.r + lane) % c.L]
-                         : 0.0f;
-    };
-    int li_n, h_n;
-    unit_of(0, li_n, h_n);
-    FlushRec rec_n = a.recs[li_n];
-    float dt_n = load_dt(rec_n, h_n), A_n = a.A[h_n];
+    // Lane 0 copies S0 (+ scales) and the live x and B rows (at most two
+    // contiguous segments each) with 1-D bulk copies; the lanes copy the live
+    // dt' values and A of the head with cp.async.  Nothing here waits for a
+    // load it issued: the next unit's flagged-row record is loaded a unit ahead.
+    int li_c = static_cast<int>(u0 / H);
+    FlushRec rec = a.recs[li_c], rec_n = rec;
+    int li_n = li_c;
     int issued = 0;
     bool ok = true;
     for (int i = 0; i < nu; ++i) {
       const int st = i % lay.ns;
       const uint32_t ph = (i / lay.ns) & 1;
-      const FlushRec rec = rec_n;
-      const int h = h_n, li = li_n;
-      const float dtj = dt_n, Ah = A_n;
-      if (i + 1 < nu) {  // prefetch the next unit
-        unit_of(i + 1, li_n, h_n);
-        if (li_n != li) rec_n = a.recs[li_n];
-        dt_n = load_dt(rec_n, h_n);
-        A_n = a.A[h_n];
+      const long long u = u0 + i;
+      const int li = static_cast<int>(u / H), h = static_cast<int>(u % H);
+      if (li != li_c) {
+        rec = li == li_n ? rec_n : a.recs[li];
+        li_c = li;
+      }
+      if (i + 1 < nu && static_cast<int>((u + 1) / H) != li) {  // prefetch the next row's record
+        li_n = static_cast<int>((u + 1) / H);
+        rec_n = a.recs[li_n];
       }
       if (i >= lay.ns && !mbar_wait(&empty[st], ph ^ 1)) {
         ok = false;
@@ -199,6 +191,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
       }
       const int s = rec.s, r = rec.r, p = rec.p, g = h / c.hpg;
       uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
+      const float* dg = c.dt_cache + static_cast<long long>(s) * c.dt_stride + static_cast<long long>(h) * L;
       if (lane == 0) {
         const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + static_cast<uint32_t>(p) * (kDim * 2 + kDstate * 2);
         mbar_expect_tx(&full[st], bytes);
@@ -207,9 +200,9 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
         bulk_g2s(sb, st_g, lay.s0_bytes, &full[st]);
         if (k8bit) bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256,
                             &full[st]);
-        const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * c.L * kDim;
-        const uint16_t* bg = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * c.L * kDstate;
-        const int n1 = min(p, c.L - r);
+        const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * L * kDim;
+        const uint16_t* bg = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
+        const int n1 = min(p, L - r);
         if (n1 > 0) {
           bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
           bulk_g2s(sb + lay.b_off, bg + r * kDstate, n1 * kDstate * 2, &full[st]);
@@ -218,25 +211,14 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
           bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (p - n1) * kDim * 2, &full[st]);
           bulk_g2s(sb + lay.b_off + n1 * kDstate * 2, bg, (p - n1) * kDstate * 2, &full[st]);
         }
+        cp_async4(sb + lay.sc_off, a.A + h);
       }
-      // canonical cumulative sums c_j (sequential fp32) and weights
-      const float aj = lane < p ? __fmul_rn(Ah, dtj) : 0.0f;
-      float cj = 0.0f;
-      for (int k = 0; k < p; ++k) {
-        const float ak = __shfl_sync(0xffffffffu, aj, k);
-        if (lane >= k) cj = __fadd_rn(cj, ak);
-      }
-      const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
-      float* wv = reinterpret_cast<float*>(sb + lay.w_off);
-      if (lane < p) wv[lane] = __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj);
-      if (lane == 0) {
-        wv[lay.KB] = spec_exp(c_end);
-        meta[st] = FoldMeta{s, h, p, rec.epoch};
-      }
+      if (lane < p) cp_async4(sb + lay.dt_off + lane * 4, dg + (r + lane >= L ? r + lane - L : r + lane));
+      cp_async_arrive_noinc(&full[st]);
+      if (lane == 0) meta[st] = FoldMeta{s, h, p, rec.epoch};
       __syncwarp();
       if (lane == 0) mbar_arrive(&full[st]);
       issued = i + 1;
-      (void)li;
     }
     if (!ok) {
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
@@ -246,33 +228,33 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
     return;
   }
 
-  // ---------------- consumer warps ----------------
-  const int rs = lane >> 4, cc = lane & 15;
-  const int r0 = 8 * warp + 4 * rs, c0 = 8 * cc;
+  // ---------------- consumer warps: rows 8*warp .. 8*warp+7, each on its own ----------------
+  // lane: rows r0..r0+3, columns c0..c0+7
+  const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
   for (int i = 0; i < nu; ++i) {
     const int st = i % lay.ns;
     const uint32_t ph = (i / lay.ns) & 1;
     if (!mbar_wait(&full[st], ph)) {
-      *abort_flag = 1;
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+      return;
     }
-    consumer_sync();  // previous unit done with uf2/bfv; abort decision is uniform
-    if (*abort_flag) return;
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
     const FoldMeta m = meta[st];
-    const float* wv = reinterpret_cast<const float*>(sb + lay.w_off);
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
-    const uint32_t* bs = reinterpret_cast<const uint32_t*>(sb + lay.b_off);
-    for (int idx = tid; idx < m.p * kDim; idx += kConsumerThreads) {
-      const float uu = __fmul_rn(wv[idx >> 6], bf16f(xs[idx]));
-      uf2[idx] = make_float2(uu, uu);
+    const int p = m.p;
+    // canonical cumulative sums c_j (sequential fp32) and the weights
+    // w_j = e^{c_end - c_j} dt'_j (lane j holds w_j), decay = e^{c_end}
+    const float hA = reinterpret_cast<const float*>(sb + lay.sc_off)[0];
+    const float dtj = lane < p ? reinterpret_cast<const float*>(sb + lay.dt_off)[lane] : 0.0f;
+    const float aj = lane < p ? __fmul_rn(hA, dtj) : 0.0f;
+    float cj = 0.0f;
+    for (int k = 0; k < p; ++k) {
+      const float ak = __shfl_sync(0xffffffffu, aj, k);
+      if (lane >= k) cj = __fadd_rn(cj, ak);
     }
-    for (int idx = tid; idx < m.p * (kDstate / 2); idx += kConsumerThreads) {
-      const uint32_t wd = bs[idx];
-      reinterpret_cast<float2*>(bfv)[idx] = make_float2(bf16lo(wd), bf16hi(wd));
-    }
+    const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
+    const float wj = lane < p ? __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj) : 0.0f;
+    const float decay = spec_exp(c_end);
     // acc = e^{c_end} * S0f
-    const float decay = wv[lay.KB];
     float2 acc[4][4];
 #pragma unroll
     for (int i4 = 0; i4 < 4; ++i4) {
@@ -305,24 +287,25 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
       for (int q = 0; q < 4; ++q)
         acc[i4][q] = make_float2(__fmul_rn(decay, v[2 * q]), __fmul_rn(decay, v[2 * q + 1]));
     }
-    consumer_sync();  // uf2 / bfv complete
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);  // the stage is no longer read
-    // acc[d][n] = fma(u_j[d], B_j[n], acc), j ascending
-    for (int j = 0; j < m.p; ++j) {
-      const float4* up = reinterpret_cast<const float4*>(uf2 + j * kDim + r0);
-      const float4 u01 = up[0], u23 = up[1];
-      const float4* bp = reinterpret_cast<const float4*>(bfv + j * kDstate + c0);
-      const float4 b0 = bp[0], b1 = bp[1];
-      const float2 bb[4] = {make_float2(b0.x, b0.y), make_float2(b0.z, b0.w), make_float2(b1.x, b1.y),
-                            make_float2(b1.z, b1.w)};
-      const float2 uu[4] = {make_float2(u01.x, u01.y), make_float2(u01.z, u01.w), make_float2(u23.x, u23.y),
-                            make_float2(u23.z, u23.w)};
+    // acc[d][n] = fma(u_j[d], B_j[n], acc), j ascending, u_j[d] = w_j x_j[d]
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
+    const uint16_t* bs = reinterpret_cast<const uint16_t*>(sb + lay.b_off);
+    for (int j = 0; j < p; ++j) {
+      const float w = __shfl_sync(0xffffffffu, wj, j);
+      const uint2 xw = *reinterpret_cast<const uint2*>(xs + j * kDim + r0);
+      const float u0v = __fmul_rn(w, bf16lo(xw.x)), u1v = __fmul_rn(w, bf16hi(xw.x));
+      const float u2v = __fmul_rn(w, bf16lo(xw.y)), u3v = __fmul_rn(w, bf16hi(xw.y));
+      const uint4 bw = *reinterpret_cast<const uint4*>(bs + j * kDstate + c0);
+      const float2 bb[4] = {make_float2(bf16lo(bw.x), bf16hi(bw.x)), make_float2(bf16lo(bw.y), bf16hi(bw.y)),
+                            make_float2(bf16lo(bw.z), bf16hi(bw.z)), make_float2(bf16lo(bw.w), bf16hi(bw.w))};
+      const float2 uu[4] = {make_float2(u0v, u0v), make_float2(u1v, u1v), make_float2(u2v, u2v), make_float2(u3v, u3v)};
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[i4][q] = __ffma2_rn(uu[i4], bb[q], acc[i4][q]);
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
     float accf[4][8];
 #pragma unroll
     for (int i4 = 0; i4 < 4; ++i4)
