@@ -23,7 +23,11 @@
  *    otherwise; the library never allocates, frees or keeps a pointer after a
  *    call returns.  Temporary storage is a caller-provided `scratch` buffer
  *    of at least rssm_scratch_bytes() bytes ([FI] Description item 1:
- *    caller-provided scratch, allocated like the output, graph safe).
+ *    caller-provided scratch, allocated like the output, graph safe).  Zero
+ *    the buffer once when it is allocated: rssm_flush keeps a counter in its
+ *    first 4 bytes that must start at zero, and every call leaves it at zero
+ *    (after a call that reported RSSM_ERRBIT_TIMEOUT, zero it again).  The
+ *    first 256 bytes are the flush's; no other call writes them.
  *  - Streams: `stream` is a cudaStream_t (NULL = the legacy default
  *    stream).  Every call only enqueues kernels on it: no host
  *    synchronisation and no host read of device data, so calls can be

@@ -118,7 +118,9 @@ def alloc_scratch(cache: RssmCache, batch: int, T: int) -> torch.Tensor:
     n = rssm_scratch_bytes(cache, batch, T)
     if n == 0:
         raise RssmError("rssm_scratch_bytes", 1)
-    return torch.empty(n, dtype=torch.uint8, device=cache.state.device)
+    # zero-filled: rssm_flush keeps a counter in the first word, which must start
+    # at zero (every call leaves it at zero)
+    return torch.zeros(n, dtype=torch.uint8, device=cache.state.device)
 
 
 def rssm_init_state(cache, states, slot_idx, seed=0, stream=None):

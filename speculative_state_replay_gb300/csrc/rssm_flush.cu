@@ -1,21 +1,16 @@
-// rssm_flush.cu -- flush (classify + fold + requantise), init, accept.
+// rssm_flush.cu -- flush (classify + fold + requantise + bookkeeping), init,
+// accept.
 //
 // Flush of the ReplaySSM checkpointing SSU (FlashInfer PR #3975, commit note
 // on the persistent path: the write decision prev_k + T > max_window is
 // taken per slot at run time; vLLM PR #65660, Details: only the accepted
-// prefix enters the checkpoint).  Two kernels:
-//   flag_kernel  one CTA: per row decide flush, compact the flagged rows into
-//                scratch records and advance the ring bookkeeping
-//                (ring_start += p mod L, pnat = 0, epoch += 1).
-//   fold_kernel  persistent, one (flagged row, head) unit at a time:
-//                S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
-//                in fp32, canonical order, then rounding to the state format.
-// The fold streams S0 (and the live x/B rows) through a 3-6 stage shared-memory
-// ring filled by a producer warp (1-D bulk copies; the dt' values by cp.async);
-// each of 8 consumer warps forms the weights itself and owns 8 rows of the
-// [64][128] state (a 4x8 fragment per lane), accumulating with packed f32x2
-// FMAs straight from the stage, with no barrier between the warps.  HBM
-// traffic per unit: read + write of S0 (+ scales) and p rows of x and B.
+// prefix enters the checkpoint).  One persistent kernel, flush_kernel:
+//   every CTA classifies the rows (p + T_b > max_window, or all under force)
+//   and folds its range of (flagged row, head) units:
+//       S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
+//   in fp32, canonical order, then rounds to the state format; the CTA that
+//   finishes last advances the ring bookkeeping (ring_start += p mod L,
+//   pnat = 0, epoch += 1).
 #include <cuda_runtime.h>
 
 #include "rssm_device.cuh"
@@ -23,71 +18,49 @@
 namespace rssm {
 
 // ---------------------------------------------------------------------------
-// classification + compaction + bookkeeping (one CTA of 1024 threads)
+// classification
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(1024) flag_kernel(FlushArgs a) {
-  __shared__ int warp_tot[32];
-  __shared__ int base;
+struct RowFlag {
+  int flag, s, p;
+};
+
+// a row's flush decision: active rows with p + T_b > max_window (all active
+// rows under force); rows failing a check set an error bit (when `errors`)
+__device__ __forceinline__ RowFlag row_flag(const FlushArgs& a, int b, bool errors) {
   const Cache& c = a.c;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  pdl_wait();
-  pdl_trigger();
-  if (tid == 0) base = 0;
-  __syncthreads();
-  for (int b0 = 0; b0 < a.batch; b0 += 1024) {
-    const int b = b0 + tid;
-    int flag = 0;
-    FlushRec rec = {};
-    if (b < a.batch) {
-      const int s = a.slot_idx[b];
-      if (s >= 1 && s < c.S) {
-        const int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
-        const int p = a.pnat[b];
-        if (Tb < 0 || Tb > a.T) {
-          set_error(c.err, RSSM_ERRBIT_SEQLEN);
-        } else if (p < 0 || p > c.L) {
-          set_error(c.err, RSSM_ERRBIT_PNAT);
-        } else if (a.force || p + Tb > c.W) {
-          const int r = c.ring_start[s];
-          const unsigned e = c.epoch[s] + 1u;
-          rec.b = b;
-          rec.s = s;
-          rec.r = r;
-          rec.p = p;
-          rec.epoch = e;
-          flag = 1;
-          c.ring_start[s] = (r + p) % c.L;
-          a.pnat[b] = 0;
-          c.epoch[s] = e;
-        }
-      }
+  RowFlag f = {0, 0, 0};
+  const int s = a.slot_idx[b];
+  if (s >= 1 && s < c.S) {
+    const int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
+    const int p = a.pnat[b];
+    if (Tb < 0 || Tb > a.T) {
+      if (errors) set_error(c.err, RSSM_ERRBIT_SEQLEN);
+    } else if (p < 0 || p > c.L) {
+      if (errors) set_error(c.err, RSSM_ERRBIT_PNAT);
+    } else if (a.force || p + Tb > c.W) {
+      f = RowFlag{1, s, p};
     }
-    // block-wide inclusive scan of the flags
-    int v = flag;
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int n = __shfl_up_sync(0xffffffffu, v, off);
-      if (lane >= off) v += n;
-    }
-    if (lane == 31) warp_tot[warp] = v;
-    __syncthreads();
-    if (warp == 0) {
-      int t = warp_tot[lane];
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int n = __shfl_up_sync(0xffffffffu, t, off);
-        if (lane >= off) t += n;
-      }
-      warp_tot[lane] = t;
-    }
-    __syncthreads();
-    const int excl = base + v - flag + (warp ? warp_tot[warp - 1] : 0);
-    if (flag) a.recs[excl] = rec;
-    __syncthreads();
-    if (tid == 0) base += warp_tot[31];
-    __syncthreads();
   }
-  if (tid == 0) *a.count = base;
+  return f;
+}
+
+// exclusive prefix of `flag` over the CTA's threads in thread order (every
+// thread calls it); `total` gets the CTA's sum
+__device__ __forceinline__ int block_excl_scan(int flag, int* wsum, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned bal = __ballot_sync(0xffffffffu, flag);
+  const int wpre = __popc(bal & ((1u << lane) - 1u));
+  if (lane == 0) wsum[warp] = __popc(bal);
+  __syncthreads();
+  int before = 0, tot = 0;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) {
+    const int v = wsum[w];
+    if (w < warp) before += v;
+    tot += v;
+  }
+  __syncthreads();  // wsum is reused
+  total = tot;
+  return before + wpre;
 }
 
 // ---------------------------------------------------------------------------
@@ -101,12 +74,13 @@ struct FoldMeta {
 struct FoldLayout {
   int ns, KB;
   uint32_t s0_bytes, scale_off, x_off, b_off, dt_off, sc_off, stage_bytes;
-  uint32_t meta_off, stages_off, total;
+  uint32_t meta_off, rows_off, stages_off, total;
 };
 
-// one stage: S0 (as stored) | 8-bit scales | live x rows | live B rows | live
-// dt' | A of the head
-__host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns) {
+// barriers | per-stage metadata | the records of the flushed rows this CTA
+// folds (up to `maxrows`) | stages; one stage: S0 (as stored) | 8-bit scales |
+// live x rows | live B rows | live dt' | A of the head
+__host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int maxrows) {
   FoldLayout f;
   f.ns = ns;
   f.KB = (L + 3) & ~3;
@@ -125,31 +99,32 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns) {
   o += 16;
   f.stage_bytes = (o + 127) & ~127u;
   f.meta_off = 256;  // after the barriers
-  f.stages_off = 512;
+  f.rows_off = 512;
+  f.stages_off = (f.rows_off + maxrows * static_cast<uint32_t>(sizeof(FlushRec)) + 127) & ~127u;
   f.total = f.stages_off + f.ns * f.stage_bytes;
   return f;
 }
 
+// Classification, fold, requantisation and bookkeeping of rssm_flush in one
+// kernel.  Every CTA classifies all rows (two passes over slot_idx, pnat and
+// the sequence bounds) and keeps the records of the flushed rows its range of
+// (flushed row, head) units covers; the producer and consumer warps then fold
+// those units; the CTA that finishes last (a self-resetting ticket) writes the
+// bookkeeping, after every CTA has read the values it replaces.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) {
+__global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns, int maxrows) {
   extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ int wsum[kThreads / 32];
+  __shared__ int s_last;
   const Cache& c = a.c;
-  const FoldLayout lay = fold_layout(DT, c.L, ns);
+  const FoldLayout lay = fold_layout(DT, c.L, ns, maxrows);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
   const int L = c.L, H = c.H;
-
-  pdl_wait();  // the flag kernel's count and records
-  pdl_trigger();
-  const long long units = static_cast<long long>(*a.count) * H;
-  const long long per = units / gridDim.x, rem = units % gridDim.x;
-  const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
-  const int nu = static_cast<int>(per + (blockIdx.x < rem ? 1 : 0));
-  if (nu == 0) return;
-
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 8;
   FoldMeta* meta = reinterpret_cast<FoldMeta*>(smem + lay.meta_off);
+  FlushRec* rows_s = reinterpret_cast<FlushRec*>(smem + lay.rows_off);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
   if (tid == 0) {
@@ -159,17 +134,42 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
     }
     fence_barrier_init();
   }
-  __syncthreads();
+  pdl_wait();  // pnat as the previous call left it
+  pdl_trigger();
+  // pass 1: the number of flushed rows (CTA 0 reports bad rows)
+  int count = 0;
+  for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+    const int b = b0 + tid;
+    const int f = b < a.batch ? row_flag(a, b, blockIdx.x == 0).flag : 0;
+    count += __syncthreads_count(f);
+  }
+  const long long units = static_cast<long long>(count) * H;
+  const long long per = units / gridDim.x, rem = units % gridDim.x;
+  const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
+  const int nu = static_cast<int>(per + (blockIdx.x < rem ? 1 : 0));
+  const int li_first = nu > 0 ? static_cast<int>(u0 / H) : 0;
+  if (nu > 0) {
+    // pass 2: compacted positions; the records of the rows this CTA folds
+    const int li_last = static_cast<int>((u0 + nu - 1) / H);
+    int base = 0;
+    for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+      const int b = b0 + tid;
+      const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0};
+      int tot = 0;
+      const int pos = base + block_excl_scan(f.flag, wsum, tot);
+      if (f.flag && pos >= li_first && pos <= li_last)
+        rows_s[pos - li_first] = FlushRec{b, f.s, c.ring_start[f.s], f.p, c.epoch[f.s] + 1u, {0, 0, 0}};
+      base += tot;
+    }
+  }
+  __syncthreads();  // barriers initialised, records in place
 
-  if (warp == kConsumerWarps) {
+  if (nu > 0 && warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
     // Lane 0 copies S0 (+ scales) and the live x and B rows (at most two
     // contiguous segments each) with 1-D bulk copies; the lanes copy the live
     // dt' values and A of the head with cp.async.  Nothing here waits for a
     // load it issued: the next unit's flagged-row record is loaded a unit ahead.
-    int li_c = static_cast<int>(u0 / H);
-    FlushRec rec = a.recs[li_c], rec_n = rec;
-    int li_n = li_c;
     int issued = 0;
     bool ok = true;
     for (int i = 0; i < nu; ++i) {
@@ -177,14 +177,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
       const uint32_t ph = (i / lay.ns) & 1;
       const long long u = u0 + i;
       const int li = static_cast<int>(u / H), h = static_cast<int>(u % H);
-      if (li != li_c) {
-        rec = li == li_n ? rec_n : a.recs[li];
-        li_c = li;
-      }
-      if (i + 1 < nu && static_cast<int>((u + 1) / H) != li) {  // prefetch the next row's record
-        li_n = static_cast<int>((u + 1) / H);
-        rec_n = a.recs[li_n];
-      }
+      const FlushRec rec = rows_s[li - li_first];
       if (i >= lay.ns && !mbar_wait(&empty[st], ph ^ 1)) {
         ok = false;
         break;
@@ -225,9 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
       // let copies already in flight land before the CTA can exit
       for (int i = max(0, issued - lay.ns); i < issued; ++i) mbar_wait(&full[i % lay.ns], (i / lay.ns) & 1);
     }
-    return;
-  }
-
+  } else if (nu > 0) {
   // ---------------- consumer warps: rows 8*warp .. 8*warp+7, each on its own ----------------
   // lane: rows r0..r0+3, columns c0..c0+7
   const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
@@ -236,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
     const uint32_t ph = (i / lay.ns) & 1;
     if (!mbar_wait(&full[st], ph)) {
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
-      return;
+      break;
     }
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
     const FoldMeta m = meta[st];
@@ -319,6 +310,35 @@ __global__ void __launch_bounds__(kThreads, 2) fold_kernel(FlushArgs a, int ns) 
     float* head_scale = k8bit ? c.scale + static_cast<long long>(m.s) * c.scale_stride + m.h * kDim : nullptr;
     quantize_store<DT>(accf, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(m.h),
                        static_cast<uint32_t>(m.s), m.epoch, a.seed);
+  }
+  }
+
+  // ---------------- the flush's bookkeeping, by the last CTA to finish ----------------
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();  // this CTA's reads of pnat, ring_start and epochs are done
+    s_last = atomicInc(a.ticket, gridDim.x - 1) == gridDim.x - 1;  // wraps back to 0
+  }
+  __syncthreads();
+  if (s_last) {
+    __threadfence();
+    int base = 0;
+    for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+      const int b = b0 + tid;
+      const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0};
+      int tot = 0;
+      const int pos = base + block_excl_scan(f.flag, wsum, tot);
+      if (f.flag) {
+        const int r = c.ring_start[f.s];
+        const unsigned e = c.epoch[f.s] + 1u;
+        a.recs[pos] = FlushRec{b, f.s, r, f.p, e, {0, 0, 0}};
+        c.ring_start[f.s] = r + f.p >= L ? r + f.p - L : r + f.p;  // (r + p) mod L
+        a.pnat[b] = 0;
+        c.epoch[f.s] = e;
+      }
+      base += tot;
+    }
+    if (tid == 0) *a.count = base;
   }
 }
 
@@ -412,35 +432,33 @@ __global__ void spec_math_kernel(const float* in, float* oexp, float* osp, long 
 // launchers
 // ---------------------------------------------------------------------------
 template <int DT>
-static int launch_fold_t(const FlushArgs& a, int num_sms, cudaStream_t st) {
-  // two CTAs per SM: as many stages (3..6) as fit 113 KB
-  int ns = 6;
-  while (ns > 2 && fold_layout(DT, a.c.L, ns).total > 113 * 1024) --ns;
-  const FoldLayout lay = fold_layout(DT, a.c.L, ns);
-  cudaError_t e = cudaFuncSetAttribute(fold_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+static int launch_flush_t(const FlushArgs& a, int num_sms, cudaStream_t st) {
+  // a fixed grid of two CTAs per SM (the number of flushed rows is only known
+  // on the device); the rows table holds the most rows one CTA's units span
+  const int grid = 2 * num_sms;
+  const long long nu_max = (static_cast<long long>(a.batch) * a.c.H + grid - 1) / grid;
+  const int maxrows = static_cast<int>(nu_max / a.c.H) + 2;
+  int ns = 6;  // as many stages (3..6) as fit 113 KB
+  while (ns > 2 && fold_layout(DT, a.c.L, ns, maxrows).total > 113 * 1024) --ns;
+  const FoldLayout lay = fold_layout(DT, a.c.L, ns, maxrows);
+  if (lay.total > 225 * 1024) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(flush_kernel<DT>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(fold_kernel<DT>, cudaFuncAttributePreferredSharedMemoryCarveout,
+  e = cudaFuncSetAttribute(flush_kernel<DT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  // the number of flagged rows is only known on the device: size the grid for
-  // the worst case (every row flagged), capped at one CTA per SM
-  const long long units = static_cast<long long>(a.batch) * a.c.H;
-  const long long cap = 2LL * num_sms;
-  const int grid = static_cast<int>(units < cap ? (units > 0 ? units : 1) : cap);
-  e = launch_pdl(fold_kernel<DT>, dim3(grid), dim3(kThreads), lay.total, st, a, ns);
+  e = launch_pdl(flush_kernel<DT>, dim3(grid), dim3(kThreads), lay.total, st, a, ns, maxrows);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 int launch_flush(const FlushArgs& a, int num_sms, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = launch_pdl(flag_kernel, dim3(1), dim3(1024), 0, st, a);
-  if (e != cudaSuccess) return e;
   switch (a.c.dtype) {
-    case RSSM_F32: return launch_fold_t<RSSM_F32>(a, num_sms, st);
-    case RSSM_BF16: return launch_fold_t<RSSM_BF16>(a, num_sms, st);
-    case RSSM_F16: return launch_fold_t<RSSM_F16>(a, num_sms, st);
-    case RSSM_I8: return launch_fold_t<RSSM_I8>(a, num_sms, st);
-    default: return launch_fold_t<RSSM_E4M3>(a, num_sms, st);
+    case RSSM_F32: return launch_flush_t<RSSM_F32>(a, num_sms, st);
+    case RSSM_BF16: return launch_flush_t<RSSM_BF16>(a, num_sms, st);
+    case RSSM_F16: return launch_flush_t<RSSM_F16>(a, num_sms, st);
+    case RSSM_I8: return launch_flush_t<RSSM_I8>(a, num_sms, st);
+    default: return launch_flush_t<RSSM_E4M3>(a, num_sms, st);
   }
 }
 

@@ -128,9 +128,10 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->pnat_rw = nullptr;
   a->work = nullptr;
   a->gdone = nullptr;
-  a->rows = static_cast<RowRec*>(scratch);
-  a->cf = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch));
-  a->rblk = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) + step_rows_bytes(batch) +
+  uint8_t* sc = static_cast<uint8_t*>(scratch) + kScratchHead;  // past the flush's ticket word
+  a->rows = reinterpret_cast<RowRec*>(sc);
+  a->cf = reinterpret_cast<uint16_t*>(sc + step_rows_bytes(batch));
+  a->rblk = reinterpret_cast<float*>(sc + step_rows_bytes(batch) +
                                      step_cf_bytes(batch, cache->ngroups, T));
   return RSSM_OK;
 }
@@ -182,8 +183,9 @@ rssm_status rssm_flush(const rssm_cache* cache, const float* A, const int32_t* s
   a.T = T;
   a.force = force;
   a.seed = seed;
-  a.count = static_cast<int*>(scratch);
-  a.recs = reinterpret_cast<FlushRec*>(static_cast<uint8_t*>(scratch) + 256);
+  a.ticket = static_cast<unsigned*>(scratch);
+  a.count = static_cast<int*>(scratch) + 1;
+  a.recs = reinterpret_cast<FlushRec*>(static_cast<uint8_t*>(scratch) + kScratchHead);
   return launch_flush(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 

@@ -64,8 +64,9 @@ struct FlushArgs {
   const int* cu;
   int batch, T, force;
   unsigned long long seed;
-  int* count;      // scratch: number of flagged rows
-  FlushRec* recs;  // scratch: flagged rows
+  unsigned* ticket;  // scratch word: CTAs done with the flush (zero between calls)
+  int* count;        // scratch: number of flagged rows (written at the end, for diagnostics)
+  FlushRec* recs;    // scratch: flagged rows (written at the end, for diagnostics)
 };
 
 struct StepArgs {
@@ -106,8 +107,10 @@ inline int ring_pad(int L) { return (L + 3) & ~3; }
 inline int t_pad(int T) { return T <= 4 ? 4 : 8; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// scratch layout
-inline size_t flush_scratch_bytes(int batch) { return 256 + align_up(sizeof(FlushRec) * (size_t)batch, 256); }
+// scratch layout: the first kScratchHead bytes hold the flush's ticket word
+// (zero between calls) and count; every other layout starts after them
+constexpr size_t kScratchHead = 256;
+inline size_t flush_scratch_bytes(int batch) { return kScratchHead + align_up(sizeof(FlushRec) * (size_t)batch, 256); }
 inline size_t step_rows_bytes(int batch) { return align_up(sizeof(RowRec) * (size_t)batch, 256); }
 inline size_t step_cf_bytes(int batch, int G, int T) {
   (void)T;
@@ -117,7 +120,7 @@ inline size_t step_rblk_floats(int T) { return (size_t)t_pad(T) * kRStride + t_p
 inline size_t step_scratch_bytes(int batch, int H, int G, int L, int T) {
   (void)L;
   const size_t blk = step_rblk_floats(T) * sizeof(float);
-  return step_rows_bytes(batch) + step_cf_bytes(batch, G, T) + align_up(blk * (size_t)batch * H, 256);
+  return kScratchHead + step_rows_bytes(batch) + step_cf_bytes(batch, G, T) + align_up(blk * (size_t)batch * H, 256);
 }
 // the flush+step call: the step's scratch, then the work counter, then the
 // per-(row, group) landed-head counters
