@@ -67,6 +67,31 @@ def workload(args):
     return W.config(args.config, **kw)
 
 
+def profiled_traffic(kernel, workload_name):
+    """DRAM bytes per launch (dram__bytes_read + dram__bytes_write) from the
+    committed ncu summary of `kernel` on this workload, if the kernel's sources
+    still hash as they did when the counters were taken; else None."""
+    import hashlib
+    import re
+
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload_name}.md")
+    if not os.path.exists(path):
+        return None
+    text = open(path).read()
+    fields = dict(re.findall(r"^\s+(traffic_bytes_per_launch|workload|sources|sources_sha256): (.+)$", text, re.M))
+    if fields.get("workload") != workload_name or "sources" not in fields:
+        return None
+    h = hashlib.sha256()
+    for src in fields["sources"].split():
+        fp = os.path.join(ROOT, src)
+        if not os.path.exists(fp):
+            return None
+        h.update(open(fp, "rb").read())
+    if h.hexdigest() != fields.get("sources_sha256"):
+        return None
+    return float(fields["traffic_bytes_per_launch"])
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -526,7 +551,9 @@ def run_gpu(args, rank, ws, local):
                        launch="one CUDA graph per step (kernels chained by programmatic dependent launch); kernel times from a second pass with one graph per launch group",
                        force_flush=bool(args.force_flush), path=args.path),
         "roofline": {"bound": "hbm", "kernel": "step_kernel" if fused else "readout_kernel",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak, "traffic": None,
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": None if fused or args.batch is not None else profiled_traffic("readout_kernel", wl.name),
+                     "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_source": peak_kind, "avg_launch_us": 1e3 * statistics.mean(read_ms),
                      "algorithmic_bytes_per_launch": read_bytes / args.steps,
                      "folded_units_per_launch": fold_units / args.steps},
