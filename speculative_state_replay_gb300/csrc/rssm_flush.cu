@@ -172,11 +172,15 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
     // load it issued: the next unit's flagged-row record is loaded a unit ahead.
     int issued = 0;
     bool ok = true;
-    for (int i = 0; i < nu; ++i) {
-      const int st = i % lay.ns;
-      const uint32_t ph = (i / lay.ns) & 1;
-      const long long u = u0 + i;
-      const int li = static_cast<int>(u / H), h = static_cast<int>(u % H);
+    // stage index and phase, and the unit's (flushed row, head), advance by
+    // increments: no division on the per-unit path
+    int st = 0, li = li_first, h = static_cast<int>(u0 % H);
+    uint32_t ph = 0;
+    for (int i = 0; i < nu; ++i, h = h + 1 == H ? 0 : h + 1, li += h == 0 ? 1 : 0) {
+      if (i > 0 && ++st == lay.ns) {
+        st = 0;
+        ph ^= 1u;
+      }
       const FlushRec rec = rows_s[li - li_first];
       if (i >= lay.ns && !mbar_wait(&empty[st], ph ^ 1)) {
         ok = false;
@@ -222,9 +226,13 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
   // ---------------- consumer warps: rows 8*warp .. 8*warp+7, each on its own ----------------
   // lane: rows r0..r0+3, columns c0..c0+7
   const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
+  int st = 0;
+  uint32_t ph = 0;
   for (int i = 0; i < nu; ++i) {
-    const int st = i % lay.ns;
-    const uint32_t ph = (i / lay.ns) & 1;
+    if (i > 0 && ++st == lay.ns) {
+      st = 0;
+      ph ^= 1u;
+    }
     if (!mbar_wait(&full[st], ph)) {
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
       break;

@@ -128,6 +128,7 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->pnat_rw = nullptr;
   a->work = nullptr;
   a->gdone = nullptr;
+  a->rwork = static_cast<unsigned*>(scratch) + 2;  // a word of the scratch head (the flush uses words 0, 1)
   uint8_t* sc = static_cast<uint8_t*>(scratch) + kScratchHead;  // past the flush's ticket word
   a->rows = reinterpret_cast<RowRec*>(sc);
   a->cf = reinterpret_cast<uint16_t*>(sc + step_rows_bytes(batch));

@@ -89,6 +89,7 @@ struct StepArgs {
   unsigned long long seed;   // stochastic-rounding key of the fold (flush_mode != 0)
   int* pnat_rw;              // pnat, written by the fold's bookkeeping (flush_mode != 0)
   unsigned* work;            // scratch: dynamic work counter of the step kernel (rssm_flush_step)
+  unsigned* rwork;           // scratch word: the readout's chunk counter, zeroed by the precompute
   unsigned* gdone;           // scratch [batch][G]: heads of a (row, group) whose ring rows have landed
   RowRec* rows;  // scratch [batch]
   uint16_t* cf;  // scratch [batch][G][8][128]: C rows in the readout's MMA operand type

@@ -45,6 +45,8 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2,
 // one 64-bit shared load; the sum over k is unchanged.  S0 arrives by TMA
 // tensor copies with the 128-byte swizzle, which keeps those loads
 // conflict-free.
+constexpr int kReadChunk = 4;  // (row, head) units per work grab of the readout
+
 struct ReadMeta {
   int b, h, s, r, p, Tb, tok0, flags;
 };

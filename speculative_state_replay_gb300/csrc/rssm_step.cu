@@ -83,6 +83,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       if (!tb_ok) Tb = 0;
       meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags;
       if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, p, 0u};
+      if (blockIdx.x == 0) *a.rwork = 0u;  // the readout's chunk counter
     }
   }
   __syncthreads();
@@ -271,11 +272,12 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
   const int H = c.H;
 
-  const long long units = static_cast<long long>(a.batch) * H;
-  const long long per = units / gridDim.x, rem = units % gridDim.x;
-  const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
-  const int nu = static_cast<int>(per + (blockIdx.x < rem ? 1 : 0));
-  if (nu == 0) return;
+  // Units are taken in chunks of kReadChunk consecutive (row, head) pairs:
+  // each CTA's first chunk is chunk blockIdx.x (its S0 can be requested
+  // before the precompute has finished); later chunks come from a counter the
+  // precompute zeroes, so CTAs that stream faster take more of them.
+  const unsigned units = static_cast<unsigned>(a.batch) * static_cast<unsigned>(H);
+  const unsigned nchunks = (units + kReadChunk - 1) / kReadChunk;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 8;
@@ -294,44 +296,61 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   if (warp == kConsumerWarps) {
     // ---------------- producer: one lane issues all copies ----------------
     if (lane != 0) return;
-    // Before waiting for the precompute: request S0 of the first stages.  S0
-    // is final by now (the precompute waited for the flush before it let this
-    // kernel launch) and needs only the slot id, an input of the call.
-    const int npre = nu < ns ? nu : ns;
+    // Before waiting for the precompute: request S0 of the first chunk's
+    // units.  S0 is final by now (the precompute waited for the flush before
+    // it let this kernel launch) and needs only the slot id, an input of the call.
+    unsigned u = blockIdx.x * kReadChunk, cend = min(u + kReadChunk, units);
+    int b = static_cast<int>(u / H), h = static_cast<int>(u % H);
+    const int npre = static_cast<int>(cend - u) < ns ? static_cast<int>(cend - u) : ns;
     uint32_t pre = 0u;
-    for (int i = 0; i < npre; ++i) {
-      const long long u = u0 + i;
-      const int b = static_cast<int>(u / H), h = static_cast<int>(u % H);
-      const int s = a.slot_idx[b];
+    for (int i = 0, pb = b, phh = h; i < npre; ++i, phh = phh + 1 == H ? 0 : phh + 1, pb += phh == 0 ? 1 : 0) {
+      const int s = a.slot_idx[pb];
       if (s >= 1 && s < c.S) {
         uint8_t* sb = smem + lay.stages_off + i * lay.stage_bytes;
         mbar_expect_tx(&full[i], lay.s0_bytes);
 #pragma unroll
-        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[i]);
+        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), phh * kDim, s, &full[i]);
         pre |= 1u << i;
       }
     }
-    pdl_wait();  // row records, C blocks, ring terms
+    pdl_wait();  // row records, C blocks, ring terms, the chunk counter
     pdl_trigger();
+    unsigned next = atomicAdd(a.rwork, 1u);  // the chunk after this one (read at the switch)
     int cur_b = -1, cur_bg = -1;
     RowRec rr = {};
     int issued = 0;
     bool ok = true;
-    for (int i = 0; i < nu; ++i) {
-      const int st = i % ns;
-      const uint32_t ph = (i / ns) & 1;
+    // per unit: stage index and phase, the (row, head) and the head's group
+    // advance by increments (no division on the per-unit path)
+    int st = 0, g = h / c.hpg, hh = h % c.hpg;
+    uint32_t ph = 0;
+    const int rstride = TP * kRStride + TP;
+    for (int i = 0;; ++i) {
+      if (u >= cend) {  // next chunk
+        const unsigned ch = gridDim.x + next;
+        if (ch >= nchunks) break;
+        u = ch * kReadChunk;
+        cend = min(u + kReadChunk, units);
+        b = static_cast<int>(u / H);
+        h = static_cast<int>(u % H);
+        g = h / c.hpg;
+        hh = h % c.hpg;
+        next = atomicAdd(a.rwork, 1u);
+      }
+      if (i > 0 && ++st == ns) {
+        st = 0;
+        ph ^= 1u;
+      }
       if (i >= ns && !mbar_wait(&empty[st], ph ^ 1)) {
         ok = false;
         break;
       }
-      const long long u = u0 + i;
-      const int b = static_cast<int>(u / H), h = static_cast<int>(u % H);
       if (b != cur_b) {
         rr = a.rows[b];
         cur_b = b;
       }
       const bool active = (rr.flags & 1) && rr.Tb > 0;
-      const int g = h / c.hpg, bg = b * c.G + g;
+      const int bg = b * c.G + g;
       // the C block is copied only when the (row, group) changes: consumers
       // keep its fragments in registers (flags bit 1 tells them to reload)
       const bool newc = active && bg != cur_bg;
@@ -343,21 +362,41 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         const bool have_s0 = i < npre && ((pre >> i) & 1u);
         const uint32_t bytes =
             (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + (newc ? 8u * kDstate * 2 : 0u) + lay.r_bytes;
-        mbar_expect_tx(&full[st], bytes);
+        mbar_arrive_expect_tx(&full[st], bytes);
         if (!have_s0) {
 #pragma unroll
           for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
         }
         if (k8bit)
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
-        if (newc)
-          bulk_g2s(sb + lay.c_off, a.cf + (static_cast<long long>(b) * c.G + g) * 8 * kDstate, 8 * kDstate * 2,
-                   &full[st]);
-        bulk_g2s(sb + lay.r_off, a.rblk + (static_cast<long long>(b) * H + h) * (TP * kRStride + TP), lay.r_bytes,
-                 &full[st]);
+        if (newc) bulk_g2s(sb + lay.c_off, a.cf + static_cast<long long>(bg) * 8 * kDstate, 8 * kDstate * 2, &full[st]);
+        bulk_g2s(sb + lay.r_off, a.rblk + static_cast<long long>(u) * rstride, lay.r_bytes, &full[st]);
+      } else {
+        mbar_arrive(&full[st]);
       }
-      mbar_arrive(&full[st]);
       issued = i + 1;
+      ++u;
+      if (++h == H) {
+        h = 0;
+        ++b;
+        g = 0;
+        hh = 0;
+      } else if (++hh == c.hpg) {
+        hh = 0;
+        ++g;
+      }
+    }
+    if (ok) {  // end of work for the consumers
+      if (++st == ns) {
+        st = 0;
+        ph ^= 1u;
+      }
+      if (issued >= ns && !mbar_wait(&empty[st], ph ^ 1)) {
+        ok = false;
+      } else {
+        meta[st].flags = 8;
+        mbar_arrive(&full[st]);
+      }
     }
     if (!ok) {
       set_error(c.err, RSSM_ERRBIT_TIMEOUT);
@@ -371,14 +410,19 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   const int d = 8 * warp + g;        // B column (row of S0) this lane loads
   const int dout = 8 * warp + 2 * cq;  // output rows this lane writes (dout, dout + 1)
   uint2 af[8];                          // C block fragments of the current (row, group)
-  for (int i = 0; i < nu; ++i) {
-    const int st = i % ns;
-    const uint32_t ph = (i / ns) & 1;
+  int st = 0;
+  uint32_t ph = 0;
+  for (int i = 0;; ++i) {
+    if (i > 0 && ++st == ns) {
+      st = 0;
+      ph ^= 1u;
+    }
     if (!mbar_wait(&full[st], ph)) {
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
       return;
     }
     const ReadMeta m = meta[st];
+    if (m.flags & 8) return;  // no more work
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
     if (!(m.flags & 1)) {
       // inactive or rejected row: zero outputs, no cache update
@@ -455,9 +499,9 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
   if (occ > ctas) occ = ctas;
-  const long long units = static_cast<long long>(a.batch) * a.c.H;
+  const long long chunks = (static_cast<long long>(a.batch) * a.c.H + kReadChunk - 1) / kReadChunk;
   const long long cap = static_cast<long long>(num_sms) * occ;
-  const int grid = static_cast<int>(units < cap ? units : cap);
+  const int grid = static_cast<int>(chunks < cap ? chunks : cap);  // every CTA has a first chunk
   e = launch_pdl(readout_kernel<DT, TP>, dim3(grid), dim3(kThreads), lay.total, st, map, a, ns);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
