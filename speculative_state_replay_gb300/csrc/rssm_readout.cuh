@@ -57,18 +57,20 @@ struct ReadLayout {
   uint32_t stages_off, total;
 };
 
-__host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns) {
+// one stage of a unit of `hpu` consecutive heads of one group: S0 as esz
+// boxes of 64*hpu rows x 128 bytes | 8-bit scales | C block | ring terms
+__host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int hpu = 1) {
   ReadLayout f;
   f.ns = ns;
   const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
-  f.s0_bytes = kHeadElems * esz;  // esz boxes of 64 rows x 128 bytes
+  f.s0_bytes = kHeadElems * esz * hpu;
   uint32_t o = f.s0_bytes;
   f.scale_off = o;
-  if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
+  if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256 * hpu;
   f.c_off = o;
   o += 8 * kDstate * 2;
   f.r_off = o;
-  f.r_bytes = (TP * kRStride + TP) * 4;
+  f.r_bytes = (TP * kRStride + TP) * 4 * hpu;
   o += f.r_bytes;
   f.stage_bytes = (o + 1023) & ~1023u;  // the swizzled boxes need 1024-byte alignment
   f.stages_off = 1024;                  // barriers and per-stage metadata
@@ -106,7 +108,8 @@ __device__ __forceinline__ void load_c_frags(const uint16_t* cblk, int g, int c,
 
 // S0 . C over dstate for state rows d (lane's B column) of this warp; even and
 // odd k steps accumulate in separate chains, added at the end
-template <int DT>
+// (BOXB: bytes between the column boxes of a 2- or 4-byte state)
+template <int DT, int BOXB = 8192>
 __device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8], int d, int c, float (&acc)[4]) {
   float a2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
@@ -115,14 +118,14 @@ __device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8]
     float(&ac)[4] = a2[ks & 1];
     if constexpr (DT == RSSM_BF16 || DT == RSSM_F16) {
       const int kb = (ks * 16 + 4 * c) * 2;  // byte within the 256-byte row
-      const uint2 bv = *reinterpret_cast<const uint2*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
+      const uint2 bv = *reinterpret_cast<const uint2*>(s0 + (kb >> 7) * BOXB + swz(d, kb & 127));
       if constexpr (DT == RSSM_BF16)
         mma_bf16(ac, av.x, av.y, bv.x, bv.y);
       else
         mma_f16(ac, av.x, av.y, bv.x, bv.y);
     } else if constexpr (DT == RSSM_F32) {
       const int kb = (ks * 16 + 4 * c) * 4;
-      const float4 f = *reinterpret_cast<const float4*>(s0 + (kb >> 7) * 8192 + swz(d, kb & 127));
+      const float4 f = *reinterpret_cast<const float4*>(s0 + (kb >> 7) * BOXB + swz(d, kb & 127));
       const uint32_t h01 = pack_bf16(f.x, f.y), h23 = pack_bf16(f.z, f.w);
       const uint32_t l01 = pack_bf16(f.x - bf16_lo_f(h01), f.y - bf16_hi_f(h01));
       const uint32_t l23 = pack_bf16(f.z - bf16_lo_f(h23), f.w - bf16_hi_f(h23));
@@ -168,7 +171,9 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 }
 
 // S0 of all slots as a 3-D tensor [slot][H*64 rows][128], boxes of 64 rows x 128 bytes, 128-byte swizzle
-inline bool encode_state_map(const Cache& c, CUtensorMap* map) {
+// S0 of all slots as a 3-D tensor [slot][H*64 rows][128], boxes of 64*hpu rows
+// x 128 bytes, 128-byte swizzle
+inline bool encode_state_map(const Cache& c, CUtensorMap* map, int hpu = 1) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
   const int esz = c.dtype == RSSM_F32 ? 4 : (c.dtype == RSSM_BF16 || c.dtype == RSSM_F16) ? 2 : 1;
@@ -177,7 +182,7 @@ inline bool encode_state_map(const Cache& c, CUtensorMap* map) {
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kDstate), static_cast<cuuint64_t>(c.H) * kDim,
                               static_cast<cuuint64_t>(c.S)};
   const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kDstate) * esz, static_cast<cuuint64_t>(c.state_stride) * esz};
-  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kDim), 1};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / esz), static_cast<cuuint32_t>(kDim * hpu), 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return enc(map, dt, 3, c.state, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;

@@ -262,21 +262,24 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 // ---------------------------------------------------------------------------
 // readout
 // ---------------------------------------------------------------------------
-template <int DT, int TP>
+// HPU: heads per unit (2 for 8-bit states when a group has an even number of
+// heads: the unit's copies then carry twice the bytes for the same work)
+template <int DT, int TP, int HPU>
 __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Cache& c = a.c;
-  const ReadLayout lay = read_layout(DT, TP, ns);
+  const ReadLayout lay = read_layout(DT, TP, ns, HPU);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
-  const int H = c.H;
+  constexpr int kBox = 8192 * HPU;  // bytes of one column box of S0 (64*HPU rows x 128 bytes)
+  const int H = c.H, HU = H / HPU;
 
   // Units are taken in chunks of kReadChunk consecutive (row, head) pairs:
   // each CTA's first chunk is chunk blockIdx.x (its S0 can be requested
   // before the precompute has finished); later chunks come from a counter the
   // precompute zeroes, so CTAs that stream faster take more of them.
-  const unsigned units = static_cast<unsigned>(a.batch) * static_cast<unsigned>(H);
+  const unsigned units = static_cast<unsigned>(a.batch) * static_cast<unsigned>(HU);
   const unsigned nchunks = (units + kReadChunk - 1) / kReadChunk;
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
@@ -300,16 +303,16 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     // units.  S0 is final by now (the precompute waited for the flush before
     // it let this kernel launch) and needs only the slot id, an input of the call.
     unsigned u = blockIdx.x * kReadChunk, cend = min(u + kReadChunk, units);
-    int b = static_cast<int>(u / H), h = static_cast<int>(u % H);
+    int b = static_cast<int>(u / HU), h = static_cast<int>(u % HU) * HPU;  // h: the unit's first head
     const int npre = static_cast<int>(cend - u) < ns ? static_cast<int>(cend - u) : ns;
     uint32_t pre = 0u;
-    for (int i = 0, pb = b, phh = h; i < npre; ++i, phh = phh + 1 == H ? 0 : phh + 1, pb += phh == 0 ? 1 : 0) {
+    for (int i = 0, pb = b, phh = h; i < npre; ++i, phh = phh + HPU == H ? 0 : phh + HPU, pb += phh == 0 ? 1 : 0) {
       const int s = a.slot_idx[pb];
       if (s >= 1 && s < c.S) {
         uint8_t* sb = smem + lay.stages_off + i * lay.stage_bytes;
         mbar_expect_tx(&full[i], lay.s0_bytes);
 #pragma unroll
-        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), phh * kDim, s, &full[i]);
+        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * kBox, &s0map, bx * (128 / esz), phh * kDim, s, &full[i]);
         pre |= 1u << i;
       }
     }
@@ -331,8 +334,8 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         if (ch >= nchunks) break;
         u = ch * kReadChunk;
         cend = min(u + kReadChunk, units);
-        b = static_cast<int>(u / H);
-        h = static_cast<int>(u % H);
+        b = static_cast<int>(u / HU);
+        h = static_cast<int>(u % HU) * HPU;
         g = h / c.hpg;
         hh = h % c.hpg;
         next = atomicAdd(a.rwork, 1u);
@@ -361,27 +364,28 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
         const bool have_s0 = i < npre && ((pre >> i) & 1u);
         const uint32_t bytes =
-            (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u : 0u) + (newc ? 8u * kDstate * 2 : 0u) + lay.r_bytes;
+            (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u * HPU : 0u) + (newc ? 8u * kDstate * 2 : 0u) + lay.r_bytes;
         mbar_arrive_expect_tx(&full[st], bytes);
         if (!have_s0) {
 #pragma unroll
-          for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
+          for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * kBox, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
         }
         if (k8bit)
-          bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256, &full[st]);
+          bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256 * HPU,
+                   &full[st]);
         if (newc) bulk_g2s(sb + lay.c_off, a.cf + static_cast<long long>(bg) * 8 * kDstate, 8 * kDstate * 2, &full[st]);
-        bulk_g2s(sb + lay.r_off, a.rblk + static_cast<long long>(u) * rstride, lay.r_bytes, &full[st]);
+        bulk_g2s(sb + lay.r_off, a.rblk + static_cast<long long>(u) * HPU * rstride, lay.r_bytes, &full[st]);
       } else {
         mbar_arrive(&full[st]);
       }
       issued = i + 1;
       ++u;
-      if (++h == H) {
+      if ((h += HPU) == H) {
         h = 0;
         ++b;
         g = 0;
         hh = 0;
-      } else if (++hh == c.hpg) {
+      } else if ((hh += HPU) == c.hpg) {
         hh = 0;
         ++g;
       }
@@ -426,9 +430,9 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
     if (!(m.flags & 1)) {
       // inactive or rejected row: zero outputs, no cache update
-      for (int idx = lane; idx < m.Tb * 4; idx += 32) {
-        const int t = idx >> 2, q = idx & 3;
-        *reinterpret_cast<uint32_t*>(a.out + (static_cast<long long>(m.tok0 + t) * H + m.h) * kDim + 8 * warp +
+      for (int idx = lane; idx < m.Tb * 4 * HPU; idx += 32) {
+        const int t = idx / (4 * HPU), j = (idx >> 2) % HPU, q = idx & 3;
+        *reinterpret_cast<uint32_t*>(a.out + (static_cast<long long>(m.tok0 + t) * H + m.h + j) * kDim + 8 * warp +
                                      2 * q) = 0u;
       }
       __syncwarp();
@@ -436,24 +440,32 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       continue;
     }
     if (m.flags & 2) load_c_frags(reinterpret_cast<const uint16_t*>(sb + lay.c_off), g, cq, af);
-    float acc[4];
-    s0_dot_c<DT>(sb, af, d, cq, acc);
-    const float* rb = reinterpret_cast<const float*>(sb + lay.r_off);
-    const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kRStride + dout) : make_float2(0.0f, 0.0f);
-    const float dec = g < TP ? rb[TP * kRStride + g] : 0.0f;
-    float sc0 = 1.0f, sc1 = 1.0f;
-    if constexpr (k8bit) {
-      const float2 scv = *reinterpret_cast<const float2*>(sb + lay.scale_off + dout * 4);
-      sc0 = scv.x;
-      sc1 = scv.y;
+    float y[HPU][2];
+#pragma unroll
+    for (int j = 0; j < HPU; ++j) {  // head m.h + j: rows 64 j .. of the stage's boxes
+      float acc[4];
+      s0_dot_c<DT, kBox>(sb + j * 8192, af, d, cq, acc);
+      const float* rb = reinterpret_cast<const float*>(sb + lay.r_off) + j * (TP * kRStride + TP);
+      const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kRStride + dout) : make_float2(0.0f, 0.0f);
+      const float dec = g < TP ? rb[TP * kRStride + g] : 0.0f;
+      float sc0 = 1.0f, sc1 = 1.0f;
+      if constexpr (k8bit) {
+        const float2 scv = *reinterpret_cast<const float2*>(sb + lay.scale_off + j * 256 + dout * 4);
+        sc0 = scv.x;
+        sc1 = scv.y;
+      }
+      y[j][0] = fmaf(dec * sc0, acc[0], rv.x);
+      y[j][1] = fmaf(dec * sc1, acc[1], rv.y);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
-    const float y0 = fmaf(dec * sc0, acc[0], rv.x);
-    const float y1 = fmaf(dec * sc1, acc[1], rv.y);
     if (g < m.Tb) {
-      const __nv_bfloat162 yv = __floats2bfloat162_rn(y0, y1);
-      *reinterpret_cast<__nv_bfloat162*>(a.out + (static_cast<long long>(m.tok0 + g) * H + m.h) * kDim + dout) = yv;
+#pragma unroll
+      for (int j = 0; j < HPU; ++j) {
+        const __nv_bfloat162 yv = __floats2bfloat162_rn(y[j][0], y[j][1]);
+        *reinterpret_cast<__nv_bfloat162*>(a.out + (static_cast<long long>(m.tok0 + g) * H + m.h + j) * kDim + dout) =
+            yv;
+      }
     }
   }
 }
@@ -475,46 +487,53 @@ int launch_precompute(const StepArgs& a, void* stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int DT, int TP>
+template <int DT, int TP, int HPU>
 static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 8
   int ns = 8, ctas = 2;
   for (; ns >= 3; --ns)
-    if (read_layout(DT, TP, ns).total <= 113 * 1024) break;
+    if (read_layout(DT, TP, ns, HPU).total <= 113 * 1024) break;
   if (ns < 3) {
     ctas = 1;
     for (ns = 8; ns > 2; --ns)
-      if (read_layout(DT, TP, ns).total <= 225 * 1024) break;
+      if (read_layout(DT, TP, ns, HPU).total <= 225 * 1024) break;
   }
-  const ReadLayout lay = read_layout(DT, TP, ns);
+  const ReadLayout lay = read_layout(DT, TP, ns, HPU);
   CUtensorMap map;
-  if (!encode_state_map(a.c, &map)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
+  if (!encode_state_map(a.c, &map, HPU)) return cudaErrorInvalidValue;
+  auto kern = readout_kernel<DT, TP, HPU>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
-  e = cudaFuncSetAttribute(readout_kernel<DT, TP>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                           cudaSharedmemCarveoutMaxShared);
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
   int occ = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, readout_kernel<DT, TP>, kThreads, lay.total);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, lay.total);
   if (e != cudaSuccess) return e;
   if (occ < 1) occ = 1;
   if (occ > ctas) occ = ctas;
-  const long long chunks = (static_cast<long long>(a.batch) * a.c.H + kReadChunk - 1) / kReadChunk;
+  const long long chunks = (static_cast<long long>(a.batch) * (a.c.H / HPU) + kReadChunk - 1) / kReadChunk;
   const long long cap = static_cast<long long>(num_sms) * occ;
   const int grid = static_cast<int>(chunks < cap ? chunks : cap);  // every CTA has a first chunk
-  e = launch_pdl(readout_kernel<DT, TP>, dim3(grid), dim3(kThreads), lay.total, st, map, a, ns);
+  e = launch_pdl(kern, dim3(grid), dim3(kThreads), lay.total, st, map, a, ns);
   return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <int DT>
+static int launch_readout_dt(const StepArgs& a, int num_sms, cudaStream_t st) {
+  constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
+  const bool pair = k8bit && a.c.hpg % 2 == 0;
+  if (a.TP == 4) return pair ? launch_readout_t<DT, 4, 2>(a, num_sms, st) : launch_readout_t<DT, 4, 1>(a, num_sms, st);
+  return pair ? launch_readout_t<DT, 8, 2>(a, num_sms, st) : launch_readout_t<DT, 8, 1>(a, num_sms, st);
 }
 
 int launch_readout(const StepArgs& a, int num_sms, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  const bool t4 = a.TP == 4;
   switch (a.c.dtype) {
-    case RSSM_F32: return t4 ? launch_readout_t<RSSM_F32, 4>(a, num_sms, st) : launch_readout_t<RSSM_F32, 8>(a, num_sms, st);
-    case RSSM_BF16: return t4 ? launch_readout_t<RSSM_BF16, 4>(a, num_sms, st) : launch_readout_t<RSSM_BF16, 8>(a, num_sms, st);
-    case RSSM_F16: return t4 ? launch_readout_t<RSSM_F16, 4>(a, num_sms, st) : launch_readout_t<RSSM_F16, 8>(a, num_sms, st);
-    case RSSM_I8: return t4 ? launch_readout_t<RSSM_I8, 4>(a, num_sms, st) : launch_readout_t<RSSM_I8, 8>(a, num_sms, st);
-    default: return t4 ? launch_readout_t<RSSM_E4M3, 4>(a, num_sms, st) : launch_readout_t<RSSM_E4M3, 8>(a, num_sms, st);
+    case RSSM_F32: return launch_readout_dt<RSSM_F32>(a, num_sms, st);
+    case RSSM_BF16: return launch_readout_dt<RSSM_BF16>(a, num_sms, st);
+    case RSSM_F16: return launch_readout_dt<RSSM_F16>(a, num_sms, st);
+    case RSSM_I8: return launch_readout_dt<RSSM_I8>(a, num_sms, st);
+    default: return launch_readout_dt<RSSM_E4M3>(a, num_sms, st);
   }
 }
 

@@ -98,6 +98,18 @@ def test_eight_bit_config_reduced(orc, dtype, rounding):
     assert pair.exact_state_steps == wl.steps
 
 
+@pytest.mark.parametrize("dtype", [W.I8, W.E4M3])
+def test_eight_bit_odd_heads_per_group(orc, dtype):
+    """8-bit states with 3 heads per group: the readout takes one head per unit
+    (with an even count it takes two)."""
+    wl = W.Workload(name="edge", num_slots=9, nheads=12, ngroups=4, max_window=16, npredicted=4, state_dtype=dtype,
+                    rounding=W.STOCHASTIC, sr_seed=5, batch=6, T=4, steps=10, pad_row=True, ring_start_random=True,
+                    prefill_live=10, accept="all", config_id=9)
+    pair = run_pair(orc, wl)
+    assert pair.oc.flush_epoch.max() >= 1
+    assert pair.exact_state_steps == wl.steps
+
+
 def test_mamba2_decode_reduced(orc):
     wl = W.config("mamba2_decode", batch=12, steps=20)
     pair = run_pair(orc, wl)
