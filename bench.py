@@ -67,6 +67,9 @@ def workload(args):
     return W.config(args.config, **kw)
 
 
+L2_BYTES = 129e6  # GB300 L2 capacity
+
+
 def profiled_traffic(kernel, workload_name):
     """DRAM bytes per launch (dram__bytes_read + dram__bytes_write) from the
     committed ncu summary of `kernel` on this workload, if the kernel's sources
@@ -349,35 +352,46 @@ def run_gpu(args, rank, ws, local):
         if cu is not None:
             cu.copy_(src["cu"], non_blocking=non_blocking)
 
-    # the four launch groups of one step, each captured once as a CUDA graph
-    def g_flush():
-        api.rssm_flush(gc, gA, gids, pnat, wl.T, scr_flush, cu_seqlens=cu, force=force, seed=wl.sr_seed)
-
-    def g_pre():
-        api.rssm_step_precompute(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
-                                 scr_step, cu_seqlens=cu)
-
-    def g_read():
-        api.rssm_step_readout(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
-                              scr_step, cu_seqlens=cu)
-
-    def g_acc():
-        api.rssm_accept(gc, gids, pnat, buf["acc"], wl.T, cu_seqlens=cu)
-
-    def g_fpre():
-        api.rssm_flush_step_classify(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
-                                       scr_step, cu_seqlens=cu, force=force, seed=wl.sr_seed)
-
-    def g_fread():
-        api.rssm_flush_step_main(gc, buf["x"], buf["dt"], gA, buf["B"], buf["C"], gD, gb, gids, pnat, wl.T, out,
-                                    scr_step, cu_seqlens=cu, force=force, seed=wl.sr_seed)
-
     fused = args.path == "fused"
+
+    def step_groups(bv, yv):
+        """The launch groups of one step on input buffers `bv` and output `yv`."""
+        cuv = bv["cu"]
+
+        def g_flush():
+            api.rssm_flush(gc, gA, gids, pnat, wl.T, scr_flush, cu_seqlens=cuv, force=force, seed=wl.sr_seed)
+
+        def g_pre():
+            api.rssm_step_precompute(gc, bv["x"], bv["dt"], gA, bv["B"], bv["C"], gD, gb, gids, pnat, wl.T, yv,
+                                     scr_step, cu_seqlens=cuv)
+
+        def g_read():
+            api.rssm_step_readout(gc, bv["x"], bv["dt"], gA, bv["B"], bv["C"], gD, gb, gids, pnat, wl.T, yv,
+                                  scr_step, cu_seqlens=cuv)
+
+        def g_acc():
+            api.rssm_accept(gc, gids, pnat, bv["acc"], wl.T, cu_seqlens=cuv)
+
+        def g_fpre():
+            api.rssm_flush_step_classify(gc, bv["x"], bv["dt"], gA, bv["B"], bv["C"], gD, gb, gids, pnat, wl.T, yv,
+                                         scr_step, cu_seqlens=cuv, force=force, seed=wl.sr_seed)
+
+        def g_fread():
+            api.rssm_flush_step_main(gc, bv["x"], bv["dt"], gA, bv["B"], bv["C"], gD, gb, gids, pnat, wl.T, yv,
+                                     scr_step, cu_seqlens=cuv, force=force, seed=wl.sr_seed)
+
+        return [g_fpre, g_fread, g_acc] if fused else [g_flush, g_pre, g_read, g_acc]
+
     # the launch groups of one step; `rg` is the dominant kernel's group
+    groups = step_groups(buf, out)
     if fused:
-        groups, names, rg = [g_fpre, g_fread, g_acc], ["classify", "step_main", "accept"], 1
+        names, rg = ["classify", "step_main", "accept"], 1
     else:
-        groups, names, rg = [g_flush, g_pre, g_read, g_acc], ["flush", "precompute", "readout", "accept"], 2
+        names, rg = ["flush", "precompute", "readout", "accept"], 2
+    # a second set of device inputs and output: the end-to-end leg alternates
+    # between the two so one step's copies overlap the neighbouring steps' work
+    dbuf_b = torch.zeros(total, dtype=torch.uint8, device=dev) if not args.no_e2e else None
+    out_b = torch.zeros((max_tok, wl.nheads, 64), dtype=torch.int16, device=dev) if not args.no_e2e else None
     # one eager step (sets kernel attributes), then capture on a snapshot of the
     # cache that is restored afterwards so capture has no side effects
     load_inputs(dev_inp[0])
@@ -398,6 +412,12 @@ def run_gpu(args, rank, ws, local):
         with torch.cuda.graph(g_step, stream=side, capture_error_mode="thread_local"):
             for f in groups:
                 f()
+        g_b = None
+        if dbuf_b is not None:
+            g_b = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_b, stream=side, capture_error_mode="thread_local"):
+                for f in step_groups(views(dbuf_b), out_b):
+                    f()
     torch.cuda.synchronize()
     # restart the workload from its initial state
     for i in range(0, active.size, chunk):
@@ -418,6 +438,12 @@ def run_gpu(args, rank, ws, local):
     def step_units():
         rr = scr_step[256: 256 + ids.size * 32].view(torch.int32).view(ids.size, 8).cpu().numpy()
         return rr, int((((rr[:, 5] & 1) == 1) & (rr[:, 3] > 0)).sum()) * wl.nheads
+
+    def host_units(k):
+        """(slot, head) updates of step k from its inputs: active rows with at
+        least one token (what the step's row records count)."""
+        tb = np.diff(host[k].cu_seqlens) if host[k].cu_seqlens is not None else np.full(ids.size, wl.T)
+        return int(((ids > 0) & (tb > 0)).sum()) * wl.nheads
 
     for k in range(args.warmup):
         load_inputs(dev_inp[k])
@@ -440,7 +466,10 @@ def run_gpu(args, rank, ws, local):
         e1.record(stream)
         torch.cuda.synchronize()
         step_ms.append(e0.elapsed_time(e1))
-        units += step_units()[1]
+        u_dev = step_units()[1]
+        if u_dev != host_units(k):
+            raise RuntimeError(f"step {k}: {u_dev} updates on the device, {host_units(k)} from the inputs")
+        units += u_dev
     clk = clocks.stop()
     barrier(ws)
     torch.cuda.synchronize()
@@ -485,54 +514,101 @@ def run_gpu(args, rank, ws, local):
     units_all = sum_over_ranks(units, ws, dev)
     value = units_all / (t_max / 1e3)
 
-    # end to end through the public calls: the step's inputs come from pinned
-    # host memory and y goes back to it, inside the timed region
+    # end to end through the public calls: every step's inputs are copied in
+    # from pinned host memory and its y is copied back, inside the timed region
     e2e = None
     if not args.no_e2e:
-        # one set of pinned staging buffers, reused every step (as a serving
-        # engine does); the host fills it with the step's inputs before the
-        # timed region, which then holds H2D copy -> step -> D2H copy of y
-        # one pinned staging buffer laid out like the device inputs, reused
-        # every step (as a serving engine does): the host fills it before the
-        # timed region, which holds one H2D copy -> step -> D2H copy of y
-        hbuf = torch.zeros(total, dtype=torch.uint8).pin_memory()
-        stg = views(hbuf)
-        yh = torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16).pin_memory()
-        e2e_ms, e2e_units, h2d, d2h = [], 0, 0, 0
-        parts = {"h2d": [], "step": [], "d2h": []}
+        n_e2e = nsteps - args.warmup
+        # pinned staging laid out like the device inputs, one per step, filled
+        # before the timed region (the host's part of a serving loop)
+        stage = [torch.empty(total, dtype=torch.uint8, pin_memory=True) for _ in range(n_e2e)]
         for k in range(args.warmup, nsteps):
-            hi = hin[k]
+            hv, hi = views(stage[k - args.warmup]), hin[k]
             n = hi["ntok"]
             for key in ("x", "dt", "B", "C"):
-                stg[key][:n].copy_(hi[key])
-            stg["acc"].copy_(hi["acc"])
+                hv[key][:n].copy_(hi[key])
+            hv["acc"].copy_(hi["acc"])
             if cu is not None:
-                stg["cu"].copy_(hi["cu"])
+                hv["cu"].copy_(hi["cu"])
+        yh = [torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16, pin_memory=True) for _ in range(2)]
+        e2e_units = sum(host_units(k) for k in range(args.warmup, nsteps))
+        d2h_sum = sum(hin[k]["ntok"] for k in range(args.warmup, nsteps)) * wl.nheads * 64 * 2
+
+        # (a) serial: H2D copy -> step -> D2H copy of y, one step at a time
+        ser_ms = []
+        parts = {"h2d": [], "step": [], "d2h": []}
+        for k in range(args.warmup, nsteps):
+            n = hin[k]["ntok"]
             cold_l2()
             e0 = ev()
             e0.record(stream)
-            dbuf.copy_(hbuf, non_blocking=True)
+            dbuf.copy_(stage[k - args.warmup], non_blocking=True)
             e_h = ev()
             e_h.record(stream)
             g_step.replay()
             e_g = ev()
             e_g.record(stream)
-            yh[:n].copy_(out[:n], non_blocking=True)
+            yh[0][:n].copy_(out[:n], non_blocking=True)
             e1 = ev()
             e1.record(stream)
             torch.cuda.synchronize()
-            e2e_ms.append(e0.elapsed_time(e1))
+            ser_ms.append(e0.elapsed_time(e1))
             parts["h2d"].append(e0.elapsed_time(e_h))
             parts["step"].append(e_h.elapsed_time(e_g))
             parts["d2h"].append(e_g.elapsed_time(e1))
-            e2e_units += step_units()[1]
-            h2d = total
-            d2h = n * wl.nheads * 64 * 2
-        t_e2e = max_over_ranks(sum(e2e_ms), ws, dev)
+        t_ser = max_over_ranks(sum(ser_ms), ws, dev)
+        serial = {"value": sum_over_ranks(e2e_units, ws, dev) / (t_ser / 1e3), "unit": UNIT,
+                  "ms_per_step": t_ser / n_e2e,
+                  "breakdown_us": {key: 1e3 * statistics.median(v) for key, v in parts.items()},
+                  "l2": "cleared before each step (untimed)"}
+
+        # (b) pipelined: the steps back to back on the compute stream, alternating
+        # between two device input/output sets; step k's H2D copy (copy stream)
+        # overlaps step k-1's kernels and its D2H copy (a third stream) step k+1's
+        dbufs, outs, gs = [dbuf, dbuf_b], [out, out_b], [g_step, g_b]
+        s_h2d, s_d2h = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        sev = lambda: torch.cuda.Event()  # noqa: E731
+        h_done, c_done, d_done = [sev() for _ in range(n_e2e)], [sev() for _ in range(n_e2e)], \
+            [sev() for _ in range(n_e2e)]
+        torch.cuda.synchronize()
+        barrier(ws)
+        torch.cuda.synchronize()
+        e_start, e_end = ev(), ev()
+        e_start.record(s_h2d)
+        for i in range(n_e2e):
+            k, par = args.warmup + i, i % 2
+            n = hin[k]["ntok"]
+            with torch.cuda.stream(s_h2d):
+                if i >= 2:
+                    s_h2d.wait_event(c_done[i - 2])  # step i-2 is done with this input set
+                dbufs[par].copy_(stage[i], non_blocking=True)
+                h_done[i].record(s_h2d)
+            with torch.cuda.stream(stream):
+                stream.wait_event(h_done[i])
+                if i >= 2:
+                    stream.wait_event(d_done[i - 2])  # y of step i-2 has left this output
+                gs[par].replay()
+                c_done[i].record(stream)
+            with torch.cuda.stream(s_d2h):
+                s_d2h.wait_event(c_done[i])
+                yh[par][:n].copy_(outs[par][:n], non_blocking=True)
+                d_done[i].record(s_d2h)
+        e_end.record(s_d2h)
+        torch.cuda.synchronize()
+        t_e2e = max_over_ranks(e_start.elapsed_time(e_end), ws, dev)
         e2e = {"value": sum_over_ranks(e2e_units, ws, dev) / (t_e2e / 1e3), "unit": UNIT,
-               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "breakdown_us": {key: 1e3 * statistics.median(v) for key, v in parts.items()},
-               "staging": "one pinned host buffer with every per-step input, reused every step; one H2D copy"}
+               "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h_sum // n_e2e),
+               "ms_per_step": t_e2e / n_e2e,
+               "mode": "rssm_flush -> rssm_step -> rssm_accept on a compute stream, every step's inputs copied in "
+                       "from pinned host memory (one H2D copy per step) and its y copied back (one D2H copy), "
+                       "copies on two other streams overlapping the neighbouring steps' kernels; two device "
+                       "input/output sets alternate",
+               "l2": ("not cleared (back-to-back steps); " +
+                      (f"each step's readout alone streams {read_bytes / args.steps / 1e6:.0f} MB, more than the "
+                       "129 MB L2" if read_bytes / args.steps > L2_BYTES else
+                       f"the step's working set ({read_bytes / args.steps / 1e6:.0f} MB read by the readout) fits in "
+                       "the L2, so this leg runs warm")),
+               "serial": serial}
 
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (sum(read_ms) / 1e3) / 1e9

@@ -143,6 +143,10 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
     const int f = b < a.batch ? row_flag(a, b, blockIdx.x == 0).flag : 0;
     count += __syncthreads_count(f);
   }
+  if (count == 0) {  // nothing to fold or book (every CTA sees the same count)
+    if (blockIdx.x == 0 && tid == 0) *a.count = 0;
+    return;
+  }
   const long long units = static_cast<long long>(count) * H;
   const long long per = units / gridDim.x, rem = units % gridDim.x;
   const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
