@@ -250,6 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
     const float dtj = lane < p ? reinterpret_cast<const float*>(sb + lay.dt_off)[lane] : 0.0f;
     const float aj = lane < p ? __fmul_rn(hA, dtj) : 0.0f;
     float cj = 0.0f;
+#pragma unroll 4
     for (int k = 0; k < p; ++k) {
       const float ak = __shfl_sync(0xffffffffu, aj, k);
       if (lane >= k) cj = __fadd_rn(cj, ak);
@@ -293,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
     // acc[d][n] = fma(u_j[d], B_j[n], acc), j ascending, u_j[d] = w_j x_j[d]
     const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
     const uint16_t* bs = reinterpret_cast<const uint16_t*>(sb + lay.b_off);
+#pragma unroll 4
     for (int j = 0; j < p; ++j) {
       const float w = __shfl_sync(0xffffffffu, wj, j);
       const uint2 xw = *reinterpret_cast<const uint2*>(xs + j * kDim + r0);

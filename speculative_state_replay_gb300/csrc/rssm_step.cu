@@ -275,12 +275,22 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   constexpr int kBox = 8192 * HPU;  // bytes of one column box of S0 (64*HPU rows x 128 bytes)
   const int H = c.H, HU = H / HPU;
 
-  // Units are taken in chunks of kReadChunk consecutive (row, head) pairs:
-  // each CTA's first chunk is chunk blockIdx.x (its S0 can be requested
-  // before the precompute has finished); later chunks come from a counter the
-  // precompute zeroes, so CTAs that stream faster take more of them.
+  // Units are taken in chunks of consecutive (row, head) pairs: each CTA's
+  // first chunk is chunk blockIdx.x (its S0 can be requested before the
+  // precompute has finished); later chunks come from a counter the
+  // precompute zeroes, so CTAs that stream faster take more of them.  Chunks
+  // hold kReadChunk units until about two units per CTA are left, then one
+  // (guided sizes: the CTAs finish within about one unit of each other).
   const unsigned units = static_cast<unsigned>(a.batch) * static_cast<unsigned>(HU);
-  const unsigned nchunks = (units + kReadChunk - 1) / kReadChunk;
+  const unsigned tail = min(units, 2u * gridDim.x);
+  const unsigned nbig = (units - tail) / kReadChunk;
+  const unsigned big_end = nbig * kReadChunk;
+  const unsigned nchunks = nbig + (units - big_end);
+  // first unit of chunk ch (< nchunks) and the end of its range
+  auto chunk_range = [&](unsigned ch, unsigned& first, unsigned& last) {
+    first = ch < nbig ? ch * kReadChunk : big_end + (ch - nbig);
+    last = ch < nbig ? first + kReadChunk : first + 1u;
+  };
 
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 8;
@@ -302,7 +312,8 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     // Before waiting for the precompute: request S0 of the first chunk's
     // units.  S0 is final by now (the precompute waited for the flush before
     // it let this kernel launch) and needs only the slot id, an input of the call.
-    unsigned u = blockIdx.x * kReadChunk, cend = min(u + kReadChunk, units);
+    unsigned u, cend;
+    chunk_range(blockIdx.x, u, cend);
     int b = static_cast<int>(u / HU), h = static_cast<int>(u % HU) * HPU;  // h: the unit's first head
     const int npre = static_cast<int>(cend - u) < ns ? static_cast<int>(cend - u) : ns;
     uint32_t pre = 0u;
@@ -332,8 +343,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       if (u >= cend) {  // next chunk
         const unsigned ch = gridDim.x + next;
         if (ch >= nchunks) break;
-        u = ch * kReadChunk;
-        cend = min(u + kReadChunk, units);
+        chunk_range(ch, u, cend);
         b = static_cast<int>(u / HU);
         h = static_cast<int>(u % HU) * HPU;
         g = h / c.hpg;
