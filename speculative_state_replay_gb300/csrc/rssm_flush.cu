@@ -9,8 +9,8 @@
 //   and folds its range of (flagged row, head) units:
 //       S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
 //   in fp32, canonical order, then rounds to the state format; the CTA that
-//   finishes last advances the ring bookkeeping (ring_start += p mod L,
-//   pnat = 0, epoch += 1).
+//   finishes classifying last advances the ring bookkeeping (ring_start += p
+//   mod L, pnat = 0, epoch += 1) while the folds run.
 #include <cuda_runtime.h>
 
 #include "rssm_device.cuh"
@@ -109,8 +109,9 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int 
 // kernel.  Every CTA classifies all rows (two passes over slot_idx, pnat and
 // the sequence bounds) and keeps the records of the flushed rows its range of
 // (flushed row, head) units covers; the producer and consumer warps then fold
-// those units; the CTA that finishes last (a self-resetting ticket) writes the
-// bookkeeping, after every CTA has read the values it replaces.
+// those units.  The bookkeeping is written by the CTA that takes the last ticket
+// once it has classified (a self-resetting ticket), i.e. after every CTA has
+// read the values it replaces; nothing in the kernel reads them afterwards.
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns, int maxrows) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -136,17 +137,23 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
   }
   pdl_wait();  // pnat as the previous call left it
   pdl_trigger();
-  // pass 1: the number of flushed rows (CTA 0 reports bad rows)
+  // pass 1: the number of flushed rows (CTA 0 reports bad rows); the flagged
+  // rows' ring start and epoch are prefetched for pass 2
   int count = 0;
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
     const int b = b0 + tid;
-    const int f = b < a.batch ? row_flag(a, b, blockIdx.x == 0).flag : 0;
-    count += __syncthreads_count(f);
+    const RowFlag f = b < a.batch ? row_flag(a, b, blockIdx.x == 0) : RowFlag{0, 0, 0};
+    if (f.flag) {
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(c.ring_start + f.s));
+      asm volatile("prefetch.global.L1 [%0];" ::"l"(c.epoch + f.s));
+    }
+    count += __syncthreads_count(f.flag);
   }
   if (count == 0) {  // nothing to fold or book (every CTA sees the same count)
     if (blockIdx.x == 0 && tid == 0) *a.count = 0;
     return;
   }
+  if (blockIdx.x == 0 && tid == 0) *a.count = count;
   const long long units = static_cast<long long>(count) * H;
   const long long per = units / gridDim.x, rem = units % gridDim.x;
   const long long u0 = blockIdx.x * per + min(static_cast<long long>(blockIdx.x), rem);
@@ -161,12 +168,33 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
       const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0};
       int tot = 0;
       const int pos = base + block_excl_scan(f.flag, wsum, tot);
-      if (f.flag && pos >= li_first && pos <= li_last)
-        rows_s[pos - li_first] = FlushRec{b, f.s, c.ring_start[f.s], f.p, c.epoch[f.s] + 1u, {0, 0, 0}};
+      if (f.flag && pos >= li_first && pos <= li_last) {
+        const FlushRec rec{b, f.s, c.ring_start[f.s], f.p, c.epoch[f.s] + 1u, {0, 0, 0}};
+        rows_s[pos - li_first] = rec;
+        // the flush record of the call: by the CTA that folds the row's head 0
+        if (static_cast<long long>(pos) * H >= u0) a.recs[pos] = rec;
+      }
       base += tot;
     }
   }
-  __syncthreads();  // barriers initialised, records in place
+  __syncthreads();  // barriers initialised, records in place, this CTA's reads of pnat, ring_start, epoch done
+  // The bookkeeping may replace those values once every CTA has read them: the
+  // CTA that takes the last ticket writes it (self-resetting ticket), from the
+  // flush records, while its producer issues the first copies.
+  if (tid == 0) {
+    __threadfence();  // this CTA's records are visible before its ticket
+    s_last = atomicInc(a.ticket, gridDim.x - 1) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (s_last && tid < kConsumerThreads) {
+    __threadfence();
+    for (int k = tid; k < count; k += kConsumerThreads) {
+      const FlushRec rec = a.recs[k];
+      c.ring_start[rec.s] = rec.r + rec.p >= L ? rec.r + rec.p - L : rec.r + rec.p;  // (r + p) mod L
+      a.pnat[rec.b] = 0;
+      c.epoch[rec.s] = rec.epoch;
+    }
+  }
 
   if (nu > 0 && warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
@@ -327,33 +355,6 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
   }
   }
 
-  // ---------------- the flush's bookkeeping, by the last CTA to finish ----------------
-  __syncthreads();
-  if (tid == 0) {
-    __threadfence();  // this CTA's reads of pnat, ring_start and epochs are done
-    s_last = atomicInc(a.ticket, gridDim.x - 1) == gridDim.x - 1;  // wraps back to 0
-  }
-  __syncthreads();
-  if (s_last) {
-    __threadfence();
-    int base = 0;
-    for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
-      const int b = b0 + tid;
-      const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0};
-      int tot = 0;
-      const int pos = base + block_excl_scan(f.flag, wsum, tot);
-      if (f.flag) {
-        const int r = c.ring_start[f.s];
-        const unsigned e = c.epoch[f.s] + 1u;
-        a.recs[pos] = FlushRec{b, f.s, r, f.p, e, {0, 0, 0}};
-        c.ring_start[f.s] = r + f.p >= L ? r + f.p - L : r + f.p;  // (r + p) mod L
-        a.pnat[b] = 0;
-        c.epoch[f.s] = e;
-      }
-      base += tot;
-    }
-    if (tid == 0) *a.count = base;
-  }
 }
 
 // ---------------------------------------------------------------------------
