@@ -450,13 +450,13 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
           const float v0 = __fmul_rn(acc[i][q], inv), v1 = __fmul_rn(acc[i][q + 1], inv);
           uint32_t pair;
           if constexpr (DT == RSSM_I8) {
-            // |v| <= amax / scale < 127.5, so round-to-nearest-even alone stays in -127..127
-            int i0, i1;
-            asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i0) : "f"(v0));
-            asm("cvt.rni.s32.f32 %0, %1;" : "=r"(i1) : "f"(v1));
-            i0 = max(-127, min(127, i0));
-            i1 = max(-127, min(127, i1));
-            pair = (static_cast<uint32_t>(i0) & 0xffu) | ((static_cast<uint32_t>(i1) & 0xffu) << 8);
+            // round-to-nearest-even onto -127..127 without a conversion
+            // instruction: for |v| <= 127, v + 1.5 * 2^23 lies in [2^23, 2^24)
+            // where the fp32 grid is the integers, so the addition itself
+            // rounds (to even) and the low byte of the sum's bits is the code
+            const float t0 = __fadd_rn(fminf(fmaxf(v0, -127.0f), 127.0f), 12582912.0f);
+            const float t1 = __fadd_rn(fminf(fmaxf(v1, -127.0f), 127.0f), 12582912.0f);
+            pair = __byte_perm(__float_as_uint(t0), __float_as_uint(t1), 0x0040u) & 0xffffu;
           } else {
             pair = static_cast<uint32_t>(__nv_cvt_float2_to_fp8x2(make_float2(v0, v1), __NV_SATFINITE, __NV_E4M3));
           }

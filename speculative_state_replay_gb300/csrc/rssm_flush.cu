@@ -310,8 +310,16 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
         const float sc = reinterpret_cast<const float*>(sb + lay.scale_off)[row];
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
-          const uint32_t byte = ((e < 4 ? q.x : q.y) >> (8 * (e & 3))) & 0xffu;
-          const float code = DT == RSSM_I8 ? static_cast<float>(static_cast<int8_t>(byte)) : e4m3_to_f32(byte);
+          const uint32_t w = e < 4 ? q.x : q.y;
+          float code;
+          if constexpr (DT == RSSM_I8) {
+            // code q as fp32 without a conversion instruction:
+            // (2^23 + (q + 128)) - (2^23 + 128), every step exact
+            const uint32_t bits = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | (e & 3));
+            code = __fsub_rn(__uint_as_float(bits), 8388736.0f);
+          } else {
+            code = e4m3_to_f32(static_cast<uint8_t>((w >> (8 * (e & 3))) & 0xffu));
+          }
           v[e] = __fmul_rn(code, sc);
         }
       }
