@@ -29,10 +29,11 @@ struct RowFlag {
 __device__ __forceinline__ RowFlag row_flag(const FlushArgs& a, int b, bool errors) {
   const Cache& c = a.c;
   RowFlag f = {0, 0, 0};
+  // the row's loads are independent: issue them together (one round trip)
   const int s = a.slot_idx[b];
+  const int p = a.pnat[b];
+  const int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
   if (s >= 1 && s < c.S) {
-    const int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
-    const int p = a.pnat[b];
     if (Tb < 0 || Tb > a.T) {
       if (errors) set_error(c.err, RSSM_ERRBIT_SEQLEN);
     } else if (p < 0 || p > c.L) {
@@ -422,19 +423,20 @@ __global__ void __launch_bounds__(256) accept_kernel(Cache c, const int* slot_id
   pdl_wait();
   pdl_trigger();
   if (b >= batch) return;
+  // the row's loads are independent: issue them together (one round trip)
   const int s = slot_idx[b];
-  if (s < 1 || s >= c.S) return;
   const int Tb = cu ? cu[b + 1] - cu[b] : T;
+  const int acc = accepted[b];
+  const int p = pnat[b];
+  if (s < 1 || s >= c.S) return;
   if (Tb < 0 || Tb > T) {
     set_error(c.err, RSSM_ERRBIT_SEQLEN);
     return;
   }
-  const int acc = accepted[b];
   if (acc < 0 || acc > Tb) {
     set_error(c.err, RSSM_ERRBIT_ACCEPT);
     return;
   }
-  const int p = pnat[b];
   if (p < 0 || p + acc > c.L) {
     set_error(c.err, RSSM_ERRBIT_PNAT);
     return;
