@@ -121,6 +121,16 @@ def test_fused_appends_overlapping_the_folded_prefix(orc, dtype):
     assert pair2.oc.flush_epoch.max() >= 4
 
 
+def test_fused_batch_beyond_one_cta(orc):
+    """640 varlen rows with a padding row, random ring starts and flushes in
+    the first steps, through rssm_flush_step."""
+    wl = W.Workload(name="edge", num_slots=700, nheads=4, ngroups=2, max_window=16, npredicted=4,
+                    state_dtype=W.BF16, batch=640, T=4, steps=6, varlen=True, pad_row=True,
+                    ring_start_random=True, prefill_live=14, config_id=9)
+    pair = run_fused(orc, wl, force_every=3)
+    assert pair.oc.flush_epoch.max() >= 2
+
+
 def test_fused_matches_two_calls_bit_for_bit():
     """rssm_flush_step and rssm_flush + rssm_step on twin GPU caches: the same
     checkpoint bits, rings and bookkeeping, step after step (outputs within

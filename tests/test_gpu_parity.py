@@ -152,6 +152,19 @@ def test_shape_edges(orc, T, W_, G):
     run_pair(orc, wl)
 
 
+def test_batch_beyond_one_classification_pass(orc):
+    """640 rows (more than one CTA's threads, so the flush classifies the rows
+    in several passes of 288 and carries the compacted positions across them),
+    varlen rows, a padding row, random ring starts, live prefixes that flush in
+    the first steps, and a forced flush every third step."""
+    wl = W.Workload(name="edge", num_slots=700, nheads=4, ngroups=2, max_window=16, npredicted=4,
+                    state_dtype=W.BF16, batch=640, T=4, steps=6, varlen=True, pad_row=True,
+                    ring_start_random=True, prefill_live=14, config_id=9)
+    pair = run_pair(orc, wl, force_every=3)
+    assert pair.oc.flush_epoch.max() >= 2
+    assert int(pair.oc.error_word[0]) == 0
+
+
 def test_bad_rows_set_error_bits_and_zero_outputs(orc):
     wl = W.config("tiny", state_dtype=W.BF16)
     gen = W.Generator(wl)
