@@ -52,12 +52,19 @@ def parse():
     ap.add_argument("--config", default="mamba2_decode")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--force-flush", action="store_true", help="flush every active row every step")
+    ap.add_argument("--full-window", action="store_true",
+                    help="before every step (outside the timed region) give every active row a full window of "
+                         "live tokens (pnat = max_window) and flush them all: the flush roofline run")
     ap.add_argument("--path", default="split", choices=["fused", "split"],
                     help="fused: rssm_flush_step; split: rssm_flush then rssm_step")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU budget of the oracle baseline sample")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.full_window:  # the refill runs between steps, so there is no back-to-back leg or oracle sample
+        args.no_e2e = True
+        args.no_cpu_baseline = True
+    return args
 
 
 def workload(args):
@@ -340,7 +347,14 @@ def run_gpu(args, rank, ws, local):
         l2.zero_()
         l2r.max()
 
-    force = 1 if args.force_flush else 0
+    force = 1 if (args.force_flush or args.full_window) else 0
+    full_p = min(wl.max_window, wl.L - wl.T)  # a full window that still leaves room for the step's tokens
+
+    def refill():
+        """Full-window runs: every active row gets pnat = max_window live tokens
+        (the rings hold earlier appends); untimed."""
+        if args.full_window:
+            pnat.masked_fill_(gids > 0, full_p)
     ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
     cu = buf["cu"]
 
@@ -446,6 +460,7 @@ def run_gpu(args, rank, ws, local):
         return int(((ids > 0) & (tb > 0)).sum()) * wl.nheads
 
     for k in range(args.warmup):
+        refill()
         load_inputs(dev_inp[k])
         cold_l2()
         g_step.replay()
@@ -457,6 +472,7 @@ def run_gpu(args, rank, ws, local):
     torch.cuda.synchronize()
     clocks = ClockSampler(torch.cuda.current_device())
     for k in range(args.warmup, nsteps):
+        refill()
         load_inputs(dev_inp[k])
         cold_l2()
         e0 = ev()
@@ -479,6 +495,7 @@ def run_gpu(args, rank, ws, local):
     grp_ms = [[] for _ in groups]
     read_bytes, fold_bytes, fold_units = 0.0, 0.0, 0
     for k in range(args.warmup, nsteps):
+        refill()
         load_inputs(dev_inp[k])
         cold_l2()
         evs = [ev()]
@@ -625,7 +642,8 @@ def run_gpu(args, rank, ws, local):
         "dtype": "f32", "data": "synthetic",
         "config": dict(wl.describe(), parallelism=f"replicas{ws}", l2="1 GiB written then 512 MiB read between steps (cold, clean L2)",
                        launch="one CUDA graph per step (kernels chained by programmatic dependent launch); kernel times from a second pass with one graph per launch group",
-                       force_flush=bool(args.force_flush), path=args.path),
+                       force_flush=bool(args.force_flush or args.full_window),
+                       full_window=bool(args.full_window), path=args.path),
         "roofline": {"bound": "hbm", "kernel": "step_kernel" if fused else "readout_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if fused or args.batch is not None else profiled_traffic("readout_kernel", wl.name),
