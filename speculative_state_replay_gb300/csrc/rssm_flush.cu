@@ -13,7 +13,10 @@
 //   mod L, pnat = 0, epoch += 1) while the folds run.
 #include <cuda_runtime.h>
 
+#include <cstring>
+
 #include "rssm_device.cuh"
+#include "rssm_readout.cuh"
 
 namespace rssm {
 
@@ -65,6 +68,40 @@ __device__ __forceinline__ int block_excl_scan(int flag, int* wsum, int& total) 
 }
 
 // ---------------------------------------------------------------------------
+// tensor-core pieces of the fold (2-byte states, nearest rounding)
+// ---------------------------------------------------------------------------
+// d += A B on one m16n8k16 tile, bf16 operands, fp32 accumulation; a0..a3 =
+// A[g][2c..2c+1], A[g+8][2c..], A[g][2c+8..], A[g+8][2c+8..]; b0, b1 =
+// B[2c..2c+1][g], B[2c+8..2c+9][g]; d = D[g][2c..2c+1], D[g+8][2c..2c+1]
+// (g = lane / 4, c = lane % 4)
+__device__ __forceinline__ void mma16816_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// four 8x8 b16 matrices from shared memory (lane 8i + k gives row k of matrix
+// i); lane (g, c) receives row g, columns 2c..2c+1 of each -- with .trans,
+// rows 2c..2c+1 of column g
+__device__ __forceinline__ void ldmatrix_x4(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t (&r)[4], uint32_t saddr) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(saddr));
+}
+// fp32 pair -> bf16 pair, round to nearest even, low half = first
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
 // fold kernel
 // ---------------------------------------------------------------------------
 struct FoldMeta {
@@ -78,33 +115,46 @@ struct FoldLayout {
   uint32_t meta_off, rows_off, stages_off, total;
 };
 
+// 2-byte states: S0 arrives as the readout's TMA boxes (64 rows x 128 bytes,
+// 128-byte swizzle) and the live x and B rows in rows padded by 16 bytes, so
+// that 8 rows read at one column (ldmatrix, the tensor-core fold's fragments)
+// fall on distinct banks.  Other states: S0 and the rows as stored.
+__host__ __device__ constexpr bool fold_2byte(int dtype) { return dtype == RSSM_BF16 || dtype == RSSM_F16; }
+__host__ __device__ constexpr int fold_xs(int dtype) { return fold_2byte(dtype) ? kDim + 8 : kDim; }        // x row stride (elements)
+__host__ __device__ constexpr int fold_bs(int dtype) { return fold_2byte(dtype) ? kDstate + 8 : kDstate; }  // B row stride (elements)
+
 // barriers | per-stage metadata | the records of the flushed rows this CTA
-// folds (up to `maxrows`) | stages; one stage: S0 (as stored) | 8-bit scales |
-// live x rows | live B rows | live dt' | A of the head
+// folds (up to `maxrows`) | stages; one stage: S0 | 8-bit scales | live x rows
+// | live B rows | live dt' | A of the head
 __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int maxrows) {
   FoldLayout f;
   f.ns = ns;
   f.KB = (L + 3) & ~3;
-  const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
+  const int esz = dtype == RSSM_F32 ? 4 : fold_2byte(dtype) ? 2 : 1;
+  const uint32_t align = fold_2byte(dtype) ? 1024u : 128u;  // swizzled TMA boxes need 1024-byte alignment
   f.s0_bytes = kHeadElems * esz;
   uint32_t o = f.s0_bytes;
   f.scale_off = o;
   if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256;
   f.x_off = o;
-  o += f.KB * kDim * 2;
+  o += f.KB * fold_xs(dtype) * 2;
   f.b_off = o;
-  o += f.KB * kDstate * 2;
+  o += f.KB * fold_bs(dtype) * 2;
   f.dt_off = o;
   o += f.KB * 4;
   f.sc_off = o;
   o += 16;
-  f.stage_bytes = (o + 127) & ~127u;
+  f.stage_bytes = (o + align - 1) & ~(align - 1);
   f.meta_off = 256;  // after the barriers
   f.rows_off = 512;
-  f.stages_off = (f.rows_off + maxrows * static_cast<uint32_t>(sizeof(FlushRec)) + 127) & ~127u;
-  f.total = f.stages_off + f.ns * f.stage_bytes;
+  f.stages_off = (f.rows_off + maxrows * static_cast<uint32_t>(sizeof(FlushRec)) + align - 1) & ~(align - 1);
+  f.total = f.stages_off + f.ns * f.stage_bytes + (align == 1024u ? 1024u : 0u);  // + slack to align the base
   return f;
 }
+
+// smallest live prefix folded on the tensor cores (2-byte states, nearest
+// rounding); shorter prefixes take the CUDA-core fold (K is padded to 16)
+constexpr int kMmaMinP = 9;
 
 // Classification, fold, requantisation and bookkeeping of rssm_flush in one
 // kernel.  Every CTA classifies all rows (two passes over slot_idx, pnat and
@@ -114,8 +164,13 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int 
 // once it has classified (a self-resetting ticket), i.e. after every CTA has
 // read the values it replaces; nothing in the kernel reads them afterwards.
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns, int maxrows) {
-  extern __shared__ __align__(128) uint8_t smem[];
+__global__ void __launch_bounds__(kThreads, 2)
+    flush_kernel(const __grid_constant__ CUtensorMap s0map, FlushArgs a, int ns, int maxrows) {
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  constexpr bool k2B = fold_2byte(DT);
+  constexpr int XS = fold_xs(DT), BS = fold_bs(DT);
+  uint8_t* smem = k2B ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
+                      : smem_raw;
   __shared__ int wsum[kThreads / 32];
   __shared__ int s_last;
   const Cache& c = a.c;
@@ -199,10 +254,12 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
 
   if (nu > 0 && warp == kConsumerWarps) {
     // ---------------- producer warp ----------------
-    // Lane 0 copies S0 (+ scales) and the live x and B rows (at most two
-    // contiguous segments each) with 1-D bulk copies; the lanes copy the live
-    // dt' values and A of the head with cp.async.  Nothing here waits for a
-    // load it issued: the next unit's flagged-row record is loaded a unit ahead.
+    // Lane 0 copies S0 (+ scales) -- 2-byte states as two TMA boxes, others
+    // with a 1-D bulk copy -- and the live x and B rows (at most two
+    // contiguous segments each) with 1-D bulk copies, except for units folded
+    // on the tensor cores, whose rows the lanes copy 16 bytes at a time into
+    // padded rows.  The lanes copy the live dt' values and A of the head with
+    // cp.async.  Nothing here waits for a load it issued.
     int issued = 0;
     bool ok = true;
     // stage index and phase, and the unit's (flushed row, head), advance by
@@ -222,26 +279,48 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
       const int s = rec.s, r = rec.r, p = rec.p, g = h / c.hpg;
       uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
       const float* dg = c.dt_cache + static_cast<long long>(s) * c.dt_stride + static_cast<long long>(h) * L;
+      const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * L * kDim;
+      const uint16_t* bg = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
+      // units folded on the tensor cores take their x and B rows padded; the rest as stored
+      const bool mma_unit = k2B && c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP;
       if (lane == 0) {
-        const uint32_t bytes = lay.s0_bytes + (k8bit ? 256u : 0u) + static_cast<uint32_t>(p) * (kDim * 2 + kDstate * 2);
+        const uint32_t bytes =
+            lay.s0_bytes + (k8bit ? 256u : 0u) + (mma_unit ? 0u : static_cast<uint32_t>(p) * (kDim * 2 + kDstate * 2));
         mbar_expect_tx(&full[st], bytes);
-        const uint8_t* st_g = static_cast<const uint8_t*>(c.state) +
-                              (static_cast<long long>(s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz;
-        bulk_g2s(sb, st_g, lay.s0_bytes, &full[st]);
-        if (k8bit) bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256,
-                            &full[st]);
-        const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * L * kDim;
-        const uint16_t* bg = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
-        const int n1 = min(p, L - r);
-        if (n1 > 0) {
-          bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
-          bulk_g2s(sb + lay.b_off, bg + r * kDstate, n1 * kDstate * 2, &full[st]);
+        if constexpr (k2B) {
+#pragma unroll
+          for (int bx = 0; bx < 2; ++bx) tma_load_3d(sb + bx * 8192, &s0map, bx * 64, h * kDim, s, &full[st]);
+        } else {
+          const uint8_t* st_g = static_cast<const uint8_t*>(c.state) +
+                                (static_cast<long long>(s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz;
+          bulk_g2s(sb, st_g, lay.s0_bytes, &full[st]);
+          if (k8bit)
+            bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256,
+                     &full[st]);
         }
-        if (p > n1) {
-          bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (p - n1) * kDim * 2, &full[st]);
-          bulk_g2s(sb + lay.b_off + n1 * kDstate * 2, bg, (p - n1) * kDstate * 2, &full[st]);
+        if (!mma_unit) {
+          const int n1 = min(p, L - r);
+          if (n1 > 0) {
+            bulk_g2s(sb + lay.x_off, xg + r * kDim, n1 * kDim * 2, &full[st]);
+            bulk_g2s(sb + lay.b_off, bg + r * kDstate, n1 * kDstate * 2, &full[st]);
+          }
+          if (p > n1) {
+            bulk_g2s(sb + lay.x_off + n1 * kDim * 2, xg, (p - n1) * kDim * 2, &full[st]);
+            bulk_g2s(sb + lay.b_off + n1 * kDstate * 2, bg, (p - n1) * kDstate * 2, &full[st]);
+          }
         }
         cp_async4(sb + lay.sc_off, a.A + h);
+      }
+      if (mma_unit) {
+        // live rows into padded shared rows: x 8 and B 16 chunks of 16 bytes per row
+        for (int q = lane; q < p * 8; q += 32) {
+          const int j = q >> 3, part = q & 7, pos = r + j >= L ? r + j - L : r + j;
+          cp_async16(sb + lay.x_off + (j * XS + part * 8) * 2, xg + pos * kDim + part * 8);
+        }
+        for (int q = lane; q < p * 16; q += 32) {
+          const int j = q >> 4, part = q & 15, pos = r + j >= L ? r + j - L : r + j;
+          cp_async16(sb + lay.b_off + (j * BS + part * 8) * 2, bg + pos * kDstate + part * 8);
+        }
       }
       if (lane < p) cp_async4(sb + lay.dt_off + lane * 4, dg + (r + lane >= L ? r + lane - L : r + lane));
       cp_async_arrive_noinc(&full[st]);
@@ -287,6 +366,89 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
     const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
     const float wj = lane < p ? __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj) : 0.0f;
     const float decay = spec_exp(c_end);
+    if constexpr (k2B) {
+      if (c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP) {
+        // The fold on the tensor cores: S0' = e^{c_end} S0 + U Bm, U[d][j] =
+        // w_j x_j[d] (64 x p), Bm[j][n] = B_j[n] (p x 128), as mma.sync
+        // m16n8k16 with fp32 accumulation starting from e^{c_end} S0; U is
+        // split into bf16 hi + lo (16 bits of its mantissa), B is exact in
+        // bf16.  The sum order differs from the canonical fp32 chain, which
+        // only 8-bit and stochastically rounded states need bit for bit.
+        // Warp: rows mr..mr+15, columns nb..nb+63 (8 tiles of 8).
+        const int g = lane >> 2, cq = lane & 3, mi = lane >> 3, rr = lane & 7;
+        const int mr = 16 * (warp & 3), nb = 64 * (warp >> 2);
+        const uint32_t sbase = smem_addr(sb);
+        float D[8][4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          // S0 fragments from the swizzled boxes: matrices (rows mr, mr + 8) x (columns n, n + 8)
+          const int d = mr + 8 * (mi & 1) + rr, n = nb + 16 * t + 8 * (mi >> 1);
+          uint32_t sv[4];
+          ldmatrix_x4(sv, sbase + swizzled_offset<2>(d, n));
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float2 v;
+            if constexpr (DT == RSSM_BF16)
+              v = make_float2(bf16lo(sv[q]), bf16hi(sv[q]));
+            else
+              v = h2f2(sv[q]);
+            float* dd = &D[2 * t + (q >> 1)][2 * (q & 1)];
+            dd[0] = __fmul_rn(decay, v.x);
+            dd[1] = __fmul_rn(decay, v.y);
+          }
+        }
+        const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
+        const uint32_t bsa = sbase + lay.b_off;
+        for (int kb = 0; kb < p; kb += 16) {
+          // A fragments: rows mr + g, mr + g + 8; tokens kb + 2cq (+1), kb + 2cq + 8 (+1)
+          uint32_t ahi[4], alo[4];
+#pragma unroll
+          for (int hh = 0; hh < 2; ++hh) {
+            float u0[2], u1[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int j = kb + 2 * cq + 8 * hh + e;
+              const float w = __shfl_sync(0xffffffffu, wj, j & 31);
+              const bool live = j < p;
+              u0[e] = live ? __fmul_rn(w, __uint_as_float(static_cast<uint32_t>(xs[j * XS + mr + g]) << 16)) : 0.0f;
+              u1[e] = live ? __fmul_rn(w, __uint_as_float(static_cast<uint32_t>(xs[j * XS + mr + g + 8]) << 16)) : 0.0f;
+            }
+            const uint32_t h0 = bf16x2_rn(u0[0], u0[1]), h1 = bf16x2_rn(u1[0], u1[1]);
+            ahi[2 * hh] = h0;
+            ahi[2 * hh + 1] = h1;
+            alo[2 * hh] = bf16x2_rn(__fsub_rn(u0[0], bf16lo(h0)), __fsub_rn(u0[1], bf16hi(h0)));
+            alo[2 * hh + 1] = bf16x2_rn(__fsub_rn(u1[0], bf16lo(h1)), __fsub_rn(u1[1], bf16hi(h1)));
+          }
+          // B fragments, two column tiles per ldmatrix: matrices (tokens kb, kb + 8)
+          // x (columns n, n + 8); token rows past p read row 0 (their U is 0)
+          const int kr = kb + 8 * (mi & 1) + rr;
+          const uint32_t rowa = bsa + static_cast<uint32_t>((kr < p ? kr : 0) * BS + 8 * (mi >> 1)) * 2;
+#pragma unroll
+          for (int t = 0; t < 4; ++t) {
+            uint32_t bv[4];
+            ldmatrix_x4_trans(bv, rowa + static_cast<uint32_t>(nb + 16 * t) * 2);
+            mma16816_bf16(D[2 * t], ahi, bv[0], bv[1]);
+            mma16816_bf16(D[2 * t], alo, bv[0], bv[1]);
+            mma16816_bf16(D[2 * t + 1], ahi, bv[2], bv[3]);
+            mma16816_bf16(D[2 * t + 1], alo, bv[2], bv[3]);
+          }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
+        uint16_t* hs = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(c.state) +
+                                                   (static_cast<long long>(m.s) * c.state_stride +
+                                                    static_cast<long long>(m.h) * kHeadElems) * esz);
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int n = nb + 8 * nt + 2 * cq;
+          *reinterpret_cast<uint32_t*>(hs + (mr + g) * kDstate + n) =
+              DT == RSSM_BF16 ? cvt_bf16x2_sat(D[nt][0], D[nt][1]) : cvt_f16x2_sat(D[nt][0], D[nt][1]);
+          *reinterpret_cast<uint32_t*>(hs + (mr + g + 8) * kDstate + n) =
+              DT == RSSM_BF16 ? cvt_bf16x2_sat(D[nt][2], D[nt][3]) : cvt_f16x2_sat(D[nt][2], D[nt][3]);
+        }
+        continue;
+      }
+    }
     // acc = e^{c_end} * S0f
     float2 acc[4][4];
 #pragma unroll
@@ -299,11 +461,11 @@ __global__ void __launch_bounds__(kThreads, 2) flush_kernel(FlushArgs a, int ns,
         v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
         v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
       } else if constexpr (DT == RSSM_BF16) {
-        const uint4 q = *reinterpret_cast<const uint4*>(sb + (row * kDstate + c0) * 2);
+        const uint4 q = *reinterpret_cast<const uint4*>(sb + swizzled_offset<2>(row, c0));
         v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
         v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
       } else if constexpr (DT == RSSM_F16) {
-        const uint4 q = *reinterpret_cast<const uint4*>(sb + (row * kDstate + c0) * 2);
+        const uint4 q = *reinterpret_cast<const uint4*>(sb + swizzled_offset<2>(row, c0));
         float2 t0 = h2f2(q.x), t1 = h2f2(q.y), t2 = h2f2(q.z), t3 = h2f2(q.w);
         v[0] = t0.x; v[1] = t0.y; v[2] = t1.x; v[3] = t1.y; v[4] = t2.x; v[5] = t2.y; v[6] = t3.x; v[7] = t3.y;
       } else {
@@ -472,7 +634,11 @@ static int launch_flush_t(const FlushArgs& a, int num_sms, cudaStream_t st) {
   e = cudaFuncSetAttribute(flush_kernel<DT>, cudaFuncAttributePreferredSharedMemoryCarveout,
                            cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(flush_kernel<DT>, dim3(grid), dim3(kThreads), lay.total, st, a, ns, maxrows);
+  // 2-byte states: S0 by TMA boxes through the readout's tensor map (unused otherwise)
+  CUtensorMap map;
+  memset(&map, 0, sizeof(map));
+  if (fold_2byte(DT) && !encode_state_map(a.c, &map, 1)) return cudaErrorInvalidValue;
+  e = launch_pdl(flush_kernel<DT>, dim3(grid), dim3(kThreads), lay.total, st, map, a, ns, maxrows);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 

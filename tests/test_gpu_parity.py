@@ -10,7 +10,7 @@ import torch
 
 from speculative_state_replay_gb300 import api
 from speculative_state_replay_gb300 import workloads as W
-from tests.gpu_harness import Pair, bf16_f32, dev_of, host_of
+from tests.gpu_harness import Pair, bf16_f32, dev_of, host_of, state_close
 from tests.harness import oracle_cache
 
 pytestmark = pytest.mark.gpu
@@ -240,6 +240,8 @@ def test_full_size_mamba2_decode_sampled_rows(orc):
         assert np.allclose(bf16_f32(yg), bf16_f32(yo), atol=2e-2, rtol=1e-2), k
         assert np.array_equal(gp.cpu().numpy()[sample], ps)
         gsid = torch.from_numpy(sid.astype(np.int64)).cuda()
-        for name in ("state", "x_cache", "B_cache", "dt_cache", "ring_start", "flush_epoch"):
+        o = oc_full.state[sid]
+        assert state_close(wl.state_dtype, host_of(gc.state[gsid], o), o), (k, "state")
+        for name in ("x_cache", "B_cache", "dt_cache", "ring_start", "flush_epoch"):
             o = getattr(oc_full, name)[sid]
             assert np.array_equal(host_of(getattr(gc, name)[gsid], o), o), (k, name)
