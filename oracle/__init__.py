@@ -84,7 +84,7 @@ def lib():
             _lib.orc_flush.argtypes = [ctypes.POINTER(OrcCache), vp, vp, vp, vp, i32, i32, i32, u64, ctypes.c_int]
             _lib.orc_step.restype = ctypes.c_int
             _lib.orc_step.argtypes = [ctypes.POINTER(OrcCache), vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32,
-                                      vp, vp, ctypes.c_int]
+                                      vp, vp, vp, ctypes.c_int]
             _lib.orc_accept.restype = ctypes.c_int
             _lib.orc_accept.argtypes = [ctypes.POINTER(OrcCache), vp, vp, vp, vp, i32, i32]
             _lib.orc_have_openmp.restype = ctypes.c_int
@@ -258,8 +258,10 @@ class OracleCache:
                              seed, nthreads)
         assert rc == 0
 
-    def step(self, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, cu_seqlens=None, want_f64=False, nthreads=0):
-        """Returns y (bf16 bits, [tok][H][64]) and optionally y in float64."""
+    def step(self, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, cu_seqlens=None, want_f64=False, nthreads=0,
+             z=None):
+        """Returns y (bf16 bits, [tok][H][64]) and optionally y in float64.
+        `z` (bf16 bits, [tok][H][64]): output gate, y * silu(z) before rounding."""
         x = np.ascontiguousarray(x, np.uint16)
         B = np.ascontiguousarray(B, np.uint16)
         C = np.ascontiguousarray(C, np.uint16)
@@ -274,8 +276,10 @@ class OracleCache:
         out = np.zeros((ntok, self.H, P_DIM), np.uint16)
         out64 = np.zeros((ntok, self.H, P_DIM), np.float64) if want_f64 else None
         st = self.struct()
+        zz = None if z is None else np.ascontiguousarray(z, np.uint16)
+        assert zz is None or zz.shape == out.shape
         rc = lib().orc_step(ctypes.byref(st), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(dt_bias),
-                            _p(slot_idx), _p(pnat), _p(cu), slot_idx.size, T, _p(out), _p(out64), nthreads)
+                            _p(slot_idx), _p(pnat), _p(cu), slot_idx.size, T, _p(zz), _p(out), _p(out64), nthreads)
         assert rc == 0
         return (out, out64) if want_f64 else out
 

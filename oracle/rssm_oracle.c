@@ -574,13 +574,18 @@ int orc_flush(const orc_cache *c, const float *A, const int32_t *slot_idx, int32
  *           + D x_t
  * (the replay of [FI] Description item 1: C.B contraction, cumulative A dt
  * decays, state replay + output projection), evaluated in double and
- * rounded to bf16 once.  New x, B, dt' are appended at (r + p + t) mod L.
+ * rounded to bf16 once; with an output gate z ([bf16 tok][H][64], nullable),
+ * y_t[d] * silu(z_t[d]) in double before that rounding (the gated output of
+ * Mamba-2's selective state update; [FI] commit notes list z among the
+ * operands the monolithic kernel stages with x).
+ * New x, B, dt' are appended at (r + p + t) mod L.
  * Rows whose slot is inactive, or which fail a range check, get y = 0 and
  * touch no cache.                                                           */
 /* ------------------------------------------------------------------------- */
 int orc_step(const orc_cache *c, const uint16_t *x, const float *dt, const float *A, const uint16_t *B,
              const uint16_t *C, const float *D, const float *dt_bias, const int32_t *slot_idx, const int32_t *pnat,
-             const int32_t *cu, int32_t batch, int32_t T, uint16_t *out, double *out_f64, int nthreads) {
+             const int32_t *cu, int32_t batch, int32_t T, const uint16_t *z, uint16_t *out, double *out_f64,
+             int nthreads) {
   if (check_cache(c) || T < 0 || batch < 0) return -1;
   int H = c->nheads, G = c->ngroups, hpg = H / G, L = ring_len(c);
   /* validate rows first (sets the error bits once per row) */
@@ -663,6 +668,10 @@ int orc_step(const orc_cache *c, const uint16_t *x, const float *dt, const float
           for (int k = 0; k <= kt; ++k) ring += coef[k] * (double)xk[k * P_DIM + d];
           double yv = decay * sc + ring + (double)D[h] * (double)xk[kt * P_DIM + d];
           size_t o = (tok * H + h) * P_DIM + d;
+          if (z) { /* output gate: y * silu(z), silu(v) = v / (1 + e^-v) */
+            double zv = orc_bf16_decode(z[o]);
+            yv *= zv / (1.0 + exp(-zv));
+          }
           out[o] = orc_f32_to_bf16((float)yv);
           if (out_f64) out_f64[o] = yv;
         }

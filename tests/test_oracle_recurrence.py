@@ -12,6 +12,8 @@ Pins:
   * ring bookkeeping equals a plain list model
   * packed cu_seqlens == separate per-request calls; padded slot pages ==
     contiguous pages; init ignores ids <= 0 or >= S
+  * output gate: y * silu(z) == torch's silu on the float64 recurrence; z = 0
+    gives zeros, z = 40 gives z * y exactly
 """
 import numpy as np
 import pytest
@@ -311,3 +313,57 @@ def test_error_bits_for_bad_rows(orc):
     c.error_word[:] = 0
     c.accept(ids, p, acc, wl.T)
     assert c.error_word[0] & orc.ERR_ACCEPT
+
+
+def _gate_bits(shape, seed, value=None):
+    """bf16 bits of an output gate z: N(0, 1) draws, or a constant."""
+    if value is not None:
+        return np.full(shape, np.float32(value), np.float32).view(np.uint32).__rshift__(16).astype(np.uint16)
+    v = np.random.default_rng(seed).standard_normal(shape).astype(np.float32)
+    return (v.view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_output_gate_equals_library_silu_on_the_recurrence(orc):
+    """y * silu(z): the gated oracle against torch's silu applied to the
+    float64 brute-force recurrence, and rounded to bf16 once."""
+    import torch
+
+    wl = W.config("tiny", prefill_live=12, ring_start_random=True)
+    gen = W.Generator(wl)
+    params = gen.params()
+    c, ids, pnat = oracle_cache(orc, wl, gen)
+    inp = gen.step(0)
+    z = _gate_bits((inp.ntok, wl.nheads, 64), 5)
+    y_bits, y64 = c.copy().step(inp.x, inp.dt, params[0], inp.B, inp.C, params[1], params[2], ids, pnat, wl.T,
+                                want_f64=True, z=z)
+    zf = torch.nn.functional.silu(torch.from_numpy(brute.bf16_to_f64(z))).numpy()
+    worst = 0.0
+    for b, s in enumerate(ids):
+        tok0, Tb = _row_tokens(inp, b, wl.T)
+        if s <= 0:
+            assert not y64[tok0:tok0 + Tb].any()
+            continue
+        for h in range(wl.nheads):
+            ys, _, _ = _bruteforce_row(c, wl, params, int(s), int(pnat[b]), h, inp, tok0, Tb)
+            want = ys * zf[tok0:tok0 + Tb, h]
+            got = y64[tok0:tok0 + Tb, h]
+            worst = max(worst, float(np.abs(got - want).max() / (np.abs(want).max() + 1e-30)))
+    assert worst < 2e-5, worst
+    assert np.array_equal(y_bits, orc.f32_to_bf16_bits(y64.astype(np.float32)))
+
+
+def test_output_gate_special_values(orc):
+    """z = 0 closes the gate (every output exactly zero); z = 40 makes
+    silu(z) = z exactly in double, so the output is z * y rounded once."""
+    wl = W.config("tiny", prefill_live=12, ring_start_random=True)
+    gen = W.Generator(wl)
+    params = gen.params()
+    c, ids, pnat = oracle_cache(orc, wl, gen)
+    inp = gen.step(0)
+    shape = (inp.ntok, wl.nheads, 64)
+    args = (inp.x, inp.dt, params[0], inp.B, inp.C, params[1], params[2], ids, pnat, wl.T)
+    y0 = c.copy().step(*args, z=_gate_bits(shape, 0, 0.0))
+    assert not (y0 & 0x7FFF).any()
+    _, y64 = c.copy().step(*args, want_f64=True)
+    y40 = c.copy().step(*args, z=_gate_bits(shape, 0, 40.0))
+    assert np.array_equal(y40, orc.f32_to_bf16_bits((y64 * 40.0).astype(np.float32)))
