@@ -246,6 +246,27 @@ rssm_status rssm_step_readout(const rssm_cache *cache, const void *x, const floa
                               void *stream);
 
 /*
+ * rssm_step and rssm_step_readout with Mamba-2's output gate: every output is
+ * y_t[d] * silu(z_t[d]) (silu(v) = v / (1 + e^-v)), formed in fp32 before
+ * the bf16 rounding; the FlashInfer PR's commit notes list z among the
+ * operands its monolithic kernel stages next to x.  z bf16 [tok][H][64]
+ * (device, 16-byte aligned; read only), laid out like out; z = NULL gives
+ * rssm_step / rssm_step_readout exactly.  Padding and rejected rows still
+ * get zeros.  Errors as rssm_step (a misaligned z: RSSM_ERR_INVALID_ARGUMENT,
+ * before any launch).  rssm_step_gated == rssm_step_precompute followed by
+ * rssm_step_readout_gated.
+ */
+rssm_status rssm_step_gated(const rssm_cache *cache, const void *x, const float *dt, const float *A, const void *B,
+                            const void *C, const float *D, const float *dt_bias, const int32_t *slot_idx,
+                            const int32_t *pnat, const int32_t *cu_seqlens, int32_t batch, int32_t T, const void *z,
+                            void *out, void *scratch, size_t scratch_bytes, void *stream);
+rssm_status rssm_step_readout_gated(const rssm_cache *cache, const void *x, const float *dt, const float *A,
+                                    const void *B, const void *C, const float *D, const float *dt_bias,
+                                    const int32_t *slot_idx, const int32_t *pnat, const int32_t *cu_seqlens,
+                                    int32_t batch, int32_t T, const void *z, void *out, void *scratch,
+                                    size_t scratch_bytes, void *stream);
+
+/*
  * Commit verified drafts: pnat[b] += accepted[b] for active rows, so the
  * first accepted[b] tokens appended by the last rssm_step join the live
  * prefix; the rest stay outside it and are overwritten by later appends

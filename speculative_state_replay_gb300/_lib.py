@@ -28,7 +28,7 @@ class RssmCacheStruct(ctypes.Structure):
 
 
 EXPORTS = ("rssm_scratch_bytes", "rssm_init_state", "rssm_flush", "rssm_step", "rssm_step_precompute",
-           "rssm_step_readout", "rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main", "rssm_accept", "rssm_eval_spec_math", "rssm_status_string")
+           "rssm_step_readout", "rssm_step_gated", "rssm_step_readout_gated", "rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main", "rssm_accept", "rssm_eval_spec_math", "rssm_status_string")
 
 
 def load(path: str | None = None):
@@ -54,6 +54,10 @@ def load(path: str | None = None):
         for name in ("rssm_step", "rssm_step_precompute", "rssm_step_readout"):
             getattr(lib, name).restype = ctypes.c_int
             getattr(lib, name).argtypes = step_args
+        gated_args = step_args[:13] + [vp] + step_args[13:]  # z before out
+        for name in ("rssm_step_gated", "rssm_step_readout_gated"):
+            getattr(lib, name).restype = ctypes.c_int
+            getattr(lib, name).argtypes = gated_args
         for name in ("rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main"):
             getattr(lib, name).restype = ctypes.c_int
             getattr(lib, name).argtypes = [cp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, u64, vp, vp, sz, vp]

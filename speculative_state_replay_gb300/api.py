@@ -141,8 +141,21 @@ def _step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch
                  scratch.numel(), _stream(stream)))
 
 
-def rssm_step(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None, stream=None):
-    _step("rssm_step", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, stream)
+def _step_gated(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, z, out, scratch, cu_seqlens, stream):
+    f = getattr(_lib.load(), fn)
+    _check(fn, f(cache.struct(), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
+                 _ptr(slot_idx), _ptr(pnat), _ptr(cu_seqlens), slot_idx.numel(), T, _ptr(z), _ptr(out),
+                 _ptr(scratch), scratch.numel(), _stream(stream)))
+
+
+def rssm_step(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None, stream=None,
+              z=None):
+    """`z`: optional output gate (bf16 bits [tok][H][64]): y * silu(z)."""
+    if z is None:
+        _step("rssm_step", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, stream)
+    else:
+        _step_gated("rssm_step_gated", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, z, out, scratch,
+                    cu_seqlens, stream)
 
 
 def rssm_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
@@ -152,9 +165,13 @@ def rssm_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, o
 
 
 def rssm_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens=None,
-                      stream=None):
-    _step("rssm_step_readout", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens,
-          stream)
+                      stream=None, z=None):
+    if z is None:
+        _step("rssm_step_readout", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens,
+              stream)
+    else:
+        _step_gated("rssm_step_readout_gated", cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, z, out,
+                    scratch, cu_seqlens, stream)
 
 
 def _flush_step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, force, seed,

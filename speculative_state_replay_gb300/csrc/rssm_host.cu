@@ -123,6 +123,7 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->TP = t_pad(T);
   a->KB = ring_pad(a->c.L);
   a->out = static_cast<uint16_t*>(out);
+  a->z = nullptr;
   a->flush_mode = 0;
   a->seed = 0;
   a->pnat_rw = nullptr;
@@ -203,28 +204,48 @@ rssm_status rssm_step_precompute(const rssm_cache* cache, const void* x, const f
   return launch_precompute(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
-rssm_status rssm_step_readout(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
-                              const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
-                              const int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, void* out,
-                              void* scratch, size_t scratch_bytes, void* stream) {
+rssm_status rssm_step_readout_gated(const rssm_cache* cache, const void* x, const float* dt, const float* A,
+                                    const void* B, const void* C, const float* D, const float* dt_bias,
+                                    const int32_t* slot_idx, const int32_t* pnat, const int32_t* cu_seqlens,
+                                    int32_t batch, int32_t T, const void* z, void* out, void* scratch,
+                                    size_t scratch_bytes, void* stream) {
   StepArgs a;
   rssm_status st = step_common(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out, scratch,
                                scratch_bytes, &a);
   if (st != RSSM_OK || batch == 0) return st;
+  if (z && !aligned16(z)) return RSSM_ERR_INVALID_ARGUMENT;
+  a.z = static_cast<const uint16_t*>(z);
   const int sms = num_sms();
   if (sms <= 0) return RSSM_ERR_CUDA;
   return launch_readout(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_step_readout(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
+                              const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
+                              const int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, void* out,
+                              void* scratch, size_t scratch_bytes, void* stream) {
+  return rssm_step_readout_gated(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, nullptr,
+                                 out, scratch, scratch_bytes, stream);
+}
+
+rssm_status rssm_step_gated(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
+                            const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
+                            const int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, const void* z,
+                            void* out, void* scratch, size_t scratch_bytes, void* stream) {
+  if (batch > 0 && z && !aligned16(z)) return RSSM_ERR_INVALID_ARGUMENT;  // checked before anything launches
+  rssm_status st = rssm_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out,
+                                        scratch, scratch_bytes, stream);
+  if (st != RSSM_OK) return st;
+  return rssm_step_readout_gated(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, z, out,
+                                 scratch, scratch_bytes, stream);
 }
 
 rssm_status rssm_step(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,
                       const void* C, const float* D, const float* dt_bias, const int32_t* slot_idx,
                       const int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, void* out,
                       void* scratch, size_t scratch_bytes, void* stream) {
-  rssm_status st = rssm_step_precompute(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out,
-                                        scratch, scratch_bytes, stream);
-  if (st != RSSM_OK) return st;
-  return rssm_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out, scratch,
-                           scratch_bytes, stream);
+  return rssm_step_gated(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, nullptr, out,
+                         scratch, scratch_bytes, stream);
 }
 
 namespace {

@@ -85,6 +85,7 @@ struct StepArgs {
   int TP;  // T padded to 4 or 8
   int KB;  // ring rows padded to a multiple of 4
   uint16_t* out;
+  const uint16_t* z;         // output gate [tok][H][64] bf16, or null: y * silu(z) (the readout)
   int flush_mode;            // rssm_flush_step: 1 flush rows with p + T_b > W first; 2 every active row
   unsigned long long seed;   // stochastic-rounding key of the fold (flush_mode != 0)
   int* pnat_rw;              // pnat, written by the fold's bookkeeping (flush_mode != 0)

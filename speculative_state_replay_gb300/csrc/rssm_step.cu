@@ -450,6 +450,14 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       continue;
     }
     if (m.flags & 2) load_c_frags(reinterpret_cast<const uint16_t*>(sb + lay.c_off), g, cq, af);
+    // output gate: this lane's z pair per head, requested before the contraction
+    uint32_t zw[HPU];
+    const bool gated = a.z != nullptr && g < m.Tb;
+#pragma unroll
+    for (int j = 0; j < HPU; ++j)
+      zw[j] = gated ? *reinterpret_cast<const uint32_t*>(a.z + (static_cast<long long>(m.tok0 + g) * H + m.h + j) *
+                                                                   kDim + dout)
+                    : 0u;
     float y[HPU][2];
 #pragma unroll
     for (int j = 0; j < HPU; ++j) {  // head m.h + j: rows 64 j .. of the stage's boxes
@@ -466,6 +474,11 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       }
       y[j][0] = fmaf(dec * sc0, acc[0], rv.x);
       y[j][1] = fmaf(dec * sc1, acc[1], rv.y);
+      if (gated) {  // y * silu(z), silu(v) = v / (1 + e^-v)
+        const float z0 = bf16lo(zw[j]), z1 = bf16hi(zw[j]);
+        y[j][0] *= z0 / (1.0f + __expf(-z0));
+        y[j][1] *= z1 / (1.0f + __expf(-z1));
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage

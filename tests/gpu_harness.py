@@ -66,8 +66,10 @@ def state_close(dtype, g, o):
 class Pair:
     """Oracle + GPU replicas of one workload."""
 
-    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False):
+    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False, gate=False):
         self.fused = fused  # GPU side through rssm_flush_step instead of rssm_flush + rssm_step
+        self.gate = gate    # output gate z (seeded N(0, 1), bf16) on both sides, split path only
+        assert not (fused and gate)
         self.orc, self.wl, self.oc = orc, wl, oc
         self.ids, self.pnat = ids, pnat.copy()
         self.device = device
@@ -86,10 +88,15 @@ class Pair:
         wl, oc, gc = self.wl, self.oc, self.gc
         d = lambda a: None if a is None else dev_of(a, self.device)  # noqa: E731
         cu = d(inp.cu_seqlens)
+        z = None
+        if self.gate:
+            zf = np.random.default_rng(1000 + self.exact_state_steps + 7919 * inp.ntok).standard_normal(
+                (max(inp.ntok, 1), wl.nheads, 64)).astype(np.float32)
+            z = (zf.view(np.uint32) >> 16).astype(np.uint16)
         # oracle
         oc.flush(self.A, self.ids, self.pnat, wl.T, cu_seqlens=inp.cu_seqlens, force=force, seed=self.seed)
         y_o = oc.step(inp.x, inp.dt, self.A, inp.B, inp.C, self.D, self.dt_bias, self.ids, self.pnat, wl.T,
-                      cu_seqlens=inp.cu_seqlens)
+                      cu_seqlens=inp.cu_seqlens, z=None if z is None else z[:inp.ntok])
         oc.accept(self.ids, self.pnat, inp.accepted, wl.T, cu_seqlens=inp.cu_seqlens)
         # gpu
         out = torch.full((max(inp.ntok, 1), wl.nheads, 64), 0x7FC0, dtype=torch.int16, device=self.device)
@@ -100,7 +107,7 @@ class Pair:
             api.rssm_flush(gc, self.gA, self.gids, self.gpnat, wl.T, self.scratch, cu_seqlens=cu, force=force,
                            seed=self.seed)
             api.rssm_step(gc, d(inp.x), d(inp.dt), self.gA, d(inp.B), d(inp.C), self.gD, self.gb, self.gids,
-                          self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu)
+                          self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu, z=None if z is None else d(z))
         api.rssm_accept(gc, self.gids, self.gpnat, d(inp.accepted), wl.T, cu_seqlens=cu)
         torch.cuda.synchronize()
         y_g = out[: inp.ntok].cpu().numpy().view(np.uint16)

@@ -165,6 +165,71 @@ def test_batch_beyond_one_classification_pass(orc):
     assert int(pair.oc.error_word[0]) == 0
 
 
+@pytest.mark.parametrize("dtype", [W.F32, W.BF16, W.F16, W.I8, W.E4M3])
+def test_output_gate_tiny_all_dtypes(orc, dtype):
+    """rssm_step_gated: y * silu(z) against the oracle's gated step (every
+    state format; 8-bit units of one head at hpg = 8 / G = 1)."""
+    wl = W.config("tiny", state_dtype=dtype, prefill_live=14, ring_start_random=True)
+    gen = W.Generator(wl)
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    pair = Pair(orc, wl, oc, ids, pnat, gate=True)
+    for k in range(wl.steps):
+        pair.step(gen.step(k))
+    assert pair.oc.flush_epoch.max() >= 1
+
+
+@pytest.mark.parametrize("cfg,over", [("mamba2_decode", dict(batch=12, steps=10)),
+                                      ("eight_bit", dict(batch=8, steps=8)),
+                                      ("sweep", dict(batch=24, steps=6))])
+def test_output_gate_reduced_configs(orc, cfg, over):
+    """The gate on the readout's other unit shapes: two-head 8-bit units,
+    varlen rows with padded slot pages."""
+    wl = W.config(cfg, **over)
+    gen = W.Generator(wl)
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    pair = Pair(orc, wl, oc, ids, pnat, gate=True)
+    for k in range(wl.steps):
+        pair.step(gen.step(k))
+
+
+def test_output_gate_closed_and_halves():
+    """z = 0 gives zeros for every output; precompute + gated readout equals
+    the gated step bit for bit; z = NULL equals the ungated step."""
+    wl = W.config("mamba2_decode", batch=8, steps=1)
+    gen = W.Generator(wl)
+    A, D, dtb = gen.params()
+    ids = gen.slot_idx()
+    act = ids[ids > 0]
+    g = lambda a: dev_of(a, "cuda")  # noqa: E731
+    outs = []
+    for mode in ("zero", "gated", "halves", "plain", "none"):
+        c = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype)
+        api.rssm_init_state(c, g(gen.init_states(0, act.size)), g(act.astype(np.int32)))
+        pn = torch.zeros(ids.size, dtype=torch.int32, device="cuda")
+        sc = api.alloc_scratch(c, ids.size, wl.T)
+        inp = gen.step(0)
+        out = torch.zeros((inp.ntok, wl.nheads, 64), dtype=torch.int16, device="cuda")
+        zf = np.random.default_rng(3).standard_normal((inp.ntok, wl.nheads, 64)).astype(np.float32)
+        z = torch.zeros_like(out) if mode == "zero" else g((zf.view(np.uint32) >> 16).astype(np.uint16))
+        args = (c, g(inp.x), g(inp.dt), g(A), g(inp.B), g(inp.C), g(D), g(dtb), g(ids), pn, wl.T, out, sc)
+        if mode == "halves":
+            api.rssm_step_precompute(*args)
+            api.rssm_step_readout(*args, z=z)
+        elif mode == "plain":
+            api.rssm_step(*args)
+        elif mode == "none":
+            api.rssm_step(*args, z=None)
+        else:
+            api.rssm_step(*args, z=z)
+        torch.cuda.synchronize()
+        outs.append(out.cpu().numpy().view(np.uint16))
+    zero, gated, halves, plain, none = outs
+    assert not (zero & 0x7FFF).any()
+    assert np.array_equal(gated, halves)
+    assert np.array_equal(plain, none)
+    assert not np.array_equal(gated, plain)
+
+
 def test_bad_rows_set_error_bits_and_zero_outputs(orc):
     wl = W.config("tiny", state_dtype=W.BF16)
     gen = W.Generator(wl)
