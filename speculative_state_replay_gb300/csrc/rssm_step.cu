@@ -264,7 +264,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 // ---------------------------------------------------------------------------
 // HPU: heads per unit (2 for 8-bit states when a group has an even number of
 // heads: the unit's copies then carry twice the bytes for the same work)
-template <int DT, int TP, int HPU>
+template <int DT, int TP, int HPU, bool GATE>
 __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -450,14 +450,18 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       continue;
     }
     if (m.flags & 2) load_c_frags(reinterpret_cast<const uint16_t*>(sb + lay.c_off), g, cq, af);
-    // output gate: this lane's z pair per head, requested before the contraction
+    // output gate (GATE): this lane's z pair per head, requested before the contraction
     uint32_t zw[HPU];
-    const bool gated = a.z != nullptr && g < m.Tb;
 #pragma unroll
-    for (int j = 0; j < HPU; ++j)
-      zw[j] = gated ? *reinterpret_cast<const uint32_t*>(a.z + (static_cast<long long>(m.tok0 + g) * H + m.h + j) *
-                                                                   kDim + dout)
-                    : 0u;
+    for (int j = 0; j < HPU; ++j) zw[j] = 0u;
+    if constexpr (GATE) {
+      if (g < m.Tb) {
+#pragma unroll
+        for (int j = 0; j < HPU; ++j)
+          zw[j] = *reinterpret_cast<const uint32_t*>(a.z + (static_cast<long long>(m.tok0 + g) * H + m.h + j) * kDim +
+                                                     dout);
+      }
+    }
     float y[HPU][2];
 #pragma unroll
     for (int j = 0; j < HPU; ++j) {  // head m.h + j: rows 64 j .. of the stage's boxes
@@ -474,7 +478,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       }
       y[j][0] = fmaf(dec * sc0, acc[0], rv.x);
       y[j][1] = fmaf(dec * sc1, acc[1], rv.y);
-      if (gated) {  // y * silu(z), silu(v) = v / (1 + e^-v)
+      if constexpr (GATE) {  // y * silu(z), silu(v) = v / (1 + e^-v)
         const float z0 = bf16lo(zw[j]), z1 = bf16hi(zw[j]);
         y[j][0] *= z0 / (1.0f + __expf(-z0));
         y[j][1] *= z1 / (1.0f + __expf(-z1));
@@ -510,7 +514,7 @@ int launch_precompute(const StepArgs& a, void* stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int DT, int TP, int HPU>
+template <int DT, int TP, int HPU, bool GATE>
 static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 8
   int ns = 8, ctas = 2;
@@ -524,7 +528,7 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   const ReadLayout lay = read_layout(DT, TP, ns, HPU);
   CUtensorMap map;
   if (!encode_state_map(a.c, &map, HPU)) return cudaErrorInvalidValue;
-  auto kern = readout_kernel<DT, TP, HPU>;
+  auto kern = readout_kernel<DT, TP, HPU, GATE>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -545,8 +549,14 @@ template <int DT>
 static int launch_readout_dt(const StepArgs& a, int num_sms, cudaStream_t st) {
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
   const bool pair = k8bit && a.c.hpg % 2 == 0;
-  if (a.TP == 4) return pair ? launch_readout_t<DT, 4, 2>(a, num_sms, st) : launch_readout_t<DT, 4, 1>(a, num_sms, st);
-  return pair ? launch_readout_t<DT, 8, 2>(a, num_sms, st) : launch_readout_t<DT, 8, 1>(a, num_sms, st);
+  if (a.z) {
+    if (a.TP == 4)
+      return pair ? launch_readout_t<DT, 4, 2, true>(a, num_sms, st) : launch_readout_t<DT, 4, 1, true>(a, num_sms, st);
+    return pair ? launch_readout_t<DT, 8, 2, true>(a, num_sms, st) : launch_readout_t<DT, 8, 1, true>(a, num_sms, st);
+  }
+  if (a.TP == 4)
+    return pair ? launch_readout_t<DT, 4, 2, false>(a, num_sms, st) : launch_readout_t<DT, 4, 1, false>(a, num_sms, st);
+  return pair ? launch_readout_t<DT, 8, 2, false>(a, num_sms, st) : launch_readout_t<DT, 8, 1, false>(a, num_sms, st);
 }
 
 int launch_readout(const StepArgs& a, int num_sms, void* stream) {
