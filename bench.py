@@ -28,6 +28,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -171,7 +172,9 @@ class ClockSampler:
 
     def __init__(self, gpu_index: int):
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{gpu_index}.csv")
+        # raw samples: a temporary file unless RSSM_BENCH_OUT names a folder to keep them in
+        out_dir = os.environ.get("RSSM_BENCH_OUT") or tempfile.gettempdir()
+        self.path = os.path.join(out_dir, f"rssm_clocks_gpu{gpu_index}_{os.getpid()}.csv")
         try:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
