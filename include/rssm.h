@@ -147,10 +147,15 @@ rssm_status rssm_init_state(const rssm_cache *cache, const float *states, const 
  * and for flagged rows, per head h, with c_j = sum_{i<=j} A[h] dt'_i over the
  * live tokens (fp32, ascending), c_end = c_{p-1} (0 if p = 0):
  *   S0' = e^{c_end} S0 + sum_{j<p} e^{c_end - c_j} dt'_j x_j (outer) B_j
- * computed in fp32 in one canonical order (acc = e^{c_end} S0; then for j
- * ascending acc = fma(e^{c_end-c_j} dt'_j x_j[d], B_j[n], acc)), rounded to
- * the state format with flush epoch flush_epoch[s] + 1; then ring_start[s] =
- * (ring_start[s] + p) mod L, pnat[b] = 0, flush_epoch[s] += 1.
+ computed in fp32 in one canonical order (acc = e^{c_end} S0; then for j
+ * ascending acc = fma(e^{c_end-c_j} dt'_j x_j[d], B_j[n], acc)) -- except
+ * that 2-byte states with nearest rounding and p >= 9 are folded on the tensor
+ * cores (fp32 accumulation from e^{c_end} S0, e^{c_end-c_j} dt'_j x_j[d] split
+ * into bf16 hi + lo), which differs from the canonical order by summation
+ * order only -- rounded to the state format with flush epoch
+ * flush_epoch[s] + 1; then ring_start[s] = (ring_start[s] + p) mod L,
+ * pnat[b] = 0, flush_epoch[s] += 1.  f32, 8-bit and stochastically rounded
+ * checkpoints are therefore a function of the inputs bit for bit.
  *   A        [H] f32 (device)
  *   slot_idx [batch] i32 (device)
  *   pnat     [batch] i32 (device, in/out): live accepted tokens per row
@@ -188,7 +193,9 @@ rssm_status rssm_step(const rssm_cache *cache, const void *x, const float *dt, c
  * One decode iteration's flush and step in one call: the same results as
  * rssm_flush(cache, A, slot_idx, pnat, cu_seqlens, batch, T, force, seed)
  * followed by rssm_step(...) with the same arguments -- outputs, checkpoints
- * (bit for bit: the fold's arithmetic and quantiser are the flush's), rings,
+ * (bit for bit for f32, 8-bit and stochastically rounded states: this call
+ * folds every state in the canonical fp32 order, which rssm_flush uses for
+ * them; 2-byte states with nearest rounding within summation order), rings,
  * ring_start, pnat, flush_epoch and error bits.  The pages keep the flush and
  * the step as separate kernels ([FI] Description items 1-2: precompute +
  * persistent main; the flush in its own kernels); here one persistent kernel
