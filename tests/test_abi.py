@@ -30,7 +30,8 @@ def header_functions():
 def test_header_declares_the_entry_points():
     names = header_functions()
     for n in ("rssm_init_state", "rssm_flush", "rssm_step", "rssm_accept", "rssm_scratch_bytes",
-              "rssm_status_string", "rssm_step_precompute", "rssm_step_readout"):
+              "rssm_status_string", "rssm_step_precompute", "rssm_step_readout", "rssm_step_gated",
+              "rssm_step_readout_gated"):
         assert n in names
 
 
@@ -95,3 +96,20 @@ def test_entry_points_reject_bad_arguments_before_launching(lib):
     assert lib.rssm_flush(c, p, p, p, nul, 0, 4, 0, 0, p, 0, nul) == 0
     for s, text in [(0, b"ok"), (3, b"scratch buffer too small")]:
         assert lib.rssm_status_string(s) == text
+
+
+def test_gated_entry_points_reject_bad_arguments_before_launching(lib):
+    """rssm_step_gated / rssm_step_readout_gated: the gate pointer is checked
+    (16-byte aligned) with everything else before any launch; z = NULL and an
+    empty batch behave as the ungated calls."""
+    c = ctypes.byref(_cache())
+    nul = None
+    p = ctypes.c_void_p(1 << 20)
+    z_bad = ctypes.c_void_p((1 << 20) + 4)
+    args = [p] * 10
+    for fn in (lib.rssm_step_gated, lib.rssm_step_readout_gated):
+        assert fn(None, *([nul] * 10), 4, 4, p, nul, nul, 0, nul) == 1
+        assert fn(c, *args, 4, 4, z_bad, p, p, 1 << 30, nul) == 1  # misaligned z
+        assert fn(c, *args, 4, 5, p, p, p, 1 << 30, nul) == 2  # T > npredicted
+        assert fn(c, *args, 4, 4, p, p, p, 16, nul) == 3  # scratch too small
+        assert fn(c, *args, 0, 4, z_bad, p, p, 0, nul) == 0  # empty batch: no-op
