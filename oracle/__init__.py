@@ -51,6 +51,9 @@ class OrcCache(ctypes.Structure):
         ("B_cache", ctypes.c_void_p), ("B_slot_stride", ctypes.c_int64),
         ("dt_cache", ctypes.c_void_p), ("dt_slot_stride", ctypes.c_int64),
         ("ring_start", ctypes.c_void_p), ("flush_epoch", ctypes.c_void_p), ("error_word", ctypes.c_void_p),
+        ("read_state", ctypes.c_void_p), ("read_slot_stride", ctypes.c_int64),
+        ("read_scale", ctypes.c_void_p), ("read_scale_stride", ctypes.c_int64),
+        ("read_dtype", ctypes.c_int32),
     ]
 
 
@@ -186,7 +189,11 @@ class OracleCache:
     """
 
     def __init__(self, num_slots, nheads, ngroups, max_window, npredicted, state_dtype, rounding=NEAREST,
-                 slot_pad_bytes=0):
+                 slot_pad_bytes=0, read_dtype=None):
+        """read_dtype (I8 or E4M3): keep a separate 8-bit read checkpoint,
+        nearest-encoded from the recurrence's fp32 values at init and at every
+        flush, which the step reads S0 from (None: the step reads the
+        recurrence state)."""
         self.S, self.H, self.G = num_slots, nheads, ngroups
         self.W, self.Tmax = max_window, npredicted
         self.L = max_window + npredicted
@@ -205,6 +212,15 @@ class OracleCache:
         self.ring_start = np.zeros(num_slots, np.int32)
         self.flush_epoch = np.zeros(num_slots, np.uint32)
         self.error_word = np.zeros(1, np.uint32)
+        self.read_dtype = read_dtype
+        self.read_state = None if read_dtype is None else np.zeros((num_slots, stride(nheads * P_DIM * N_DIM, 1)), np.uint8)
+        self.read_scale = None if read_dtype is None else np.ones((num_slots, stride(nheads * P_DIM, 4)), np.float32)
+
+    def read_state_view(self):
+        return self.read_state[:, : self.H * P_DIM * N_DIM].reshape(self.S, self.H, P_DIM, N_DIM)
+
+    def read_scale_view(self):
+        return self.read_scale[:, : self.H * P_DIM].reshape(self.S, self.H, P_DIM)
 
     # logical views (no padding)
     def state_view(self):
@@ -238,6 +254,11 @@ class OracleCache:
         c.B_cache, c.B_slot_stride = _p(self.B_cache), self.B_cache.shape[1]
         c.dt_cache, c.dt_slot_stride = _p(self.dt_cache), self.dt_cache.shape[1]
         c.ring_start, c.flush_epoch, c.error_word = _p(self.ring_start), _p(self.flush_epoch), _p(self.error_word)
+        rd = getattr(self, "read_state", None)
+        if rd is not None:
+            c.read_state, c.read_slot_stride = _p(rd), rd.shape[1]
+            c.read_scale, c.read_scale_stride = _p(self.read_scale), self.read_scale.shape[1]
+            c.read_dtype = self.read_dtype
         return c
 
     def init_state(self, states, ids, seed=0):

@@ -57,6 +57,16 @@ typedef struct {
   int32_t *ring_start;                          /* [slot] */
   uint32_t *flush_epoch;                        /* [slot] */
   uint32_t *error_word;                         /* [1] */
+  /* Separate read checkpoint ([vS] Overview: an FP16 recurrence checkpoint
+   * with stochastic rounding, FP32 flush work, an 8-bit read checkpoint, BF16
+   * readout; Claims: read checkpoints use nearest encoding).  8-bit codes
+   * [slot][H][64][128] with FP32 row scales [slot][H][64], encoded to nearest
+   * from the same fp32 values as the recurrence state (at init and at every
+   * flush); the step's readout reads S0 from them.  read_state = NULL: the
+   * step reads the recurrence state itself.                                 */
+  void *read_state;  int64_t read_slot_stride;  /* elements */
+  float *read_scale; int64_t read_scale_stride;
+  int32_t read_dtype;                           /* ORC_I8 or ORC_E4M3 */
 } orc_cache;
 
 /* ------------------------------------------------------------------------- */
@@ -405,7 +415,23 @@ static void store_state_head(const orc_cache *c, int s, int h, const float *acc 
                                               : NULL;
     quantize_row(c->state_dtype, c->rounding, acc + (size_t)d * N_DIM, (uint32_t)h, (uint32_t)s, (uint32_t)d,
                  epoch, seed, (char *)c->state + off * eb, sc);
+    if (c->read_state) { /* the read checkpoint: the same fp32 row, nearest */
+      size_t roff = (size_t)s * c->read_slot_stride + ((size_t)h * P_DIM + d) * N_DIM;
+      quantize_row(c->read_dtype, ORC_NEAREST, acc + (size_t)d * N_DIM, (uint32_t)h, (uint32_t)s, (uint32_t)d,
+                   epoch, seed, (uint8_t *)c->read_state + roff,
+                   &c->read_scale[(size_t)s * c->read_scale_stride + (size_t)h * P_DIM + d]);
+    }
   }
+}
+
+/* The fp32 value of S0 element (d, n) the step's readout uses: the read
+ * checkpoint's code * scale when there is one, else the recurrence state. */
+static float readout_f32(const orc_cache *c, int s, int h, int d, int n) {
+  if (!c->read_state) return state_f32(c, s, h, d, n);
+  size_t off = (size_t)s * c->read_slot_stride + ((size_t)h * P_DIM + d) * N_DIM + n;
+  float sc = c->read_scale[(size_t)s * c->read_scale_stride + (size_t)h * P_DIM + d];
+  if (c->read_dtype == ORC_I8) return (float)((const int8_t *)c->read_state)[off] * sc;
+  return orc_e4m3_decode(((const uint8_t *)c->read_state)[off]) * sc;
 }
 
 /* ------------------------------------------------------------------------- */
@@ -446,6 +472,7 @@ static inline int slot_active(const orc_cache *c, int s) { return s >= 1 && s < 
 
 static int check_cache(const orc_cache *c) {
   if (!c || c->nheads <= 0 || c->ngroups <= 0 || c->nheads % c->ngroups) return -1;
+  if (c->read_state && (!c->read_scale || !dtype_is_8bit(c->read_dtype))) return -1;
   if (c->max_window < 0 || c->npredicted < 1 || c->max_window + c->npredicted > 256) return -1;
   return 0;
 }
@@ -647,7 +674,7 @@ int orc_step(const orc_cache *c, const uint16_t *x, const float *dt, const float
         cum[k] = cv;
       }
       for (int d = 0; d < P_DIM; ++d)
-        for (int n = 0; n < N_DIM; ++n) s0[d * N_DIM + n] = state_f32(c, s, h, d, n);
+        for (int n = 0; n < N_DIM; ++n) s0[d * N_DIM + n] = readout_f32(c, s, h, d, n);
       for (int t = 0; t < Tb; ++t) {
         size_t tok = (size_t)(tok0 + t);
         const uint16_t *ct = C + (tok * G + g) * N_DIM;
