@@ -3,23 +3,26 @@
 A step = flush + step + accept over one batch of synthetic decode inputs:
 by default (--path split) rssm_flush (classify + fold + bookkeeping) -> rssm_step
 (precompute + readout) -> rssm_accept; with --path fused, rssm_flush_step
-(flush decision + precompute, then the fused fold + readout) -> rssm_accept.  Default workload:
-Mamba-2-style decode, batch 64 of 256 slots, 128 heads, 8 groups, bf16
-checkpoints, window 16, T = 4 drafts.
+(flush decision + precompute, then the fused fold + readout) -> rssm_accept.
+Default workload: the largest batch of the decode sweep -- 1024 rows of 2049
+slots, 128 heads in 8 groups, bf16 checkpoints, window 16, 1..5 draft tokens
+per row through cu_seqlens, padded slot pages, prefilled rings.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
-                    [--config NAME] [--path fused|split] [--force-flush] [--no-e2e]
-                    [--no-cpu-baseline]
+                    [--config NAME] [--batch B] [--path fused|split] [--force-flush]
+                    [--full-window] [--no-full-window-leg] [--no-e2e] [--no-cpu-baseline]
 
 Timing: W untimed warm-up steps, then K steps, each one CUDA graph (the
 library's kernels chained by programmatic dependent launch) bracketed by CUDA
 events on the launching stream -> `value`.  A second pass replays the same
 steps as one graph per launch group with events between the groups -> the
-per-kernel durations behind `roofline`.  Between steps (outside the events) a
-1 GiB buffer is written and a 512 MiB buffer read, so every step starts with a
-cold L2 that holds no dirty lines.  Under torchrun (N > 1) every rank runs an
-independent replica (weak scaling, no data-path collective); the time is the
-max over ranks.  Prints one JSON line on rank 0.
+per-kernel durations behind `roofline`.  A last leg flushes every active row
+with a full window (pnat = max_window, set outside the events) -> the flush
+roofline.  Between steps (outside the events) a 1 GiB buffer is written and a
+512 MiB buffer read, so every step starts with a cold L2 that holds no dirty
+lines.  Under torchrun (N > 1) every rank runs an independent replica (weak
+scaling, no data-path collective); the time is the max over ranks.  Prints one
+JSON line on rank 0.
 """
 from __future__ import annotations
 
@@ -50,7 +53,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=32)
     ap.add_argument("--warmup", type=int, default=4)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--config", default="mamba2_decode")
+    ap.add_argument("--config", default="sweep")
     ap.add_argument("--batch", type=int, default=None, help="override the workload's batch")
     ap.add_argument("--force-flush", action="store_true", help="flush every active row every step")
     ap.add_argument("--full-window", action="store_true",
@@ -58,6 +61,9 @@ def parse():
                          "live tokens (pnat = max_window) and flush them all: the flush roofline run")
     ap.add_argument("--path", default="split", choices=["fused", "split"],
                     help="fused: rssm_flush_step; split: rssm_flush then rssm_step")
+    ap.add_argument("--no-full-window-leg", action="store_true",
+                    help="skip the full-window flush leg (split path only) at the end of the run")
+    ap.add_argument("--full-window-reps", type=int, default=8)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="CPU budget of the oracle baseline sample")
@@ -65,6 +71,9 @@ def parse():
     if args.full_window:  # the refill runs between steps, so there is no back-to-back leg or oracle sample
         args.no_e2e = True
         args.no_cpu_baseline = True
+        args.no_full_window_leg = True
+    if args.path == "fused":
+        args.no_full_window_leg = True
     return args
 
 
@@ -78,10 +87,12 @@ def workload(args):
 L2_BYTES = 129e6  # GB300 L2 capacity
 
 
-def profiled_traffic(kernel, workload_name):
+def profiled_traffic(kernel, workload_name, units_per_launch=None):
     """DRAM bytes per launch (dram__bytes_read + dram__bytes_write) from the
     committed ncu summary of `kernel` on this workload, if the kernel's sources
-    still hash as they did when the counters were taken; else None."""
+    still hash as they did when the counters were taken; else None.  A summary
+    taken on a smaller launch of the same workload gives its traffic per
+    (row, head) unit, scaled here to the launch's units."""
     import hashlib
     import re
 
@@ -89,7 +100,8 @@ def profiled_traffic(kernel, workload_name):
     if not os.path.exists(path):
         return None
     text = open(path).read()
-    fields = dict(re.findall(r"^\s+(traffic_bytes_per_launch|workload|sources|sources_sha256): (.+)$", text, re.M))
+    fields = dict(re.findall(r"^\s+(traffic_bytes_per_launch|traffic_bytes_per_unit|workload|sources|sources_sha256): "
+                             r"(.+)$", text, re.M))
     if fields.get("workload") != workload_name or "sources" not in fields:
         return None
     h = hashlib.sha256()
@@ -100,7 +112,11 @@ def profiled_traffic(kernel, workload_name):
         h.update(open(fp, "rb").read())
     if h.hexdigest() != fields.get("sources_sha256"):
         return None
-    return float(fields["traffic_bytes_per_launch"])
+    if "traffic_bytes_per_launch" in fields:
+        return float(fields["traffic_bytes_per_launch"])
+    if "traffic_bytes_per_unit" in fields and units_per_launch:
+        return float(fields["traffic_bytes_per_unit"]) * units_per_launch
+    return None
 
 
 def measured_peaks():
@@ -179,7 +195,7 @@ class ClockSampler:
             os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                                          "-lms", "200", "-i", str(gpu_index)], stdout=self.f,
+                                          "-lms", "100", "-i", str(gpu_index)], stdout=self.f,
                                          stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -435,6 +451,12 @@ def run_gpu(args, rank, ws, local):
             with torch.cuda.graph(g_b, stream=side, capture_error_mode="thread_local"):
                 for f in step_groups(views(dbuf_b), out_b):
                     f()
+        # the full-window flush leg: every active row flushed (force = 1)
+        g_fw = None
+        if not args.no_full_window_leg:
+            g_fw = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_fw, stream=side, capture_error_mode="thread_local"):
+                api.rssm_flush(gc, gA, gids, pnat, wl.T, scr_flush, cu_seqlens=cu, force=1, seed=wl.sr_seed)
     torch.cuda.synchronize()
     # restart the workload from its initial state
     for i in range(0, active.size, chunk):
@@ -473,6 +495,8 @@ def run_gpu(args, rank, ws, local):
     step_ms, units = [], 0
     barrier(ws)
     torch.cuda.synchronize()
+    # clocks are sampled across every timed leg (whole steps, per-kernel pass,
+    # end to end, full-window flush)
     clocks = ClockSampler(torch.cuda.current_device())
     for k in range(args.warmup, nsteps):
         refill()
@@ -489,7 +513,6 @@ def run_gpu(args, rank, ws, local):
         if u_dev != host_units(k):
             raise RuntimeError(f"step {k}: {u_dev} updates on the device, {host_units(k)} from the inputs")
         units += u_dev
-    clk = clocks.stop()
     barrier(ws)
     torch.cuda.synchronize()
 
@@ -539,11 +562,14 @@ def run_gpu(args, rank, ws, local):
     e2e = None
     if not args.no_e2e:
         n_e2e = nsteps - args.warmup
-        # pinned staging laid out like the device inputs, one per step, filled
-        # before the timed region (the host's part of a serving loop)
-        stage = [torch.empty(total, dtype=torch.uint8, pin_memory=True) for _ in range(n_e2e)]
-        for k in range(args.warmup, nsteps):
-            hv, hi = views(stage[k - args.warmup]), hin[k]
+        # pinned staging laid out like the device inputs, filled before the
+        # timed region (the host's part of a serving loop); at most 4 buffers:
+        # the timed steps take the inputs of the first n_stage timed steps in turn
+        n_stage = min(n_e2e, 4)
+        stage = [torch.empty(total, dtype=torch.uint8, pin_memory=True) for _ in range(n_stage)]
+        ks = [args.warmup + i % n_stage for i in range(n_e2e)]  # the inputs each e2e step takes
+        for j in range(n_stage):
+            hv, hi = views(stage[j]), hin[args.warmup + j]
             n = hi["ntok"]
             for key in ("x", "dt", "B", "C"):
                 hv[key][:n].copy_(hi[key])
@@ -551,18 +577,18 @@ def run_gpu(args, rank, ws, local):
             if cu is not None:
                 hv["cu"].copy_(hi["cu"])
         yh = [torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16, pin_memory=True) for _ in range(2)]
-        e2e_units = sum(host_units(k) for k in range(args.warmup, nsteps))
-        d2h_sum = sum(hin[k]["ntok"] for k in range(args.warmup, nsteps)) * wl.nheads * 64 * 2
+        e2e_units = sum(host_units(k) for k in ks)
+        d2h_sum = sum(hin[k]["ntok"] for k in ks) * wl.nheads * 64 * 2
 
         # (a) serial: H2D copy -> step -> D2H copy of y, one step at a time
         ser_ms = []
         parts = {"h2d": [], "step": [], "d2h": []}
-        for k in range(args.warmup, nsteps):
+        for i, k in enumerate(ks):
             n = hin[k]["ntok"]
             cold_l2()
             e0 = ev()
             e0.record(stream)
-            dbuf.copy_(stage[k - args.warmup], non_blocking=True)
+            dbuf.copy_(stage[i % n_stage], non_blocking=True)
             e_h = ev()
             e_h.record(stream)
             g_step.replay()
@@ -596,12 +622,12 @@ def run_gpu(args, rank, ws, local):
         e_start, e_end = ev(), ev()
         e_start.record(s_h2d)
         for i in range(n_e2e):
-            k, par = args.warmup + i, i % 2
+            k, par = ks[i], i % 2
             n = hin[k]["ntok"]
             with torch.cuda.stream(s_h2d):
                 if i >= 2:
                     s_h2d.wait_event(c_done[i - 2])  # step i-2 is done with this input set
-                dbufs[par].copy_(stage[i], non_blocking=True)
+                dbufs[par].copy_(stage[i % n_stage], non_blocking=True)
                 h_done[i].record(s_h2d)
             with torch.cuda.stream(stream):
                 stream.wait_event(h_done[i])
@@ -622,13 +648,40 @@ def run_gpu(args, rank, ws, local):
                "mode": "rssm_flush -> rssm_step -> rssm_accept on a compute stream, every step's inputs copied in "
                        "from pinned host memory (one H2D copy per step) and its y copied back (one D2H copy), "
                        "copies on two other streams overlapping the neighbouring steps' kernels; two device "
-                       "input/output sets alternate",
+                       f"input/output sets alternate; {n_stage} pinned input sets (the inputs of the first "
+                       f"{n_stage} timed steps) taken in turn",
                "l2": ("not cleared (back-to-back steps); " +
                       (f"each step's readout alone streams {read_bytes / args.steps / 1e6:.0f} MB, more than the "
                        "129 MB L2" if read_bytes / args.steps > L2_BYTES else
                        f"the step's working set ({read_bytes / args.steps / 1e6:.0f} MB read by the readout) fits in "
                        "the L2, so this leg runs warm")),
                "serial": serial}
+
+    # full-window flush: every active row holds a full window of live tokens
+    # (pnat set outside the events; the rings hold earlier appends) and flushes
+    fw = None
+    if g_fw is not None:
+        fw_ms, fw_bytes, fw_units = [], 0.0, 0
+        for r in range(args.full_window_reps):
+            pnat.masked_fill_(gids > 0, full_p)
+            cold_l2()
+            e0 = ev()
+            e0.record(stream)
+            g_fw.replay()
+            e1 = ev()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            fw_ms.append(e0.elapsed_time(e1))
+            cnt = int(scr_flush[4:8].view(torch.int32).item())
+            recs = (scr_flush[256: 256 + cnt * 32].view(torch.int32).view(cnt, 8).cpu().numpy() if cnt
+                    else np.zeros((0, 8)))
+            fw_bytes += flush_bytes(wl, [int(v[3]) for v in recs], esz)
+            fw_units += cnt * wl.nheads
+        fw = dict(ms=fw_ms, bytes=fw_bytes, units=fw_units)
+    clk = clocks.stop()
+    err = int(gc.error_word.item())
+    if err:
+        raise RuntimeError(f"device error bits set: {err:#x}")
 
     peak, peak_kind = measured_peaks()
     achieved = read_bytes / (sum(read_ms) / 1e3) / 1e9
@@ -639,6 +692,17 @@ def run_gpu(args, rank, ws, local):
                           "peak": peak, "unit": "GB/s", "frac": fold_achieved / peak,
                           "avg_us": 1e3 * statistics.mean(flush_ms),
                           "algorithmic_bytes_per_step": fold_bytes / args.steps}
+    fw_roofline = None
+    if fw is not None:
+        fw_achieved = fw["bytes"] / (sum(fw["ms"]) / 1e3) / 1e9
+        fw_roofline = {"bound": "hbm", "kernel": "flush_kernel", "achieved": fw_achieved, "peak": peak,
+                       "unit": "GB/s", "frac": fw_achieved / peak, "avg_us": 1e3 * statistics.mean(fw["ms"]),
+                       "launches": len(fw["ms"]), "live_tokens_per_row": full_p,
+                       "units_per_launch": fw["units"] / len(fw["ms"]),
+                       "algorithmic_bytes_per_launch": fw["bytes"] / len(fw["ms"]),
+                       "mode": "rssm_flush with force = 1 after every active row's pnat is set to max_window "
+                               "(outside the events), one CUDA graph per launch, cold L2"}
+    units_per_read = sum(host_units(k) for k in range(args.warmup, nsteps)) / args.steps
     res = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": t_max / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -649,14 +713,16 @@ def run_gpu(args, rank, ws, local):
                        full_window=bool(args.full_window), path=args.path),
         "roofline": {"bound": "hbm", "kernel": "step_kernel" if fused else "readout_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "traffic": None if fused or args.batch is not None else profiled_traffic("readout_kernel", wl.name),
+                     "traffic": None if fused or args.batch is not None else profiled_traffic(
+                         "readout_kernel", wl.name, units_per_read),
                      "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                      "peak_source": peak_kind, "avg_launch_us": 1e3 * statistics.mean(read_ms),
                      "algorithmic_bytes_per_launch": read_bytes / args.steps,
                      "folded_units_per_launch": fold_units / args.steps},
         "flush_roofline": flush_roofline,
+        "flush_roofline_full_window": fw_roofline,
         "e2e": e2e,
-        # per step: classify, step kernel, accept (split: flush, precompute, readout, accept)
+        # per timed step: classify, step kernel, accept (split: flush, precompute, readout, accept)
         "gpu_launches": (3 if fused else 4) * args.steps,
         "clocks": clk,
         "device_time_ms": dict({"step": statistics.mean(step_ms)},
@@ -686,6 +752,15 @@ class OracleRun:
         act = self.ids[self.ids > 0]
         self.oc.init_state(self.gen.init_states(0, act.size), act, seed=wl.sr_seed)
         self.pnat = np.zeros(self.ids.size, np.int32)
+        if wl.prefill_live:  # prefilled rings, as the GPU run starts
+            for b, s in enumerate(self.ids):
+                if s > 0:
+                    x, B, dtp, live = self.gen.ring_prefill(int(s))
+                    self.oc.x_view()[s] = x
+                    self.oc.B_view()[s] = B
+                    self.oc.dt_view()[s] = dtp
+                    self.pnat[b] = live
+        self.oc.ring_start[:] = self.gen.ring_start()
         self.k = 0
 
     def step(self):
@@ -711,7 +786,7 @@ class OracleRun:
 
 
 def cpu_baseline(wl, seconds):
-    run = OracleRun(wl)
+    run = OracleRun(wl, rows=min(wl.batch, 128))
     units, secs, steps = 0, 0.0, 0
     while secs < seconds and steps < 64:
         u, dt = run.step()

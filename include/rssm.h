@@ -34,6 +34,12 @@
  *    captured in a CUDA graph ([vAPI] selective_state_update_replayssm: the
  *    call is prepared for graph capture).  Calls on one cache must be ordered
  *    on one stream (or by the caller).
+ *  - Grid sizing: the persistent kernels size their grids for the device's
+ *    SM count; a positive integer in the environment variable RSSM_SM_LIMIT
+ *    (read at every call) caps the count they size for, to leave SMs to
+ *    concurrent work.  Work is handed out per (row, head) and each unit is
+ *    computed the same way by whichever CTA takes it, so results are the
+ *    same bits for every grid size.
  *  - Alignment: all pointers and slot strides must give 16-byte aligned rows
  *    (the kernels move rows with bulk copies); violations return
  *    RSSM_ERR_INVALID_ARGUMENT before anything is launched.
@@ -147,12 +153,12 @@ rssm_status rssm_init_state(const rssm_cache *cache, const float *states, const 
  * and for flagged rows, per head h, with c_j = sum_{i<=j} A[h] dt'_i over the
  * live tokens (fp32, ascending), c_end = c_{p-1} (0 if p = 0):
  *   S0' = e^{c_end} S0 + sum_{j<p} e^{c_end - c_j} dt'_j x_j (outer) B_j
- computed in fp32 in one canonical order (acc = e^{c_end} S0; then for j
+ * computed in fp32 in one canonical order (acc = e^{c_end} S0; then for j
  * ascending acc = fma(e^{c_end-c_j} dt'_j x_j[d], B_j[n], acc)) -- except
  * that 2-byte states with nearest rounding and p >= 9 are folded on the tensor
  * cores (fp32 accumulation from e^{c_end} S0, e^{c_end-c_j} dt'_j x_j[d] split
- * into bf16 hi + lo), which differs from the canonical order by summation
- * order only -- rounded to the state format with flush epoch
+ * into three bf16 parts that carry all 24 bits of its fp32 value), which
+ * differs from the canonical order by summation order only -- rounded to the state format with flush epoch
  * flush_epoch[s] + 1; then ring_start[s] = (ring_start[s] + p) mod L,
  * pnat[b] = 0, flush_epoch[s] += 1.  f32, 8-bit and stochastically rounded
  * checkpoints are therefore a function of the inputs bit for bit.
@@ -237,9 +243,10 @@ rssm_status rssm_flush_step_main(const rssm_cache *cache, const void *x, const f
  * The two halves of rssm_step, exposed for profiling and for callers that
  * want to place other work between them.  rssm_step == rssm_step_precompute
  * followed by rssm_step_readout with the same arguments and scratch.
- *   precompute: per (row, group): dt', cumulative A dt', C.B contraction and
- *               the decayed replay coefficients into scratch; appends B, dt'.
- *   readout:    per (row, head): streams S0 once, forms y, appends x.
+ *   precompute: per (row, group): dt', cumulative A dt', C.B contraction,
+ *               the decayed replay coefficients applied to the x rows (the
+ *               ring term) into scratch; appends B, x and dt' to the rings.
+ *   readout:    per (row, head): streams S0 once, forms y.
  */
 rssm_status rssm_step_precompute(const rssm_cache *cache, const void *x, const float *dt, const float *A,
                                  const void *B, const void *C, const float *D, const float *dt_bias,
@@ -291,6 +298,19 @@ rssm_status rssm_accept(const rssm_cache *cache, const int32_t *slot_idx, int32_
  */
 rssm_status rssm_eval_spec_math(const float *in, float *out_exp, float *out_softplus, int64_t n, void *stream);
 
+/*
+ * Diagnostics: a self-test of the bounded waits every pipeline kernel uses
+ * (a wait that gives up records RSSM_ERRBIT_TIMEOUT and the kernel returns
+ * instead of hanging; the pages have no counterpart to this call).  Launches
+ * one warp that waits on an mbarrier told to expect 256 bytes of transactions
+ * no copy will bring, with the library's wait bounded to about wait_ms
+ * milliseconds (1..10000); the wait runs out, RSSM_ERRBIT_TIMEOUT is set in
+ * *error_word (device, 4-byte aligned) and the kernel returns.  A genuine
+ * bulk copy issued next to it is waited for in full, so nothing is in flight
+ * when the kernel ends and the context stays usable.
+ */
+rssm_status rssm_selftest_wait_timeout(uint32_t *error_word, int32_t wait_ms, void *stream);
+
 const char *rssm_status_string(rssm_status status);
 
 /*
@@ -305,9 +325,11 @@ const char *rssm_status_string(rssm_status status);
  * every GPU that loads it until the process exits.  A step whose
  * rssm_scratch_bytes() exceeds that size returns RSSM_ERR_SCRATCH_TOO_SMALL
  * and launches nothing.  The call allocates and frees nothing.
- *  - The first call on a device looks up the array's device address (once
- *    per device, with that device current); make that first call before any
- *    stream capture.
+ *  - The first call in each CUDA context looks up the array's device address
+ *    (once per context, with that context current: the primary context of a
+ *    device, a context the caller made current, or the one created after a
+ *    device reset each get their own lookup); make that first call before
+ *    any stream capture.
  *  - Every call on a device shares the one array and leaves its contents
  *    behind; nothing in it needs to start at zero.  Calls whose kernels
  *    overlap on the GPU (different streams without ordering) race on the

@@ -28,7 +28,8 @@ class RssmCacheStruct(ctypes.Structure):
 
 
 EXPORTS = ("rssm_scratch_bytes", "rssm_init_state", "rssm_flush", "rssm_step", "rssm_step_precompute",
-           "rssm_step_readout", "rssm_step_gated", "rssm_step_readout_gated", "rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main", "rssm_accept", "rssm_eval_spec_math", "rssm_status_string")
+           "rssm_step_readout", "rssm_step_gated", "rssm_step_readout_gated", "rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main", "rssm_accept", "rssm_eval_spec_math", "rssm_selftest_wait_timeout",
+           "rssm_status_string")
 
 
 def load(path: str | None = None):
@@ -65,6 +66,8 @@ def load(path: str | None = None):
         lib.rssm_accept.argtypes = [cp, vp, vp, vp, vp, i32, i32, vp]
         lib.rssm_eval_spec_math.restype = ctypes.c_int
         lib.rssm_eval_spec_math.argtypes = [vp, vp, vp, i64, vp]
+        lib.rssm_selftest_wait_timeout.restype = ctypes.c_int
+        lib.rssm_selftest_wait_timeout.argtypes = [vp, i32, vp]
         lib.rssm_status_string.restype = ctypes.c_char_p
         lib.rssm_status_string.argtypes = [ctypes.c_int]
         _lib = lib

@@ -44,6 +44,26 @@ def _check(fn, status):
         raise RssmError(fn, status)
 
 
+def _check_tokens(fn, cache, slot_idx, T, cu_seqlens, **per_token):
+    """Host-side size check of the per-token tensors (no device read).
+
+    Without cu_seqlens the kernels address batch * T tokens in every per-token
+    tensor (x, dt, B, C, z, out), so each must hold at least that many token
+    rows of its row size; with cu_seqlens the token count lives on the device
+    and the caller sizes the tensors (include/rssm.h)."""
+    if cu_seqlens is not None:
+        return
+    need = slot_idx.numel() * T
+    row = {"x": cache.H * DIM, "out": cache.H * DIM, "z": cache.H * DIM, "dt": cache.H,
+           "B": cache.G * DSTATE, "C": cache.G * DSTATE}
+    for name, t in per_token.items():
+        if t is None or need == 0:
+            continue
+        if t.numel() < need * row[name]:
+            raise ValueError(f"{fn}: {name} holds {t.numel()} elements, fewer than batch * T = {need} tokens of "
+                             f"{row[name]} (pass cu_seqlens for variable-length rows)")
+
+
 class RssmCache:
     """Cache of all slots on one device: checkpoints, rings, bookkeeping.
 
@@ -135,6 +155,7 @@ def rssm_flush(cache, A, slot_idx, pnat, T, scratch, cu_seqlens=None, force=0, s
 
 
 def _step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, stream):
+    _check_tokens(fn, cache, slot_idx, T, cu_seqlens, x=x, dt=dt, B=B, C=C, out=out)
     f = getattr(_lib.load(), fn)
     _check(fn, f(cache.struct(), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
                  _ptr(slot_idx), _ptr(pnat), _ptr(cu_seqlens), slot_idx.numel(), T, _ptr(out), _ptr(scratch),
@@ -142,6 +163,7 @@ def _step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch
 
 
 def _step_gated(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, z, out, scratch, cu_seqlens, stream):
+    _check_tokens(fn, cache, slot_idx, T, cu_seqlens, x=x, dt=dt, B=B, C=C, z=z, out=out)
     f = getattr(_lib.load(), fn)
     _check(fn, f(cache.struct(), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
                  _ptr(slot_idx), _ptr(pnat), _ptr(cu_seqlens), slot_idx.numel(), T, _ptr(z), _ptr(out),
@@ -176,6 +198,7 @@ def rssm_step_readout(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out,
 
 def _flush_step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, force, seed,
                 stream):
+    _check_tokens(fn, cache, slot_idx, T, cu_seqlens, x=x, dt=dt, B=B, C=C, out=out)
     f = getattr(_lib.load(), fn)
     _check(fn, f(cache.struct(), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dt_bias),
                  _ptr(slot_idx), _ptr(pnat), _ptr(cu_seqlens), slot_idx.numel(), T, force, seed, _ptr(out),
@@ -208,3 +231,9 @@ def rssm_accept(cache, slot_idx, pnat, accepted, T, cu_seqlens=None, stream=None
 def rssm_eval_spec_math(x, out_exp=None, out_softplus=None, stream=None):
     _check("rssm_eval_spec_math", _lib.load().rssm_eval_spec_math(_ptr(x), _ptr(out_exp), _ptr(out_softplus),
                                                                   x.numel(), _stream(stream)))
+
+
+def rssm_selftest_wait_timeout(error_word, wait_ms=50, stream=None):
+    """Diagnostics: one bounded mbarrier wait that runs out (sets ERRBIT_TIMEOUT)."""
+    _check("rssm_selftest_wait_timeout", _lib.load().rssm_selftest_wait_timeout(_ptr(error_word), wait_ms,
+                                                                                _stream(stream)))

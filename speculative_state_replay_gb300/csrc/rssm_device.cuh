@@ -88,10 +88,11 @@ __device__ __forceinline__ bool mbar_try_wait_for(uint64_t* bar, uint32_t parity
       : "memory");
   return ok != 0;
 }
-// Bounded wait on a phase of an mbarrier: gives up after about two seconds.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Bounded wait on a phase of an mbarrier: gives up after `tries` suspending
+// tests of up to ~1 ms each (about two seconds by default).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint32_t tries = kWaitTries) {
   if (mbar_try_wait(bar, parity)) return true;
-  for (uint32_t i = 0; i < kWaitTries; ++i)
+  for (uint32_t i = 0; i < tries; ++i)
     if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
   return false;
 }

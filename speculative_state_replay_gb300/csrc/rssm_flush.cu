@@ -371,9 +371,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         // The fold on the tensor cores: S0' = e^{c_end} S0 + U Bm, U[d][j] =
         // w_j x_j[d] (64 x p), Bm[j][n] = B_j[n] (p x 128), as mma.sync
         // m16n8k16 with fp32 accumulation starting from e^{c_end} S0; U is
-        // split into bf16 hi + lo (16 bits of its mantissa), B is exact in
-        // bf16.  The sum order differs from the canonical fp32 chain, which
-        // only 8-bit and stochastically rounded states need bit for bit.
+        // split into three bf16 parts hi + mid + lo (each the rounded
+        // remainder of the previous: 24 significant bits, so U is carried to
+        // fp32 precision), B is exact in bf16.  Only the summation order
+        // differs from the canonical fp32 chain, which 8-bit and
+        // stochastically rounded states need bit for bit.
         // Warp: rows mr..mr+15, columns nb..nb+63 (8 tiles of 8).
         const int g = lane >> 2, cq = lane & 3, mi = lane >> 3, rr = lane & 7;
         const int mr = 16 * (warp & 3), nb = 64 * (warp >> 2);
@@ -401,23 +403,28 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t bsa = sbase + lay.b_off;
         for (int kb = 0; kb < p; kb += 16) {
           // A fragments: rows mr + g, mr + g + 8; tokens kb + 2cq (+1), kb + 2cq + 8 (+1)
-          uint32_t ahi[4], alo[4];
+          uint32_t ahi[4], amid[4], alo[4];
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh) {
-            float u0[2], u1[2];
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-              const int j = kb + 2 * cq + 8 * hh + e;
-              const float w = __shfl_sync(0xffffffffu, wj, j & 31);
-              const bool live = j < p;
-              u0[e] = live ? __fmul_rn(w, __uint_as_float(static_cast<uint32_t>(xs[j * XS + mr + g]) << 16)) : 0.0f;
-              u1[e] = live ? __fmul_rn(w, __uint_as_float(static_cast<uint32_t>(xs[j * XS + mr + g + 8]) << 16)) : 0.0f;
+            for (int rw = 0; rw < 2; ++rw) {  // A rows mr + g (rw = 0) and mr + g + 8
+              float u[2];
+#pragma unroll
+              for (int e = 0; e < 2; ++e) {
+                const int j = kb + 2 * cq + 8 * hh + e;
+                const float w = __shfl_sync(0xffffffffu, wj, j & 31);
+                u[e] = j < p ? __fmul_rn(w, __uint_as_float(static_cast<uint32_t>(xs[j * XS + mr + g + 8 * rw]) << 16))
+                             : 0.0f;
+              }
+              // u = hi + mid + lo: each part the bf16 rounding of what the
+              // previous parts leave (the remainders are exact in fp32)
+              const uint32_t hi = bf16x2_rn(u[0], u[1]);
+              const float r0 = __fsub_rn(u[0], bf16lo(hi)), r1 = __fsub_rn(u[1], bf16hi(hi));
+              const uint32_t mid = bf16x2_rn(r0, r1);
+              ahi[2 * hh + rw] = hi;
+              amid[2 * hh + rw] = mid;
+              alo[2 * hh + rw] = bf16x2_rn(__fsub_rn(r0, bf16lo(mid)), __fsub_rn(r1, bf16hi(mid)));
             }
-            const uint32_t h0 = bf16x2_rn(u0[0], u0[1]), h1 = bf16x2_rn(u1[0], u1[1]);
-            ahi[2 * hh] = h0;
-            ahi[2 * hh + 1] = h1;
-            alo[2 * hh] = bf16x2_rn(__fsub_rn(u0[0], bf16lo(h0)), __fsub_rn(u0[1], bf16hi(h0)));
-            alo[2 * hh + 1] = bf16x2_rn(__fsub_rn(u1[0], bf16lo(h1)), __fsub_rn(u1[1], bf16hi(h1)));
           }
           // B fragments, two column tiles per ldmatrix: matrices (tokens kb, kb + 8)
           // x (columns n, n + 8); token rows past p read row 0 (their U is 0)
@@ -428,8 +435,10 @@ __global__ void __launch_bounds__(kThreads, 2)
             uint32_t bv[4];
             ldmatrix_x4_trans(bv, rowa + static_cast<uint32_t>(nb + 16 * t) * 2);
             mma16816_bf16(D[2 * t], ahi, bv[0], bv[1]);
+            mma16816_bf16(D[2 * t], amid, bv[0], bv[1]);
             mma16816_bf16(D[2 * t], alo, bv[0], bv[1]);
             mma16816_bf16(D[2 * t + 1], ahi, bv[2], bv[3]);
+            mma16816_bf16(D[2 * t + 1], amid, bv[2], bv[3]);
             mma16816_bf16(D[2 * t + 1], alo, bv[2], bv[3]);
           }
         }
@@ -613,6 +622,41 @@ __global__ void spec_math_kernel(const float* in, float* oexp, float* osp, long 
     if (oexp) oexp[k] = spec_exp(v);
     if (osp) osp[k] = spec_softplus(v);
   }
+}
+
+// ---------------------------------------------------------------------------
+// self-test of the bounded mbarrier wait: one warp.  Barrier `lost` is told to
+// expect 256 bytes of transactions that no copy will bring (the state a stage
+// barrier is in when a copy it counts on never lands); its wait runs out after
+// `tries` tests and the kernel sets RSSM_ERRBIT_TIMEOUT, as the pipeline
+// kernels do.  Barrier `real` counts one genuine 256-byte bulk copy, waited
+// for in full, so no copy is in flight when the kernel returns.
+// ---------------------------------------------------------------------------
+__device__ __align__(16) unsigned char g_wait_probe_src[256];
+
+__global__ void wait_timeout_kernel(unsigned* err, unsigned tries) {
+  __shared__ __align__(16) unsigned char buf[256];
+  __shared__ __align__(8) uint64_t bars[2];
+  uint64_t* lost = &bars[0];
+  uint64_t* real = &bars[1];
+  if (threadIdx.x == 0) {
+    mbar_init(lost, 1);
+    mbar_init(real, 1);
+    fence_barrier_init();
+  }
+  __syncwarp();
+  if (threadIdx.x != 0) return;
+  mbar_arrive_expect_tx(lost, 256u);  // nothing will ever complete these bytes
+  mbar_arrive_expect_tx(real, 256u);
+  bulk_g2s(buf, g_wait_probe_src, 256u, real);
+  const bool lost_ok = mbar_wait(lost, 0u, tries);
+  const bool real_ok = mbar_wait(real, 0u);  // the genuine copy has landed
+  if (!lost_ok || !real_ok) set_error(err, RSSM_ERRBIT_TIMEOUT);
+}
+
+int launch_wait_timeout(unsigned* err, unsigned tries, void* stream) {
+  wait_timeout_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, tries);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

@@ -3,6 +3,7 @@
 // so every call is stream ordered and capturable in a CUDA graph.
 #include <cuda_runtime.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "rssm.h"
@@ -78,17 +79,25 @@ rssm_status check_cache(const rssm_cache* c, Cache* out) {
   return RSSM_OK;
 }
 
-// SM count of the current device, cached per device
+// SMs the persistent kernels size their grids for: the current device's SM
+// count (cached per device), capped by the environment variable
+// RSSM_SM_LIMIT when it holds a positive integer (read at every call, so a
+// caller can leave SMs to concurrent work; results do not depend on it)
 int num_sms() {
   static std::mutex mu;
   static int cache[64] = {0};
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
-  if (dev < 64 && cache[dev]) return cache[dev];
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-  std::lock_guard<std::mutex> g(mu);
-  if (dev < 64) cache[dev] = n;
+  int n = dev < 64 ? cache[dev] : 0;
+  if (!n) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    std::lock_guard<std::mutex> g(mu);
+    if (dev < 64) cache[dev] = n;
+  }
+  if (const char* lim = getenv("RSSM_SM_LIMIT")) {
+    const long v = strtol(lim, nullptr, 10);
+    if (v > 0 && v < n) n = static_cast<int>(v);
+  }
   return n;
 }
 
@@ -326,6 +335,13 @@ rssm_status rssm_eval_spec_math(const float* in, float* out_exp, float* out_soft
   if (n < 0 || (n > 0 && !in)) return RSSM_ERR_INVALID_ARGUMENT;
   if (n == 0) return RSSM_OK;
   return launch_spec_math(in, out_exp, out_softplus, n, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}
+
+rssm_status rssm_selftest_wait_timeout(uint32_t* error_word, int32_t wait_ms, void* stream) {
+  if (!error_word || (reinterpret_cast<uintptr_t>(error_word) & 3u)) return RSSM_ERR_INVALID_ARGUMENT;
+  if (wait_ms < 1 || wait_ms > 10000) return RSSM_ERR_INVALID_ARGUMENT;
+  return launch_wait_timeout(error_word, static_cast<unsigned>(wait_ms), stream) == cudaSuccess ? RSSM_OK
+                                                                                               : RSSM_ERR_CUDA;
 }
 
 const char* rssm_status_string(rssm_status s) {

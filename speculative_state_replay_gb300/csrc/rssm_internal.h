@@ -140,5 +140,6 @@ int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* acc
                   int T, void* stream);
 int launch_init(const InitArgs& a, void* stream);
 int launch_spec_math(const float* in, float* oexp, float* osp, long long n, void* stream);
+int launch_wait_timeout(unsigned* err, unsigned tries, void* stream);
 
 }  // namespace rssm

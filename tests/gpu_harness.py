@@ -1,9 +1,9 @@
 """Drive the CUDA library and the oracle on the same inputs (test-only).
 
 The GPU cache is a byte copy of the oracle cache; every step both run flush ->
-step -> accept on identical inputs and the results are compared.  After the
-comparison the GPU cache is overwritten with the oracle's, so each step is
-checked from identical state.
+step -> accept on identical inputs and the results are compared.  By default
+the GPU cache is then overwritten with the oracle's, so each step is checked
+from identical state; with resync=False both sides carry their own state on.
 """
 import numpy as np
 import torch
@@ -13,7 +13,15 @@ from speculative_state_replay_gb300 import workloads as W
 
 Y_ATOL, Y_RTOL = 2e-2, 1e-2          # bf16 outputs
 F32_STATE_RTOL, F32_STATE_ATOL = 1e-4, 1e-6
-HALF_STATE_ATOL, HALF_STATE_RTOL = 2e-2, 1e-2
+# 2-byte checkpoints: at most one unit in the last place of the oracle's code
+# (the GPU's tensor-core fold differs from the oracle's fp32 chain by
+# summation order only, which can move a value across one rounding boundary),
+# or within 2^-20 of it: near zero, where the fold's terms cancel, the fp32
+# accumulators of the two orders still agree to ~1e-7 absolute while one unit
+# of the code is smaller than that.  The slack only matters below |v| = 2^-12
+# (bf16) or 2^-9 (f16).  One folded token changes a checkpoint by ~1e-2.
+HALF_STATE_ULPS = 1
+HALF_STATE_ABS = 2.0 ** -20
 
 
 def dev_of(a, device):
@@ -53,22 +61,55 @@ def sync_gpu_from(gc, oc):
         dst.copy_(dev_of(src, dst.device).view(dst.dtype))
 
 
-def state_close(dtype, g, o):
-    """Checkpoint comparison: bit-exact for 8-bit codes, tolerance otherwise."""
+def half_decode(dtype, bits):
+    b = np.asarray(bits, np.uint16)
+    return bf16_f32(b) if dtype == W.BF16 else b.view(np.float16).astype(np.float32)
+
+
+def code_distance(bits_a, bits_b):
+    """Distance in units in the last place between two 16-bit sign-magnitude
+    codes (bf16 or f16), through the order-preserving map code -> integer
+    (+0 and -0 both map to 0)."""
+    def ordinal(b):
+        b = np.asarray(b, np.uint16).astype(np.int64)
+        mag = b & 0x7FFF
+        return np.where(b & 0x8000, -mag, mag)
+
+    return np.abs(ordinal(bits_a) - ordinal(bits_b))
+
+
+def half_state_close(dtype, g, o, ulps=HALF_STATE_ULPS, abs_slack=HALF_STATE_ABS):
+    """Per element: code distance <= ulps, or decoded difference <= abs_slack."""
+    g = np.asarray(g).view(np.uint16)
+    o = np.asarray(o).view(np.uint16)
+    near = code_distance(g, o) <= ulps
+    if near.all():
+        return True
+    diff = np.abs(half_decode(dtype, g).astype(np.float64) - half_decode(dtype, o).astype(np.float64))
+    return bool(np.all(near | (diff <= abs_slack)))
+
+
+def state_close(dtype, g, o, ulps=HALF_STATE_ULPS):
+    """Checkpoint comparison: bit-exact for 8-bit codes, 1e-4 relative for f32,
+    `ulps` units in the last place (with the near-zero slack) for bf16/f16."""
     if dtype in (W.I8, W.E4M3):
         return np.array_equal(g, o)
     if dtype == W.F32:
         return bool(np.all(np.abs(g - o) <= F32_STATE_RTOL * np.abs(o) + F32_STATE_ATOL))
-    f = bf16_f32 if dtype == W.BF16 else (lambda b: np.asarray(b, np.uint16).view(np.float16).astype(np.float32))
-    return bool(np.allclose(f(g), f(o), atol=HALF_STATE_ATOL, rtol=HALF_STATE_RTOL))
+    return half_state_close(dtype, g, o, ulps=ulps)
 
 
 class Pair:
     """Oracle + GPU replicas of one workload."""
 
-    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False, gate=False):
+    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False, gate=False, resync=True):
         self.fused = fused  # GPU side through rssm_flush_step instead of rssm_flush + rssm_step
         self.gate = gate    # output gate z (seeded N(0, 1), bf16) on both sides, split path only
+        # resync: after each comparison the GPU cache is overwritten with the
+        # oracle's; without it both sides carry their own checkpoints on (2-byte
+        # checkpoints folded on the tensor cores may then drift by one more unit
+        # in the last place, decayed, at later flushes)
+        self.resync = resync
         assert not (fused and gate)
         self.orc, self.wl, self.oc = orc, wl, oc
         self.ids, self.pnat = ids, pnat.copy()
@@ -127,11 +168,71 @@ class Pair:
             g = host_of(getattr(gc, name), getattr(oc, name))
             assert np.array_equal(g, getattr(oc, name)), name
         gs = host_of(gc.state, oc.state)
-        assert state_close(oc.state_dtype, gs, oc.state), "checkpoint"
+        assert state_close(oc.state_dtype, gs, oc.state, ulps=1 if self.resync else 2), "checkpoint"
         if oc.state_dtype in (W.I8, W.E4M3):
             assert np.array_equal(host_of(gc.scale, oc.scale), oc.scale), "scales"
         if np.array_equal(gs, oc.state):
             self.exact_state_steps += 1
-        # continue from identical state
-        sync_gpu_from(gc, oc)
-        self.gpnat.copy_(dev_of(self.pnat, self.device))
+        if self.resync:  # continue from identical state
+            sync_gpu_from(gc, oc)
+            self.gpnat.copy_(dev_of(self.pnat, self.device))
+
+
+def init_gpu_cache_like_bench(wl, gen, ids, device="cuda"):
+    """A full-size GPU cache initialised the way bench.py initialises it:
+    every active row's FP32 state through rssm_init_state (16 rows a call),
+    prefilled rings, the workload's ring starts.  Returns (cache, pnat0)."""
+    gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
+                       wl.rounding, device=device, slot_pad_bytes=wl.slot_pad_bytes)
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+    active = ids[ids > 0]
+    for i in range(0, active.size, 16):
+        sl = active[i:i + 16]
+        api.rssm_init_state(gc, t(gen.init_states(i, sl.size)), t(sl.astype(np.int32)), seed=wl.sr_seed)
+    pnat0 = np.zeros(ids.size, np.int32)
+    if wl.prefill_live:
+        for b, s in enumerate(ids):
+            if s > 0:
+                x, B, dtp, live = gen.ring_prefill(int(s))
+                gc.x_view()[s] = t(x.view(np.int16))
+                gc.B_view()[s] = t(B.view(np.int16))
+                gc.dt_view()[s] = t(dtp)
+                pnat0[b] = live
+    gc.ring_start.copy_(t(gen.ring_start()))
+    torch.cuda.synchronize()
+    return gc, pnat0
+
+
+def oracle_cache_for_rows(orc, wl, gen, ids, rows):
+    """An oracle cache holding only the given rows of a full-size workload,
+    initialised exactly as init_gpu_cache_like_bench initialises them (rows
+    are independent, so the oracle can follow a sample of them)."""
+    oc = orc.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
+                         wl.rounding, slot_pad_bytes=wl.slot_pad_bytes)
+    act_pos = np.cumsum(ids > 0) - 1  # index of each row among the active rows
+    for b in rows:
+        s = int(ids[b])
+        if s <= 0:
+            continue
+        oc.init_state(gen.init_states(int(act_pos[b]), 1), np.array([s], np.int32), seed=wl.sr_seed)
+        if wl.prefill_live:
+            x, B, dtp, _ = gen.ring_prefill(s)
+            oc.x_view()[s] = x
+            oc.B_view()[s] = B
+            oc.dt_view()[s] = dtp
+    oc.ring_start[:] = gen.ring_start()
+    return oc
+
+
+def token_rows(inp, rows, T):
+    """Token indices of `rows` in a step's packed inputs and the cu_seqlens of
+    those rows packed alone (None without varlen)."""
+    if inp.cu_seqlens is None:
+        tok = (np.asarray(rows)[:, None] * T + np.arange(T)[None]).reshape(-1)
+        return tok, None
+    cu = inp.cu_seqlens
+    parts = [np.arange(cu[b], cu[b + 1]) for b in rows]
+    lens = np.array([p.size for p in parts], np.int32)
+    sub = np.zeros(len(rows) + 1, np.int32)
+    sub[1:] = np.cumsum(lens)
+    return np.concatenate(parts).astype(np.int64), sub

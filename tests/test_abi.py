@@ -113,3 +113,37 @@ def test_gated_entry_points_reject_bad_arguments_before_launching(lib):
         assert fn(c, *args, 4, 5, p, p, p, 1 << 30, nul) == 2  # T > npredicted
         assert fn(c, *args, 4, 4, p, p, p, 16, nul) == 3  # scratch too small
         assert fn(c, *args, 0, 4, z_bad, p, p, 0, nul) == 0  # empty batch: no-op
+
+
+def test_binding_refuses_token_tensors_shorter_than_batch_times_T():
+    """Without cu_seqlens the kernels address batch * T tokens in every
+    per-token tensor: the binding checks the sizes on the host (no device read)
+    and raises before calling the library."""
+    import torch
+
+    from speculative_state_replay_gb300 import api
+
+    c = api.RssmCache(5, 8, 1, 16, 4, api.BF16, device="cpu")
+    batch, T = 3, 4
+    ids = torch.zeros(batch, dtype=torch.int32)
+    f = torch.zeros(8)
+    x = torch.zeros((batch * T - 1, 8, 64), dtype=torch.int16)  # one token short
+    dt = torch.zeros((batch * T, 8))
+    B = torch.zeros((batch * T, 1, 128), dtype=torch.int16)
+    out = torch.zeros((batch * T, 8, 64), dtype=torch.int16)
+    scratch = torch.zeros(1 << 16, dtype=torch.uint8)
+    for fn in (api.rssm_step, api.rssm_step_precompute, api.rssm_step_readout, api.rssm_flush_step):
+        with pytest.raises(ValueError, match="x holds"):
+            fn(c, x, dt, f, B, B, f, f, ids, ids, T, out, scratch)
+    with pytest.raises(ValueError, match="out holds"):
+        api.rssm_step(c, out, dt, f, B, B, f, f, ids, ids, T, x, scratch)
+    with pytest.raises(ValueError, match="z holds"):
+        api.rssm_step(c, out, dt, f, B, B, f, f, ids, ids, T, out, scratch, z=x)
+
+
+def test_wait_selftest_rejects_bad_arguments(lib):
+    assert lib.rssm_selftest_wait_timeout(None, 50, None) == 1
+    p = ctypes.c_void_p(1 << 20)
+    assert lib.rssm_selftest_wait_timeout(p, 0, None) == 1
+    assert lib.rssm_selftest_wait_timeout(p, 20000, None) == 1
+    assert lib.rssm_selftest_wait_timeout(ctypes.c_void_p((1 << 20) + 2), 50, None) == 1

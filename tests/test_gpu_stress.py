@@ -1,0 +1,211 @@
+"""CUDA library vs CPU oracle over long runs, back-to-back launches under
+contention, and across runs and grid sizes (needs a GPU).
+
+* No re-synchronisation: both sides carry their own caches through 20 decode
+  steps; every step's outputs at the bf16 tolerance, 8-bit codes and scales,
+  f32 and stochastically rounded checkpoints, rings and bookkeeping bit for
+  bit, 2-byte checkpoints folded on the tensor cores within two units in the
+  last place (a summation-order difference folded into a later flush, decayed,
+  can add one rounding boundary).
+* Contention: the decode steps run back to back -- all steps of a round in one
+  CUDA graph (kernels chained by programmatic dependent launch, also across
+  steps) or as eager launches -- while a second stream in the same process
+  keeps the SMs busy with matmuls, bandwidth-bound kernels or many short
+  kernels.  The FlashInfer PR #3975 commit note on its PDL race describes the
+  hazard this looks for: a read placed before the grid-dependency wait that is
+  correct on an idle GPU and corrupt under a concurrent load.
+* Determinism: identical bits over two runs and over several grid sizes
+  (RSSM_SM_LIMIT), since each (row, head) is computed the same way by
+  whichever CTA takes it.
+"""
+import numpy as np
+import pytest
+import torch
+
+from speculative_state_replay_gb300 import api
+from speculative_state_replay_gb300 import workloads as W
+from tests.gpu_harness import Pair, bf16_f32, dev_of, gpu_cache_from, host_of, state_close
+from tests.harness import oracle_cache, run_oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from speculative_state_replay_gb300 import _lib, build
+
+    build.build()
+    _lib.load()
+
+
+@pytest.mark.parametrize("cfg,over", [
+    ("mamba2_decode", dict(batch=16, prefill_live=14, ring_start_random=True)),  # bf16, tensor-core folds
+    ("large_batch", dict(batch=16, prefill_live=14)),                           # fp16, T = 7, wraparound
+    ("eight_bit", dict(batch=8)),                                                # int8 nearest
+    ("eight_bit", dict(batch=8, state_dtype=W.E4M3, rounding=W.STOCHASTIC, sr_seed=7)),
+    ("tiny", dict(prefill_live=14, ring_start_random=True)),                    # f32
+    ("sweep", dict(batch=16)),                                                   # varlen, padded pages
+    ("mamba2_decode", dict(batch=16, rounding=W.STOCHASTIC, sr_seed=3, prefill_live=14)),
+])
+def test_twenty_steps_without_resync(orc, cfg, over):
+    wl = W.config(cfg, steps=20, **over)
+    gen = W.Generator(wl)
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    pair = Pair(orc, wl, oc, ids, pnat, resync=False)
+    for k in range(wl.steps):
+        pair.step(gen.step(k))
+    assert pair.oc.flush_epoch.max() >= 2
+    tensor_core_fold = wl.state_dtype in (W.BF16, W.F16) and wl.rounding == W.NEAREST
+    if not tensor_core_fold:  # the canonical fold: the checkpoints themselves bit for bit
+        assert pair.exact_state_steps == wl.steps
+
+
+# --------------------------------------------------------------------------- #
+# back to back under contention
+# --------------------------------------------------------------------------- #
+class Burner:
+    """Bounded concurrent load on its own stream (a few tens of ms)."""
+
+    def __init__(self, device):
+        self.stream = torch.cuda.Stream(device=device)
+        g = torch.Generator(device=device).manual_seed(11)
+        self.a = torch.randn((4096, 4096), generator=g, device=device, dtype=torch.bfloat16)
+        self.big = torch.zeros(1 << 27, device=device, dtype=torch.float32)  # 512 MB
+        self.small = torch.zeros(1 << 16, device=device, dtype=torch.float32)
+
+    def start(self, kind):
+        with torch.cuda.stream(self.stream):
+            if kind == "matmul":
+                for _ in range(150):
+                    torch.matmul(self.a, self.a)
+            elif kind == "bandwidth":
+                for _ in range(60):
+                    self.big.add_(1.0)
+            else:  # many short kernels
+                for _ in range(3000):
+                    self.small.mul_(1.0)
+
+
+def _device_inputs(inp, dev):
+    d = lambda a: None if a is None else dev_of(a, dev)  # noqa: E731
+    return dict(x=d(inp.x), dt=d(inp.dt), B=d(inp.B), C=d(inp.C), acc=d(inp.accepted), cu=d(inp.cu_seqlens),
+                ntok=inp.ntok)
+
+
+@pytest.mark.parametrize("dtype,rounding", [(W.BF16, W.NEAREST), (W.E4M3, W.STOCHASTIC)])
+def test_steps_back_to_back_under_contention(orc, dtype, rounding):
+    dev = "cuda"
+    wl = W.config("mamba2_decode", batch=32, state_dtype=dtype, rounding=rounding, sr_seed=5, prefill_live=14,
+                  ring_start_random=True)
+    rounds = [("graph", "matmul"), ("eager", "bandwidth"), ("graph", "short"), ("graph", "matmul")]
+    per_round = 12
+    nsteps = per_round * len(rounds)
+    gen = W.Generator(wl)
+    A, D, dtb = gen.params()
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    gc = gpu_cache_from(oc, dev)
+    inputs = [gen.step(k) for k in range(nsteps)]
+    # the oracle's sequence
+    pnat_o = pnat.copy()
+    ys_o = [run_oracle_step(oc, wl, (A, D, dtb), ids, pnat_o, inputs[k]) for k in range(nsteps)]
+
+    g = lambda a: dev_of(a, dev)  # noqa: E731
+    gA, gD, gb, gids, gpnat = g(A), g(D), g(dtb), g(ids), g(pnat)
+    dins = [_device_inputs(i, dev) for i in inputs]
+    outs = [torch.full((i.ntok, wl.nheads, 64), 0x7FC0, dtype=torch.int16, device=dev) for i in inputs]
+    scratch = api.alloc_scratch(gc, ids.size, wl.T)
+
+    def launch(k, cache, pn, sc):
+        d = dins[k]
+        api.rssm_flush(cache, gA, gids, pn, wl.T, sc, cu_seqlens=d["cu"], seed=wl.sr_seed)
+        api.rssm_step(cache, d["x"], d["dt"], gA, d["B"], d["C"], gD, gb, gids, pn, wl.T, outs[k], sc,
+                      cu_seqlens=d["cu"])
+        api.rssm_accept(cache, gids, pn, d["acc"], wl.T, cu_seqlens=d["cu"])
+
+    # warm-up launches on a throwaway copy (kernel attributes, module loading), then capture
+    warm = gpu_cache_from(oc, dev)
+    launch(0, warm, gpnat.clone(), api.alloc_scratch(warm, ids.size, wl.T))
+    torch.cuda.synchronize()
+    graphs = {}
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for r, (mode, _) in enumerate(rounds):
+            if mode == "graph":
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr, stream=side, capture_error_mode="thread_local"):
+                    for k in range(r * per_round, (r + 1) * per_round):
+                        launch(k, gc, gpnat, scratch)
+                graphs[r] = gr
+    torch.cuda.synchronize()
+    burner = Burner(dev)
+    main = torch.cuda.current_stream()
+    for r, (mode, load) in enumerate(rounds):
+        burner.start(load)
+        if mode == "graph":
+            graphs[r].replay()
+        else:
+            for k in range(r * per_round, (r + 1) * per_round):
+                launch(k, gc, gpnat, scratch)
+        main.wait_stream(burner.stream)  # the next round starts on a fresh load
+    torch.cuda.synchronize()
+
+    for k in range(nsteps):
+        yg = outs[k].cpu().numpy().view(np.uint16)
+        a, b = bf16_f32(yg), bf16_f32(ys_o[k])
+        bad = ~(np.abs(a - b) <= 2e-2 + 1e-2 * np.abs(b))
+        assert not bad.any(), (k, np.argwhere(bad)[:4].tolist())
+    assert np.array_equal(gpnat.cpu().numpy(), pnat_o)
+    for name in ("x_cache", "B_cache", "dt_cache", "ring_start", "flush_epoch", "error_word"):
+        o = getattr(oc, name)
+        assert np.array_equal(host_of(getattr(gc, name), o), o), name
+    gs = host_of(gc.state, oc.state)
+    if rounding == W.STOCHASTIC:
+        assert np.array_equal(gs, oc.state)
+        assert np.array_equal(host_of(gc.scale, oc.scale), oc.scale)
+    else:
+        assert state_close(dtype, gs, oc.state, ulps=2)
+    assert oc.flush_epoch.max() >= 3
+
+
+# --------------------------------------------------------------------------- #
+# determinism
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("dtype,rounding", [(W.F32, W.NEAREST), (W.BF16, W.NEAREST), (W.F16, W.STOCHASTIC),
+                                            (W.I8, W.NEAREST), (W.E4M3, W.STOCHASTIC)])
+def test_same_bits_across_runs_and_grid_sizes(orc, dtype, rounding, monkeypatch):
+    wl = W.config("mamba2_decode", batch=24, steps=10, state_dtype=dtype, rounding=rounding, sr_seed=7,
+                  prefill_live=14, ring_start_random=True)
+    gen = W.Generator(wl)
+    A, D, dtb = gen.params()
+    oc, ids, pnat = oracle_cache(orc, wl, gen)
+    inputs = [gen.step(k) for k in range(wl.steps)]
+    g = lambda a: dev_of(a, "cuda")  # noqa: E731
+    runs = []
+    for limit in (None, None, "37", "3"):
+        if limit is None:
+            monkeypatch.delenv("RSSM_SM_LIMIT", raising=False)
+        else:
+            monkeypatch.setenv("RSSM_SM_LIMIT", limit)
+        gc = gpu_cache_from(oc)
+        gp = g(pnat)
+        gA, gD, gb, gids = g(A), g(D), g(dtb), g(ids)
+        scratch = api.alloc_scratch(gc, ids.size, wl.T)
+        ys = []
+        for k, inp in enumerate(inputs):
+            out = torch.empty((inp.ntok, wl.nheads, 64), dtype=torch.int16, device="cuda")
+            api.rssm_flush(gc, gA, gids, gp, wl.T, scratch, force=1 if k == 4 else 0, seed=wl.sr_seed)
+            api.rssm_step(gc, g(inp.x), g(inp.dt), gA, g(inp.B), g(inp.C), gD, gb, gids, gp, wl.T, out, scratch)
+            api.rssm_accept(gc, gids, gp, g(inp.accepted), wl.T)
+            ys.append(out)
+        torch.cuda.synchronize()
+        runs.append(dict(y=torch.stack(ys).cpu(), pnat=gp.cpu(),
+                         **{n: getattr(gc, n).cpu() for n in ("state", "scale", "x_cache", "B_cache", "dt_cache",
+                                                               "ring_start", "flush_epoch", "error_word")}))
+    monkeypatch.delenv("RSSM_SM_LIMIT", raising=False)
+    for r in runs[1:]:
+        for name, v in runs[0].items():
+            assert torch.equal(v, r[name]), name
+    assert int(runs[0]["flush_epoch"].max()) >= 2
