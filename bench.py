@@ -280,10 +280,13 @@ def fused_bytes(wl, rows_rec, esz):
 
 def flush_bytes(wl, recs, esz):
     """Algorithmic bytes of one fold launch: S0 read + write (+ scales), live x
-    and B rows per flagged (row, head)."""
+    and B rows per flagged (row, head); with a separate read checkpoint also
+    its 8-bit codes and row scales written."""
     total = 0
+    rd = 64 * 128 + 256 if wl.read_dtype is not None else 0
     for p in recs:
-        total += wl.nheads * (2 * 64 * 128 * esz + (512 if esz == 1 else 0) + p * 128 + p * 256 / wl.hpg + p * 4)
+        total += wl.nheads * (2 * 64 * 128 * esz + (512 if esz == 1 else 0) + p * 128 + p * 256 / wl.hpg + p * 4
+                              + rd)
     return total
 
 
@@ -300,9 +303,11 @@ def run_gpu(args, rank, ws, local):
     A, D, dt_bias = gen.params()
     ids = gen.slot_idx()
     esz = W.DTYPE_BYTES[wl.state_dtype]
+    # the readout streams the read checkpoint when there is one
+    read_esz = esz if wl.read_dtype is None else W.DTYPE_BYTES[wl.read_dtype]
 
     gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
-                       wl.rounding, device=dev, slot_pad_bytes=wl.slot_pad_bytes)
+                       wl.rounding, device=dev, slot_pad_bytes=wl.slot_pad_bytes, read_dtype=wl.read_dtype)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(dev)  # noqa: E731
     active = ids[ids > 0]
     chunk = 16
@@ -539,7 +544,7 @@ def run_gpu(args, rank, ws, local):
             read_bytes += fused_bytes(wl, [tuple(int(v) for v in r) for r in rr], esz)
             fold_units += int(((rr[:, 5] & 2) != 0).sum()) * wl.nheads
         else:
-            read_bytes += algorithmic_bytes(wl, [tuple(r[:6]) for r in rr], None, esz)
+            read_bytes += algorithmic_bytes(wl, [tuple(r[:6]) for r in rr], None, read_esz)
             cnt = int(scr_flush[4:8].view(torch.int32).item())
             recs = (scr_flush[256: 256 + cnt * 32].view(torch.int32).view(cnt, 8).cpu().numpy() if cnt
                     else np.zeros((0, 8)))
@@ -748,7 +753,8 @@ class OracleRun:
         ids = self.gen.slot_idx()
         self.ids = ids[:rows] if rows is not None and rows < ids.size else ids
         self.oc = oracle.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted,
-                                     wl.state_dtype, wl.rounding, slot_pad_bytes=wl.slot_pad_bytes)
+                                     wl.state_dtype, wl.rounding, slot_pad_bytes=wl.slot_pad_bytes,
+                                     read_dtype=wl.read_dtype)
         act = self.ids[self.ids > 0]
         self.oc.init_state(self.gen.init_states(0, act.size), act, seed=wl.sr_seed)
         self.pnat = np.zeros(self.ids.size, np.int32)

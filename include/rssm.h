@@ -124,6 +124,21 @@ typedef struct {
   int32_t *ring_start; /* [slot]: physical position of live token 0 */
   uint32_t *flush_epoch; /* [slot]: number of flushes since init (random counter) */
   uint32_t *error_word;  /* [1]: sticky RSSM_ERRBIT_* bits */
+  /* Optional separate read checkpoint ([vS] Overview: an FP16 recurrence
+   * checkpoint with stochastic rounding, FP32 flush work, an FP8 read
+   * checkpoint, BF16 readout; Claims: read checkpoints use nearest
+   * encoding).  8-bit codes of read_dtype with one FP32 scale per (slot,
+   * head, d) row, written with nearest rounding from the same fp32 values as
+   * the recurrence state `state` -- the FP32 prefill states in
+   * rssm_init_state, the fold's fp32 accumulators in rssm_flush -- and read
+   * by rssm_step's readout in place of `state`.  With a read checkpoint every
+   * fold takes the canonical fp32 order, so both encodings are functions of
+   * the inputs bit for bit.  read_state = NULL: no read checkpoint (the
+   * step reads `state`); the other read fields are then ignored.
+   * rssm_flush_step does not take a read checkpoint (RSSM_ERR_UNSUPPORTED). */
+  void *read_state;    int64_t read_slot_stride;       /* 8-bit [slot][H][64][128] */
+  float *read_scale;   int64_t read_scale_slot_stride; /* f32 [slot][H][64] */
+  int32_t read_dtype;                                  /* RSSM_I8 or RSSM_E4M3 */
 } rssm_cache;
 
 /*

@@ -24,6 +24,9 @@ class RssmCacheStruct(ctypes.Structure):
         ("B_cache", ctypes.c_void_p), ("B_slot_stride", ctypes.c_int64),
         ("dt_cache", ctypes.c_void_p), ("dt_slot_stride", ctypes.c_int64),
         ("ring_start", ctypes.c_void_p), ("flush_epoch", ctypes.c_void_p), ("error_word", ctypes.c_void_p),
+        ("read_state", ctypes.c_void_p), ("read_slot_stride", ctypes.c_int64),
+        ("read_scale", ctypes.c_void_p), ("read_scale_slot_stride", ctypes.c_int64),
+        ("read_dtype", ctypes.c_int32),
     ]
 
 

@@ -69,10 +69,12 @@ class RssmCache:
 
     Every tensor is 2-D [slot, slot_stride]; `slot_pad_bytes` adds padding
     after each slot's page.  bf16/f16 data is held as raw 16-bit words.
+    `read_dtype` (I8 or E4M3) adds a separate 8-bit read checkpoint
+    (`read_state`, `read_scale`) that the step's readout reads S0 from.
     """
 
     def __init__(self, num_slots, nheads, ngroups, max_window, npredicted, state_dtype, rounding=NEAREST,
-                 device="cuda", slot_pad_bytes=0):
+                 device="cuda", slot_pad_bytes=0, read_dtype=None):
         self.S, self.H, self.G = num_slots, nheads, ngroups
         self.W, self.Tmax = max_window, npredicted
         self.L = max_window + npredicted
@@ -93,6 +95,12 @@ class RssmCache:
         self.ring_start = z((num_slots,), torch.int32)
         self.flush_epoch = z((num_slots,), torch.int32)
         self.error_word = z((1,), torch.int32)
+        self.read_dtype = read_dtype
+        if read_dtype is not None:
+            self.read_state = z((num_slots, stride(nheads * DIM * DSTATE, 1)), STATE_TORCH[read_dtype])
+            self.read_scale = torch.ones((num_slots, stride(nheads * DIM, 4)), dtype=torch.float32, device=dev)
+        else:
+            self.read_state = self.read_scale = None
         self._struct = None
 
     def struct(self):
@@ -110,6 +118,10 @@ class RssmCache:
             c.ring_start = self.ring_start.data_ptr()
             c.flush_epoch = self.flush_epoch.data_ptr()
             c.error_word = self.error_word.data_ptr()
+            if self.read_state is not None:
+                c.read_state, c.read_slot_stride = self.read_state.data_ptr(), self.read_state.shape[1]
+                c.read_scale, c.read_scale_slot_stride = self.read_scale.data_ptr(), self.read_scale.shape[1]
+                c.read_dtype = self.read_dtype
             self._struct = c
         return ctypes.byref(self._struct)
 

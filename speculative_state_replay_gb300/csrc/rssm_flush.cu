@@ -153,8 +153,23 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int 
 }
 
 // smallest live prefix folded on the tensor cores (2-byte states, nearest
-// rounding); shorter prefixes take the CUDA-core fold (K is padded to 16)
+// rounding, no read checkpoint); shorter prefixes take the CUDA-core fold (K
+// is padded to 16)
 constexpr int kMmaMinP = 9;
+
+// The separate read checkpoint of head h in slot s: the lane's 4 x 8 fp32
+// values (the ones the recurrence state was just rounded from) encoded to the
+// 8-bit read format with nearest rounding and per-row scales
+__device__ __forceinline__ void store_read_checkpoint(const Cache& c, float (&acc)[4][8], int r0, int c0, int lane,
+                                                      int s, int h) {
+  uint8_t* rs = static_cast<uint8_t*>(c.read_state) +
+                static_cast<long long>(s) * c.read_stride + static_cast<long long>(h) * kHeadElems;
+  float* rsc = c.read_scale + static_cast<long long>(s) * c.read_scale_stride + h * kDim;
+  if (c.read_dtype == RSSM_I8)
+    quantize_store<RSSM_I8>(acc, r0, c0, lane, rs, rsc, RSSM_ROUND_NEAREST, 0u, 0u, 0u, 0ull);
+  else
+    quantize_store<RSSM_E4M3>(acc, r0, c0, lane, rs, rsc, RSSM_ROUND_NEAREST, 0u, 0u, 0u, 0ull);
+}
 
 // Classification, fold, requantisation and bookkeeping of rssm_flush in one
 // kernel.  Every CTA classifies all rows (two passes over slot_idx, pnat and
@@ -282,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * L * kDim;
       const uint16_t* bg = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
       // units folded on the tensor cores take their x and B rows padded; the rest as stored
-      const bool mma_unit = k2B && c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP;
+      const bool mma_unit = k2B && c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP && !c.read_state;
       if (lane == 0) {
         const uint32_t bytes =
             lay.s0_bytes + (k8bit ? 256u : 0u) + (mma_unit ? 0u : static_cast<uint32_t>(p) * (kDim * 2 + kDstate * 2));
@@ -367,7 +382,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const float wj = lane < p ? __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj) : 0.0f;
     const float decay = spec_exp(c_end);
     if constexpr (k2B) {
-      if (c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP) {
+      if (c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP && !c.read_state) {
         // The fold on the tensor cores: S0' = e^{c_end} S0 + U Bm, U[d][j] =
         // w_j x_j[d] (64 x p), Bm[j][n] = B_j[n] (p x 128), as mma.sync
         // m16n8k16 with fp32 accumulation starting from e^{c_end} S0; U is
@@ -532,6 +547,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     float* head_scale = k8bit ? c.scale + static_cast<long long>(m.s) * c.scale_stride + m.h * kDim : nullptr;
     quantize_store<DT>(accf, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(m.h),
                        static_cast<uint32_t>(m.s), m.epoch, a.seed);
+    if (c.read_state) store_read_checkpoint(c, accf, r0, c0, lane, m.s, m.h);
   }
   }
 
@@ -564,6 +580,7 @@ __global__ void __launch_bounds__(kConsumerThreads) init_quant_kernel(InitArgs a
       (DT == RSSM_I8 || DT == RSSM_E4M3) ? c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim : nullptr;
   quantize_store<DT>(acc, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(h),
                      static_cast<uint32_t>(s), 0u, a.seed);
+  if (c.read_state) store_read_checkpoint(c, acc, r0, c0, lane, s, h);
 }
 
 __global__ void __launch_bounds__(256) init_clear_kernel(InitArgs a) {

@@ -51,6 +51,13 @@ rssm_status check_cache(const rssm_cache* c, Cache* out) {
   if (c->x_slot_stride < H * L * kDim || (c->x_slot_stride * 2) % 16) return RSSM_ERR_INVALID_ARGUMENT;
   if (c->B_slot_stride < G * L * kDstate || (c->B_slot_stride * 2) % 16) return RSSM_ERR_INVALID_ARGUMENT;
   if (c->dt_slot_stride < H * L) return RSSM_ERR_INVALID_ARGUMENT;
+  if (c->read_state) {
+    if (c->read_dtype != RSSM_I8 && c->read_dtype != RSSM_E4M3) return RSSM_ERR_INVALID_ARGUMENT;
+    if (!c->read_scale || !aligned16(c->read_state) || !aligned16(c->read_scale)) return RSSM_ERR_INVALID_ARGUMENT;
+    if (c->read_slot_stride < H * kHeadElems || c->read_slot_stride % 16) return RSSM_ERR_INVALID_ARGUMENT;
+    if (c->read_scale_slot_stride < H * kDim || (c->read_scale_slot_stride * 4) % 16)
+      return RSSM_ERR_INVALID_ARGUMENT;
+  }
   if (out) {
     Cache& v = *out;
     v.S = c->num_slots;
@@ -75,6 +82,11 @@ rssm_status check_cache(const rssm_cache* c, Cache* out) {
     v.ring_start = c->ring_start;
     v.epoch = c->flush_epoch;
     v.err = c->error_word;
+    v.read_state = c->read_state;
+    v.read_stride = c->read_state ? c->read_slot_stride : 0;
+    v.read_scale = c->read_state ? c->read_scale : nullptr;
+    v.read_scale_stride = c->read_state ? c->read_scale_slot_stride : 0;
+    v.read_dtype = c->read_state ? c->read_dtype : -1;
   }
   return RSSM_OK;
 }
@@ -144,6 +156,15 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->cf = reinterpret_cast<uint16_t*>(sc + step_rows_bytes(batch));
   a->rblk = reinterpret_cast<float*>(sc + step_rows_bytes(batch) +
                                      step_cf_bytes(batch, cache->ngroups, T));
+  if (a->c.read_state) {
+    // the step never writes S0: its readout (and the C block's operand type,
+    // which follows the format it reads) works on the read checkpoint
+    a->c.state = a->c.read_state;
+    a->c.state_stride = a->c.read_stride;
+    a->c.scale = a->c.read_scale;
+    a->c.scale_stride = a->c.read_scale_stride;
+    a->c.dtype = a->c.read_dtype;
+  }
   return RSSM_OK;
 }
 
@@ -264,6 +285,7 @@ rssm_status flush_step_args(const rssm_cache* cache, const void* x, const float*
                             int32_t* pnat, const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force,
                             uint64_t seed, void* out, void* scratch, size_t scratch_bytes, StepArgs* a, int* sms) {
   if (force != 0 && force != 1) return RSSM_ERR_INVALID_ARGUMENT;
+  if (cache && cache->read_state) return RSSM_ERR_UNSUPPORTED;  // the one-call path keeps one checkpoint
   rssm_status st = step_common(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, out, scratch,
                                scratch_bytes, a);
   if (st != RSSM_OK || batch == 0) return st;

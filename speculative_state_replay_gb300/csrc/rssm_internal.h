@@ -37,6 +37,12 @@ struct Cache {
   int* ring_start;
   unsigned* epoch;
   unsigned* err;
+  // separate read checkpoint (8-bit codes + row scales, nearest), or null
+  void* read_state;
+  long long read_stride;
+  float* read_scale;
+  long long read_scale_stride;
+  int read_dtype;
 };
 
 // one flagged row of a flush (written by the flag kernel), 32 bytes

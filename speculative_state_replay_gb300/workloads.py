@@ -48,6 +48,7 @@ class Workload:
     slot_pad_bytes: int = 0      # padding after each slot in every cache tensor
     pad_row: bool = False        # one extra row that points at padding slot 0
     config_id: int = 0
+    read_dtype: int | None = None  # separate 8-bit read checkpoint (I8 / E4M3), nearest-encoded
 
     @property
     def L(self) -> int:
@@ -67,11 +68,15 @@ class Workload:
             "ngroups": self.ngroups, "dim": P_DIM, "dstate": N_DIM, "state_dtype": DTYPE_NAMES[self.state_dtype],
             "rounding": "stochastic" if self.rounding == STOCHASTIC else "nearest", "max_window": self.max_window,
             "T": self.T, "L": self.L, "varlen": self.varlen,
+            "read_checkpoint": None if self.read_dtype is None else DTYPE_NAMES[self.read_dtype],
         }
 
 
 def config(name: str, **overrides) -> Workload:
-    """The five decode configurations (sizes of the benchmark definitions)."""
+    """The five decode configurations (sizes of the benchmark definitions),
+    and "separate": the sweep's largest batch with the separate checkpoints of
+    vLLM PR #65660 (Overview: an FP16 recurrence checkpoint with stochastic
+    rounding, an FP8 read checkpoint the readout streams)."""
     base = {
         "tiny": dict(num_slots=5, nheads=8, ngroups=1, max_window=16, npredicted=4, state_dtype=F32, batch=4,
                      T=4, steps=12, pad_row=True, config_id=1),
@@ -84,9 +89,13 @@ def config(name: str, **overrides) -> Workload:
         "sweep": dict(num_slots=2 * 1024 + 1, nheads=128, ngroups=8, max_window=16, npredicted=5,
                       state_dtype=BF16, batch=1024, T=5, steps=32, varlen=True, ring_start_random=True,
                       prefill_live=16, slot_pad_bytes=4096, config_id=5),
+        "separate": dict(num_slots=2 * 1024 + 1, nheads=128, ngroups=8, max_window=16, npredicted=5,
+                         state_dtype=F16, rounding=STOCHASTIC, sr_seed=7, read_dtype=E4M3, batch=1024, T=5,
+                         steps=32, varlen=True, ring_start_random=True, prefill_live=16, slot_pad_bytes=4096,
+                         config_id=6),
     }[name]
     base.update(overrides)
-    if name == "sweep" and "batch" in overrides and "num_slots" not in overrides:
+    if name in ("sweep", "separate") and "batch" in overrides and "num_slots" not in overrides:
         base["num_slots"] = 2 * overrides["batch"] + 1
     return Workload(name=name, **base)
 

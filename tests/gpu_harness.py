@@ -48,13 +48,17 @@ CACHE_ARRAYS = ("state", "scale", "x_cache", "B_cache", "dt_cache", "ring_start"
 def gpu_cache_from(oc, device="cuda"):
     pad = (oc.state.shape[1] - oc.H * 64 * 128) * oc.state.dtype.itemsize
     gc = api.RssmCache(oc.S, oc.H, oc.G, oc.W, oc.Tmax, oc.state_dtype, oc.rounding, device=device,
-                       slot_pad_bytes=pad)
+                       slot_pad_bytes=pad, read_dtype=getattr(oc, "read_dtype", None))
     sync_gpu_from(gc, oc)
     return gc
 
 
+def cache_arrays(oc):
+    return CACHE_ARRAYS + (("read_state", "read_scale") if getattr(oc, "read_dtype", None) is not None else ())
+
+
 def sync_gpu_from(gc, oc):
-    for name in CACHE_ARRAYS:
+    for name in cache_arrays(oc):
         src = getattr(oc, name)
         dst = getattr(gc, name)
         assert tuple(dst.shape) == src.shape, (name, tuple(dst.shape), src.shape)
@@ -89,13 +93,42 @@ def half_state_close(dtype, g, o, ulps=HALF_STATE_ULPS, abs_slack=HALF_STATE_ABS
     return bool(np.all(near | (diff <= abs_slack)))
 
 
-def state_close(dtype, g, o, ulps=HALF_STATE_ULPS):
-    """Checkpoint comparison: bit-exact for 8-bit codes, 1e-4 relative for f32,
-    `ulps` units in the last place (with the near-zero slack) for bf16/f16."""
+def half_state_close_carried(dtype, g, o, row_ulps=2, abs_slack=HALF_STATE_ABS):
+    """The bar for 2-byte checkpoints that have gone through several folds on
+    each side without being re-synchronised: every element within `row_ulps`
+    units in the last place of its row's largest magnitude (rows of 128
+    dstate values).  A one-unit difference left by an earlier fold enters the
+    next fold in absolute terms, scaled by its decay e^{c_end} < 1, next to the
+    new fold's own rounding; where the new terms cancel to a small value that
+    carried difference is many units of the new code but stays below one unit
+    of the row's scale, and decays at every later fold."""
+    g = np.asarray(g).view(np.uint16)
+    o = np.asarray(o).view(np.uint16)
+    n = g.size // 128 * 128
+    gv = half_decode(dtype, g.reshape(-1)[:n]).astype(np.float64).reshape(-1, 128)
+    ov = half_decode(dtype, o.reshape(-1)[:n]).astype(np.float64).reshape(-1, 128)
+    if not np.array_equal(g.reshape(-1)[n:], o.reshape(-1)[n:]):
+        return False
+    m = np.abs(ov).max(axis=1, keepdims=True)
+    mant = 7 if dtype == W.BF16 else 10
+    _, e = np.frexp(m)  # m = f 2^e, f in [0.5, 1): the binade of m starts at 2^(e-1)
+    ulp = np.where(m > 0, np.ldexp(1.0, e - 1 - mant), 0.0)
+    if dtype == W.F16:
+        ulp = np.maximum(ulp, 2.0 ** -24)
+    return bool(np.all(np.abs(gv - ov) <= row_ulps * ulp + abs_slack))
+
+
+def state_close(dtype, g, o, ulps=HALF_STATE_ULPS, carried=False):
+    """Checkpoint comparison: bit-exact for 8-bit codes, 1e-4 relative for f32;
+    bf16/f16: `ulps` units in the last place (with the near-zero slack) after
+    one fold from identical state, or the carried-difference bar
+    (half_state_close_carried) when both sides have folded on their own."""
     if dtype in (W.I8, W.E4M3):
         return np.array_equal(g, o)
     if dtype == W.F32:
         return bool(np.all(np.abs(g - o) <= F32_STATE_RTOL * np.abs(o) + F32_STATE_ATOL))
+    if carried:
+        return half_state_close_carried(dtype, g, o)
     return half_state_close(dtype, g, o, ulps=ulps)
 
 
@@ -107,8 +140,8 @@ class Pair:
         self.gate = gate    # output gate z (seeded N(0, 1), bf16) on both sides, split path only
         # resync: after each comparison the GPU cache is overwritten with the
         # oracle's; without it both sides carry their own checkpoints on (2-byte
-        # checkpoints folded on the tensor cores may then drift by one more unit
-        # in the last place, decayed, at later flushes)
+        # checkpoints folded on the tensor cores are then held to the
+        # carried-difference bar)
         self.resync = resync
         assert not (fused and gate)
         self.orc, self.wl, self.oc = orc, wl, oc
@@ -168,9 +201,12 @@ class Pair:
             g = host_of(getattr(gc, name), getattr(oc, name))
             assert np.array_equal(g, getattr(oc, name)), name
         gs = host_of(gc.state, oc.state)
-        assert state_close(oc.state_dtype, gs, oc.state, ulps=1 if self.resync else 2), "checkpoint"
+        assert state_close(oc.state_dtype, gs, oc.state, carried=not self.resync), "checkpoint"
         if oc.state_dtype in (W.I8, W.E4M3):
             assert np.array_equal(host_of(gc.scale, oc.scale), oc.scale), "scales"
+        if getattr(oc, "read_dtype", None) is not None:  # the read checkpoint: nearest codes, bit for bit
+            assert np.array_equal(host_of(gc.read_state, oc.read_state), oc.read_state), "read checkpoint"
+            assert np.array_equal(host_of(gc.read_scale, oc.read_scale), oc.read_scale), "read scales"
         if np.array_equal(gs, oc.state):
             self.exact_state_steps += 1
         if self.resync:  # continue from identical state
@@ -183,7 +219,7 @@ def init_gpu_cache_like_bench(wl, gen, ids, device="cuda"):
     every active row's FP32 state through rssm_init_state (16 rows a call),
     prefilled rings, the workload's ring starts.  Returns (cache, pnat0)."""
     gc = api.RssmCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
-                       wl.rounding, device=device, slot_pad_bytes=wl.slot_pad_bytes)
+                       wl.rounding, device=device, slot_pad_bytes=wl.slot_pad_bytes, read_dtype=wl.read_dtype)
     t = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
     active = ids[ids > 0]
     for i in range(0, active.size, 16):
@@ -208,7 +244,7 @@ def oracle_cache_for_rows(orc, wl, gen, ids, rows):
     initialised exactly as init_gpu_cache_like_bench initialises them (rows
     are independent, so the oracle can follow a sample of them)."""
     oc = orc.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
-                         wl.rounding, slot_pad_bytes=wl.slot_pad_bytes)
+                         wl.rounding, slot_pad_bytes=wl.slot_pad_bytes, read_dtype=wl.read_dtype)
     act_pos = np.cumsum(ids > 0) - 1  # index of each row among the active rows
     for b in rows:
         s = int(ids[b])

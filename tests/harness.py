@@ -12,7 +12,7 @@ def oracle_cache(orc, wl, gen, slot_pad_bytes=None, ring_start=None):
     """Oracle cache initialised like a fresh decode batch of `wl`."""
     pad = wl.slot_pad_bytes if slot_pad_bytes is None else slot_pad_bytes
     c = orc.OracleCache(wl.num_slots, wl.nheads, wl.ngroups, wl.max_window, wl.npredicted, wl.state_dtype,
-                        wl.rounding, slot_pad_bytes=pad)
+                        wl.rounding, slot_pad_bytes=pad, read_dtype=wl.read_dtype)
     ids = gen.slot_idx()
     active = ids[ids > 0]
     states = gen.init_states(0, active.size)

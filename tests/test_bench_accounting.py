@@ -51,3 +51,13 @@ def test_flush_bytes_of_a_full_window(bench):
     assert bench.flush_bytes(wl, [16] * 64, 2) == 287834112
     # 8-bit states add the 64 row scales read and written
     assert bench.flush_bytes(W.config("eight_bit"), [0], 1) == 128 * (2 * 8192 + 512)
+
+
+def test_bytes_with_a_separate_read_checkpoint(bench):
+    """The separate-checkpoint workload (fp16 recurrence, e4m3 read copy): the
+    readout streams 8192 codes + 64 row scales per (row, head) -- about half of
+    a 2-byte checkpoint -- and a fold also writes the read copy."""
+    wl = W.config("separate")
+    row = (1, 0, 0, 5, 0, 1)
+    assert bench.algorithmic_bytes(wl, [row], None, 1) == 128 * (8192 + 256 + 5 * 256 / 16 + 5 * 128)
+    assert bench.flush_bytes(wl, [16], 2) == 128 * (2 * 16384 + 16 * 132 + 16 * 256 / 16 + 8192 + 256)

@@ -322,7 +322,7 @@ def test_full_size_sampled_rows(orc, cfg, sample, steps):
         assert np.allclose(bf16_f32(yg), bf16_f32(yo), atol=2e-2, rtol=1e-2), k
         assert np.array_equal(gp.cpu().numpy()[sample], ps), k
         o = oc.state[sid]
-        assert state_close(wl.state_dtype, host_of(gc.state[gsid], o), o, ulps=2), (k, "state")
+        assert state_close(wl.state_dtype, host_of(gc.state[gsid], o), o, carried=True), (k, "state")
         for name in ("x_cache", "B_cache", "dt_cache", "ring_start", "flush_epoch"):
             o = getattr(oc, name)[sid]
             assert np.array_equal(host_of(getattr(gc, name)[gsid], o), o), (k, name)

@@ -57,6 +57,10 @@ def test_bar_rejects_a_wrong_token_in_the_fold(orc, dtype, mutate, token):
     far = (code_distance(bad.view(np.uint16), ref.view(np.uint16)) > 1).mean()
     if token == 13:
         assert far > 0.3, far
+        # the newest token also fails the bar for checkpoints carried through
+        # several folds (two units of each row's largest magnitude)
+        assert not state_close(dtype, bad, ref, carried=True)
+        assert state_close(dtype, ref, ref, carried=True)
 
 
 @pytest.mark.parametrize("dtype", [W.BF16, W.F16])
@@ -69,6 +73,7 @@ def test_bar_admits_one_unit_in_the_last_place(orc, dtype):
     up2 = np.where(finite, bits + 2, bits).astype(np.uint16)
     assert half_state_close(dtype, up1, bits)
     assert not half_state_close(dtype, up2, bits)
+    assert state_close(dtype, up1, bits, carried=True)  # one unit of a value <= two of its row maximum
     # the near-zero slack: +0 against the smallest codes of either sign
     tiny = np.array([0x0001, 0x8003, 0x0000], np.uint16)
     assert half_state_close(dtype, tiny, np.zeros(3, np.uint16))
