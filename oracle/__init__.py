@@ -21,7 +21,7 @@ _LIB_PATH = os.path.join(_HERE, "liboracle_rssm.so")
 _lock = threading.Lock()
 _lib = None
 
-F32, BF16, F16, I8, E4M3 = 0, 1, 2, 3, 4
+F32, BF16, F16, I8, E4M3, NVFP4 = 0, 1, 2, 3, 4, 5
 NEAREST, STOCHASTIC = 0, 1
 ERR_PNAT, ERR_SEQLEN, ERR_ACCEPT = 1, 2, 4
 P_DIM, N_DIM = 64, 128
@@ -54,6 +54,8 @@ class OrcCache(ctypes.Structure):
         ("read_state", ctypes.c_void_p), ("read_slot_stride", ctypes.c_int64),
         ("read_scale", ctypes.c_void_p), ("read_scale_stride", ctypes.c_int64),
         ("read_dtype", ctypes.c_int32),
+        ("read_sf", ctypes.c_void_p), ("read_sf_stride", ctypes.c_int64),
+        ("read_gs", ctypes.c_void_p),
     ]
 
 
@@ -72,7 +74,8 @@ def lib():
                 getattr(_lib, name).restype = f32
                 getattr(_lib, name).argtypes = [f32]
             for name in ("orc_spec_exp_n", "orc_spec_log1p_n", "orc_spec_softplus_n", "orc_f32_to_bf16_n",
-                         "orc_f32_to_f16_n", "orc_f32_to_e4m3_n", "orc_f16_decode_n", "orc_e4m3_decode_n"):
+                         "orc_f32_to_f16_n", "orc_f32_to_e4m3_n", "orc_f16_decode_n", "orc_e4m3_decode_n",
+                         "orc_f32_to_e2m1_n", "orc_e2m1_decode_n"):
                 getattr(_lib, name).restype = None
                 getattr(_lib, name).argtypes = [vp, vp, ctypes.c_long]
             _lib.orc_philox4x32.argtypes = [u32, vp, vp, vp]
@@ -90,6 +93,9 @@ def lib():
                                       vp, vp, vp, ctypes.c_int]
             _lib.orc_accept.restype = ctypes.c_int
             _lib.orc_accept.argtypes = [ctypes.POINTER(OrcCache), vp, vp, vp, vp, i32, i32]
+            _lib.orc_quantize_rows_nvfp4.argtypes = [vp, ctypes.c_int, f32, vp, vp]
+            _lib.orc_nvfp4_global_scale.restype = f32
+            _lib.orc_nvfp4_global_scale.argtypes = [vp, ctypes.c_long]
             _lib.orc_have_openmp.restype = ctypes.c_int
             del i64
         return _lib
@@ -132,6 +138,30 @@ def f32_to_f16_bits(x):
 
 def f32_to_e4m3_bits(x):
     return _map("orc_f32_to_e4m3_n", np.asarray(x, np.float32), np.uint8)
+
+
+def f32_to_e2m1_bits(x):
+    return _map("orc_f32_to_e2m1_n", np.asarray(x, np.float32), np.uint8)
+
+
+def e2m1_decode(bits):
+    return _map("orc_e2m1_decode_n", np.asarray(bits, np.uint8), np.float32)
+
+
+def quantize_rows_nvfp4(acc, gs):
+    """NVFP4-encode rows x 128 fp32 values with global scale gs; returns
+    (codes [rows][64] bytes, two per byte, even element low; block scales
+    [rows][8] e4m3 bytes)."""
+    acc = np.ascontiguousarray(acc, dtype=np.float32).reshape(-1, N_DIM)
+    codes = np.zeros((acc.shape[0], N_DIM // 2), np.uint8)
+    sf = np.zeros((acc.shape[0], N_DIM // 16), np.uint8)
+    lib().orc_quantize_rows_nvfp4(_p(acc), acc.shape[0], np.float32(gs), _p(codes), _p(sf))
+    return codes, sf
+
+
+def nvfp4_global_scale(state):
+    st = np.ascontiguousarray(state, dtype=np.float32)
+    return float(lib().orc_nvfp4_global_scale(_p(st), st.size))
 
 
 def f16_decode(bits):
@@ -190,10 +220,11 @@ class OracleCache:
 
     def __init__(self, num_slots, nheads, ngroups, max_window, npredicted, state_dtype, rounding=NEAREST,
                  slot_pad_bytes=0, read_dtype=None):
-        """read_dtype (I8 or E4M3): keep a separate 8-bit read checkpoint,
+        """read_dtype (I8, E4M3 or NVFP4): keep a separate read checkpoint,
         nearest-encoded from the recurrence's fp32 values at init and at every
         flush, which the step reads S0 from (None: the step reads the
-        recurrence state)."""
+        recurrence state).  NVFP4: E2M1 codes (two per byte), one E4M3 scale
+        per 16 dstate values, one FP32 global scale per slot."""
         self.S, self.H, self.G = num_slots, nheads, ngroups
         self.W, self.Tmax = max_window, npredicted
         self.L = max_window + npredicted
@@ -213,11 +244,22 @@ class OracleCache:
         self.flush_epoch = np.zeros(num_slots, np.uint32)
         self.error_word = np.zeros(1, np.uint32)
         self.read_dtype = read_dtype
-        self.read_state = None if read_dtype is None else np.zeros((num_slots, stride(nheads * P_DIM * N_DIM, 1)), np.uint8)
-        self.read_scale = None if read_dtype is None else np.ones((num_slots, stride(nheads * P_DIM, 4)), np.float32)
+        self.read_state = self.read_scale = self.read_sf = self.read_gs = None
+        if read_dtype == NVFP4:
+            self.read_state = np.zeros((num_slots, stride(nheads * P_DIM * N_DIM // 2, 1)), np.uint8)
+            self.read_sf = np.zeros((num_slots, stride(nheads * P_DIM * N_DIM // 16, 1)), np.uint8)
+            self.read_gs = np.ones(num_slots, np.float32)
+        elif read_dtype is not None:
+            self.read_state = np.zeros((num_slots, stride(nheads * P_DIM * N_DIM, 1)), np.uint8)
+            self.read_scale = np.ones((num_slots, stride(nheads * P_DIM, 4)), np.float32)
 
     def read_state_view(self):
+        if self.read_dtype == NVFP4:
+            return self.read_state[:, : self.H * P_DIM * N_DIM // 2].reshape(self.S, self.H, P_DIM, N_DIM // 2)
         return self.read_state[:, : self.H * P_DIM * N_DIM].reshape(self.S, self.H, P_DIM, N_DIM)
+
+    def read_sf_view(self):
+        return self.read_sf[:, : self.H * P_DIM * N_DIM // 16].reshape(self.S, self.H, P_DIM, N_DIM // 16)
 
     def read_scale_view(self):
         return self.read_scale[:, : self.H * P_DIM].reshape(self.S, self.H, P_DIM)
@@ -257,8 +299,12 @@ class OracleCache:
         rd = getattr(self, "read_state", None)
         if rd is not None:
             c.read_state, c.read_slot_stride = _p(rd), rd.shape[1]
-            c.read_scale, c.read_scale_stride = _p(self.read_scale), self.read_scale.shape[1]
             c.read_dtype = self.read_dtype
+            if self.read_dtype == NVFP4:
+                c.read_sf, c.read_sf_stride = _p(self.read_sf), self.read_sf.shape[1]
+                c.read_gs = _p(self.read_gs)
+            else:
+                c.read_scale, c.read_scale_stride = _p(self.read_scale), self.read_scale.shape[1]
         return c
 
     def init_state(self, states, ids, seed=0):

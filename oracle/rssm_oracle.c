@@ -38,7 +38,7 @@
 #define P_DIM 64   /* head dim, [vAPI] module docstring (kernels take head dim 64) */
 #define N_DIM 128  /* dstate,   [vAPI] module docstring (state dim 128) */
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F16 = 2, ORC_I8 = 3, ORC_E4M3 = 4 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_F16 = 2, ORC_I8 = 3, ORC_E4M3 = 4, ORC_NVFP4 = 5 };
 enum { ORC_NEAREST = 0, ORC_STOCHASTIC = 1 };
 
 /* Device-side error bits, sticky.  Same meaning as the library's. */
@@ -64,9 +64,17 @@ typedef struct {
    * from the same fp32 values as the recurrence state (at init and at every
    * flush); the step's readout reads S0 from them.  read_state = NULL: the
    * step reads the recurrence state itself.                                 */
-  void *read_state;  int64_t read_slot_stride;  /* elements */
+  void *read_state;  int64_t read_slot_stride;  /* elements (NVFP4: bytes, two codes each) */
   float *read_scale; int64_t read_scale_stride;
-  int32_t read_dtype;                           /* ORC_I8 or ORC_E4M3 */
+  int32_t read_dtype;                           /* ORC_I8, ORC_E4M3 or ORC_NVFP4 */
+  /* NVFP4 read checkpoint (read_dtype = ORC_NVFP4; [vAPI]
+   * initialize_replayssm_state, NVFP4 branch, and the kernels' state_lo /
+   * sf_lo / sg_meta arguments): FP4 E2M1 codes [slot][H][64][64 bytes] in
+   * read_state, one E4M3 scale per 16 consecutive dstate values
+   * [slot][H][64][8] in read_sf, one FP32 global scale per slot in read_gs
+   * (read_scale unused).                                                    */
+  uint8_t *read_sf;  int64_t read_sf_stride;    /* bytes */
+  float *read_gs;                               /* [slot] */
 } orc_cache;
 
 /* ------------------------------------------------------------------------- */
@@ -315,10 +323,32 @@ float orc_e4m3_decode(uint8_t c) {
   return sign * ldexpf((float)(8 + m), ex - 10);
 }
 
+/* FP4 E2M1 (OCP microscaling formats): 1 sign, 2 exponent bits (bias 1), 1
+ * fraction bit; magnitudes 0, 0.5 (subnormal), 1, 1.5, 2, 3, 4, 6; no inf or
+ * NaN.  Code = sign << 3 | exponent << 1 | fraction.                        */
+#define E2M1_MAXF 6.0f
+uint8_t orc_e2m1_encode(float g) { /* g on the e2m1 grid, |g| <= 6 */
+  uint8_t sign = signbit(g) ? 0x8u : 0u;
+  float a = fabsf(g);
+  if (a < 1.0f) return (uint8_t)(sign | (uint8_t)(a / 0.5f)); /* 0 or the subnormal 0.5 */
+  int fe;
+  frexpf(a, &fe);
+  int e = fe - 1; /* 0..2 */
+  uint32_t frac = (uint32_t)(a / ldexpf(1.0f, e - 1)) - 2u;
+  return (uint8_t)(sign | (uint32_t)(e + 1) << 1 | frac);
+}
+float orc_e2m1_decode(uint8_t c) {
+  float sign = (c & 0x8u) ? -1.0f : 1.0f;
+  int ex = (c >> 1) & 0x3, m = c & 0x1;
+  if (ex == 0) return sign * 0.5f * (float)m;
+  return sign * ldexpf((float)(2 + m), ex - 2);
+}
+
 /* Round-to-nearest conversions used for plain data (y output, tests). */
 uint16_t orc_f32_to_bf16(float v) { return orc_bf16_encode(round_nearest_grid(v, 7, -126, BF16_MAXF)); }
 uint16_t orc_f32_to_f16(float v) { return orc_f16_encode(round_nearest_grid(v, 10, -14, F16_MAXF)); }
 uint8_t orc_f32_to_e4m3(float v) { return orc_e4m3_encode(round_nearest_grid(v, 3, -6, E4M3_MAXF)); }
+uint8_t orc_f32_to_e2m1(float v) { return orc_e2m1_encode(round_nearest_grid(v, 1, 0, E2M1_MAXF)); }
 
 static int dtype_bytes(int dt) {
   switch (dt) {
@@ -328,6 +358,51 @@ static int dtype_bytes(int dt) {
   }
 }
 static int dtype_is_8bit(int dt) { return dt == ORC_I8 || dt == ORC_E4M3; }
+static int read_dtype_ok(int dt) { return dt == ORC_I8 || dt == ORC_E4M3 || dt == ORC_NVFP4; }
+
+/* ------------------------------------------------------------------------- */
+/* NVFP4 read checkpoint of one (slot, head, d) row.  Reading of [vAPI]
+ * initialize_replayssm_state (NVFP4 branch): the slot's global scale is the
+ * largest magnitude of its FP32 state divided by 6 * 448 (the E2M1 maximum
+ * times the E4M3 maximum), 1 for an all-zero state; it is set at init and kept
+ * by the slot's later flushes.  Each block of 16 consecutive dstate values
+ * takes an E4M3 scale sf = e4m3_nearest(block max / (6 gs)) (saturating at
+ * 448), and each value the E2M1 code nearest to v / (gs * sf) (saturating at
+ * 6; a block whose scale rounds to 0 is all zeros).  Decoded value:
+ * e2m1(code) * sf * gs.  Nearest rounding throughout ([vS] Claims: read
+ * checkpoints use nearest encoding).                                       */
+/* ------------------------------------------------------------------------- */
+#define NVFP4_BLOCK 16
+static void quantize_row_nvfp4(const float *acc, float gs, uint8_t *codes /* 64 bytes */, uint8_t *sf /* 8 */) {
+  for (int blk = 0; blk < N_DIM / NVFP4_BLOCK; ++blk) {
+    const float *v = acc + blk * NVFP4_BLOCK;
+    float bmax = 0.0f;
+    for (int i = 0; i < NVFP4_BLOCK; ++i) bmax = fmaxf(bmax, fabsf(v[i]));
+    uint8_t sc = orc_f32_to_e4m3(bmax / (6.0f * gs));
+    sf[blk] = sc;
+    float q = orc_e4m3_decode(sc) * gs;
+    for (int i = 0; i < NVFP4_BLOCK; i += 2) {
+      uint8_t c0 = 0, c1 = 0;
+      if (q > 0.0f) {
+        c0 = orc_f32_to_e2m1(v[i] / q);
+        c1 = orc_f32_to_e2m1(v[i + 1] / q);
+      }
+      codes[(blk * NVFP4_BLOCK + i) / 2] = (uint8_t)(c0 | c1 << 4); /* even element in the low nibble */
+    }
+  }
+}
+
+/* Exported for direct tests of the NVFP4 row encoder. */
+void orc_quantize_rows_nvfp4(const float *acc, int rows, float gs, uint8_t *codes, uint8_t *sf) {
+  for (int i = 0; i < rows; ++i) quantize_row_nvfp4(acc + (size_t)i * N_DIM, gs, codes + (size_t)i * 64, sf + (size_t)i * 8);
+}
+
+/* The slot's NVFP4 global scale from its FP32 state (all heads). */
+float orc_nvfp4_global_scale(const float *state, long n) {
+  float m = 0.0f;
+  for (long i = 0; i < n; ++i) m = fmaxf(m, fabsf(state[i]));
+  return m > 0.0f ? m / (6.0f * 448.0f) : 1.0f;
+}
 
 /* ------------------------------------------------------------------------- */
 /* Checkpoint quantiser.  [vS] commit notes: quantised checkpoints carry FP32
@@ -415,7 +490,11 @@ static void store_state_head(const orc_cache *c, int s, int h, const float *acc 
                                               : NULL;
     quantize_row(c->state_dtype, c->rounding, acc + (size_t)d * N_DIM, (uint32_t)h, (uint32_t)s, (uint32_t)d,
                  epoch, seed, (char *)c->state + off * eb, sc);
-    if (c->read_state) { /* the read checkpoint: the same fp32 row, nearest */
+    if (c->read_state && c->read_dtype == ORC_NVFP4) { /* the read checkpoint: the same fp32 row */
+      size_t roff = (size_t)s * c->read_slot_stride + ((size_t)h * P_DIM + d) * (N_DIM / 2);
+      size_t soff = (size_t)s * c->read_sf_stride + ((size_t)h * P_DIM + d) * (N_DIM / NVFP4_BLOCK);
+      quantize_row_nvfp4(acc + (size_t)d * N_DIM, c->read_gs[s], (uint8_t *)c->read_state + roff, c->read_sf + soff);
+    } else if (c->read_state) { /* the read checkpoint: the same fp32 row, nearest */
       size_t roff = (size_t)s * c->read_slot_stride + ((size_t)h * P_DIM + d) * N_DIM;
       quantize_row(c->read_dtype, ORC_NEAREST, acc + (size_t)d * N_DIM, (uint32_t)h, (uint32_t)s, (uint32_t)d,
                    epoch, seed, (uint8_t *)c->read_state + roff,
@@ -428,6 +507,13 @@ static void store_state_head(const orc_cache *c, int s, int h, const float *acc 
  * checkpoint's code * scale when there is one, else the recurrence state. */
 static float readout_f32(const orc_cache *c, int s, int h, int d, int n) {
   if (!c->read_state) return state_f32(c, s, h, d, n);
+  if (c->read_dtype == ORC_NVFP4) {
+    size_t row = (size_t)h * P_DIM + d;
+    uint8_t byte = ((const uint8_t *)c->read_state)[(size_t)s * c->read_slot_stride + row * (N_DIM / 2) + n / 2];
+    uint8_t code = (n & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 0xfu);
+    uint8_t sc = c->read_sf[(size_t)s * c->read_sf_stride + row * (N_DIM / NVFP4_BLOCK) + n / NVFP4_BLOCK];
+    return orc_e2m1_decode(code) * orc_e4m3_decode(sc) * c->read_gs[s];
+  }
   size_t off = (size_t)s * c->read_slot_stride + ((size_t)h * P_DIM + d) * N_DIM + n;
   float sc = c->read_scale[(size_t)s * c->read_scale_stride + (size_t)h * P_DIM + d];
   if (c->read_dtype == ORC_I8) return (float)((const int8_t *)c->read_state)[off] * sc;
@@ -472,7 +558,9 @@ static inline int slot_active(const orc_cache *c, int s) { return s >= 1 && s < 
 
 static int check_cache(const orc_cache *c) {
   if (!c || c->nheads <= 0 || c->ngroups <= 0 || c->nheads % c->ngroups) return -1;
-  if (c->read_state && (!c->read_scale || !dtype_is_8bit(c->read_dtype))) return -1;
+  if (c->read_state && !read_dtype_ok(c->read_dtype)) return -1;
+  if (c->read_state && c->read_dtype != ORC_NVFP4 && !c->read_scale) return -1;
+  if (c->read_state && c->read_dtype == ORC_NVFP4 && (!c->read_sf || !c->read_gs)) return -1;
   if (c->max_window < 0 || c->npredicted < 1 || c->max_window + c->npredicted > 256) return -1;
   return 0;
 }
@@ -489,6 +577,8 @@ int orc_init_state(const orc_cache *c, const float *states, const int32_t *ids, 
   for (int i = 0; i < n; ++i) {
     int s = ids[i];
     if (!slot_active(c, s)) continue;
+    if (c->read_state && c->read_dtype == ORC_NVFP4) /* the slot's global scale, from all its heads */
+      c->read_gs[s] = orc_nvfp4_global_scale(states + (size_t)i * H * P_DIM * N_DIM, (long)H * P_DIM * N_DIM);
     for (int h = 0; h < H; ++h)
       store_state_head(c, s, h, states + ((size_t)i * H + h) * P_DIM * N_DIM, 0u, seed);
     for (int h = 0; h < H; ++h)
@@ -751,6 +841,8 @@ void orc_f32_to_f16_n(const float *x, uint16_t *y, long n) { for (long i = 0; i 
 void orc_f32_to_e4m3_n(const float *x, uint8_t *y, long n) { for (long i = 0; i < n; ++i) y[i] = orc_f32_to_e4m3(x[i]); }
 void orc_f16_decode_n(const uint16_t *x, float *y, long n) { for (long i = 0; i < n; ++i) y[i] = orc_f16_decode(x[i]); }
 void orc_e4m3_decode_n(const uint8_t *x, float *y, long n) { for (long i = 0; i < n; ++i) y[i] = orc_e4m3_decode(x[i]); }
+void orc_f32_to_e2m1_n(const float *x, uint8_t *y, long n) { for (long i = 0; i < n; ++i) y[i] = orc_f32_to_e2m1(x[i]); }
+void orc_e2m1_decode_n(const uint8_t *x, float *y, long n) { for (long i = 0; i < n; ++i) y[i] = orc_e2m1_decode(x[i]); }
 int orc_have_openmp(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();
