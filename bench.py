@@ -242,7 +242,8 @@ def algorithmic_bytes(wl, rows_rec, ntok_b, esz):
     hpg = wl.hpg
     for (s, r, p, Tb, tok0, flags) in rows_rec:
         if (flags & 1) and Tb > 0:
-            per_head = 64 * 128 * esz + (256 if esz == 1 else 0) + Tb * 256 / hpg + Tb * 128
+            # 8-bit: 64 row scales; NVFP4 (0.5 bytes an element): 64 x 8 block scales
+            per_head = 64 * 128 * esz + {1: 256, 0.5: 512}.get(esz, 0) + Tb * 256 / hpg + Tb * 128
             total += per_head * wl.nheads
         elif Tb > 0:
             total += Tb * 128 * wl.nheads
@@ -250,28 +251,26 @@ def algorithmic_bytes(wl, rows_rec, ntok_b, esz):
 
 
 def fused_bytes(wl, rows_rec, esz):
-    """Algorithmic HBM bytes of one step-kernel launch (rssm_flush_step) from its
-    per-row records (s, r, p, Tb, tok0, flags, p_old, epoch), per (row, head):
-    S0 (+ scales) read once if the row is read out or folded; for a folded row
-    the new S0 (+ scales) written and its pre-flush live x rows, dt' and (the
-    group's share of) B rows read; for a row read out its live and new x rows
-    and dt, the group's share of its live and new B rows and of its C rows, y
-    written, and the appended x rows, dt' and B rows written; rows without
-    outputs write zero y."""
+    """Algorithmic HBM bytes of one readout-with-fold launch (the main half of
+    rssm_flush_step) from its per-row records (s, r, p, Tb, tok0, flags,
+    epoch, gs), per (row, head): S0 (+ scales) read once if the row is read out or
+    folded; for a folded row the new S0 (+ scales) written and its live x rows
+    and (the group's share of) B rows read; for a row read out the group's
+    share of its C rows and y written; rows without outputs write zero y.
+    (dt', the replay terms and the ring appends are the precompute's.)"""
     total = 0
     hpg = wl.hpg
     s0 = 64 * 128 * esz + (256 if esz == 1 else 0)
-    for (s, r, p, Tb, tok0, flags, p_old, ep) in rows_rec:
+    for (s, r, p, Tb, tok0, flags, ep, gs) in rows_rec:
         out_ok, fo = (flags & 1) and Tb > 0, flags & 2
+        p_old = p  # the prefix a fold folds is the live prefix the outputs replay
         per_head = 0
         if out_ok or fo:
             per_head += s0
         if fo:
-            per_head += s0 + p_old * (128 + 4) + p_old * 256 / hpg
+            per_head += s0 + p_old * 128 + p_old * 256 / hpg
         if out_ok:
-            k = p + Tb
-            per_head += k * (128 + 4) + k * 256 / hpg + Tb * 256 / hpg  # x, dt, B, C read
-            per_head += Tb * 128 + Tb * (128 + 4) + Tb * 256 / hpg      # y, appends written
+            per_head += Tb * 256 / hpg + Tb * 128
         elif Tb > 0:
             per_head += Tb * 128
         total += per_head * wl.nheads
@@ -283,7 +282,11 @@ def flush_bytes(wl, recs, esz):
     and B rows per flagged (row, head); with a separate read checkpoint also
     its 8-bit codes and row scales written."""
     total = 0
-    rd = 64 * 128 + 256 if wl.read_dtype is not None else 0
+    rd = 0
+    if wl.read_dtype == W.NVFP4:
+        rd = 64 * 128 // 2 + 512
+    elif wl.read_dtype is not None:
+        rd = 64 * 128 + 256
     for p in recs:
         total += wl.nheads * (2 * 64 * 128 * esz + (512 if esz == 1 else 0) + p * 128 + p * 256 / wl.hpg + p * 4
                               + rd)
@@ -423,7 +426,7 @@ def run_gpu(args, rank, ws, local):
     # the launch groups of one step; `rg` is the dominant kernel's group
     groups = step_groups(buf, out)
     if fused:
-        names, rg = ["classify", "step_main", "accept"], 1
+        names, rg = ["precompute", "readout_fold", "accept"], 1
     else:
         names, rg = ["flush", "precompute", "readout", "accept"], 2
     # a second set of device inputs and output: the end-to-end leg alternates
@@ -716,7 +719,7 @@ def run_gpu(args, rank, ws, local):
                        launch="one CUDA graph per step (kernels chained by programmatic dependent launch); kernel times from a second pass with one graph per launch group",
                        force_flush=bool(args.force_flush or args.full_window),
                        full_window=bool(args.full_window), path=args.path),
-        "roofline": {"bound": "hbm", "kernel": "step_kernel" if fused else "readout_kernel",
+        "roofline": {"bound": "hbm", "kernel": "readout_kernel (fold variant)" if fused else "readout_kernel",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "traffic": None if fused or args.batch is not None else profiled_traffic(
                          "readout_kernel", wl.name, units_per_read),
@@ -727,7 +730,7 @@ def run_gpu(args, rank, ws, local):
         "flush_roofline": flush_roofline,
         "flush_roofline_full_window": fw_roofline,
         "e2e": e2e,
-        # per timed step: classify, step kernel, accept (split: flush, precompute, readout, accept)
+        # per timed step: precompute, readout with fold, accept (split: flush, precompute, readout, accept)
         "gpu_launches": (3 if fused else 4) * args.steps,
         "clocks": clk,
         "device_time_ms": dict({"step": statistics.mean(step_ms)},

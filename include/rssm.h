@@ -84,7 +84,13 @@ typedef enum {
 /* Checkpoint state formats.  8-bit formats carry one FP32 scale per
  * (slot, head, d) row of 128 dstate values ([vS] commit notes: quantised
  * checkpoints with FP32 row scales). */
-typedef enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2, RSSM_I8 = 3, RSSM_E4M3 = 4 } rssm_dtype;
+typedef enum { RSSM_F32 = 0, RSSM_BF16 = 1, RSSM_F16 = 2, RSSM_I8 = 3, RSSM_E4M3 = 4, RSSM_NVFP4 = 5 } rssm_dtype;
+/* RSSM_NVFP4 is a read-checkpoint format only (rssm_cache.read_dtype): FP4
+ * E2M1 codes (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6), two per byte with the
+ * even dstate element in the low nibble, one E4M3 scale per 16 consecutive
+ * dstate values of a row, one FP32 global scale per slot; a value decodes as
+ * e2m1(code) * e4m3(scale) * global ([vAPI] initialize_replayssm_state,
+ * NVFP4 branch; the NVFP4 kernels' state_lo / sf_lo / sg_meta arguments). */
 
 /* How a flush or init rounds fp32 values to the state format: nearest
  * (ties to even, saturating) or stochastic with a Philox4x32-7 hash keyed by
@@ -136,9 +142,19 @@ typedef struct {
    * the inputs bit for bit.  read_state = NULL: no read checkpoint (the
    * step reads `state`); the other read fields are then ignored.
    * rssm_flush_step does not take a read checkpoint (RSSM_ERR_UNSUPPORTED). */
-  void *read_state;    int64_t read_slot_stride;       /* 8-bit [slot][H][64][128] */
-  float *read_scale;   int64_t read_scale_slot_stride; /* f32 [slot][H][64] */
-  int32_t read_dtype;                                  /* RSSM_I8 or RSSM_E4M3 */
+  void *read_state;    int64_t read_slot_stride;       /* 8-bit [slot][H][64][128]; NVFP4: bytes [slot][H][64][64] */
+  float *read_scale;   int64_t read_scale_slot_stride; /* f32 [slot][H][64] (8-bit read formats) */
+  int32_t read_dtype;                                  /* RSSM_I8, RSSM_E4M3 or RSSM_NVFP4 */
+  /* NVFP4 read checkpoint only (else ignored): the E4M3 block scales
+   * [slot][H][64][8] (bytes; stride in bytes) and the FP32 global scale of
+   * each slot [slot].  rssm_init_state sets a slot's global scale to the
+   * largest magnitude of its FP32 prefill state / (6 * 448) (1 for a zero
+   * state); the slot's flushes keep it.  Block scale = e4m3 nearest of
+   * (block max / (6 * global)), saturating; code = e2m1 nearest of
+   * (v / (global * block scale)), saturating at 6 (0 where the block scale is
+   * 0). */
+  void *read_sf;       int64_t read_sf_slot_stride;
+  float *read_gs;
 } rssm_cache;
 
 /*
@@ -211,23 +227,30 @@ rssm_status rssm_step(const rssm_cache *cache, const void *x, const float *dt, c
                       void *scratch, size_t scratch_bytes, void *stream);
 
 /*
- * One decode iteration's flush and step in one call: the same results as
+ * One decode iteration's flush and step in one call, in the shape of the
+ * pages' own design ([FI] Description item 1: a precompute, then a persistent
+ * main kernel that replays the state and, for rows whose window is full,
+ * writes the folded checkpoint in the same pass).  Same results as
  * rssm_flush(cache, A, slot_idx, pnat, cu_seqlens, batch, T, force, seed)
- * followed by rssm_step(...) with the same arguments -- outputs, checkpoints
- * (bit for bit for f32, 8-bit and stochastically rounded states: this call
- * folds every state in the canonical fp32 order, which rssm_flush uses for
- * them; 2-byte states with nearest rounding within summation order), rings,
- * ring_start, pnat, flush_epoch and error bits.  The pages keep the flush and
- * the step as separate kernels ([FI] Description items 1-2: precompute +
- * persistent main; the flush in its own kernels); here one persistent kernel
- * takes each (row, head) once: it folds a flushed head in the shared-memory
- * stage its checkpoint arrived in, forms the step's replay terms for it and
- * reads the outputs out of the same stage, so each checkpoint is read from
- * HBM once per decode iteration.
+ * followed by rssm_step(...) with the same arguments, except as noted:
+ *  - checkpoints, 8-bit scales, rings, ring_start, pnat, flush_epoch and error
+ *    bits: the same bits -- every fold here takes the canonical fp32 order
+ *    (also for 2-byte states with nearest rounding, which rssm_flush may fold
+ *    on the tensor cores);
+ *  - outputs: a flushed row's outputs replay its whole live prefix from the
+ *    old checkpoint (the fold's fp32 values before their rounding), where the
+ *    two calls read the rounded new checkpoint; they agree within the bf16
+ *    output tolerance;
+ *  - a row with pnat + T_b > L (its new tokens would land on live slots the
+ *    fold reads) is refused with RSSM_ERRBIT_PNAT (zero outputs, caches
+ *    untouched), where the two calls fold it first.  The decode protocol
+ *    (flush -> step -> accept) never produces such a row when max_window >=
+ *    npredicted.
+ * Each flushed checkpoint is read from HBM once (folded in the stage its
+ * outputs are read from) instead of twice.
  *   pnat     [batch] i32 (device, in/out): set to 0 for flushed rows
  *   force, seed as in rssm_flush; scratch of at least rssm_scratch_bytes().
- * Ring appends are made after the live prefix they may land on has been read,
- * so rows with pnat + T_b > L (whenever max_window < T) give the same result.
+ * A cache with a separate read checkpoint is refused (RSSM_ERR_UNSUPPORTED).
  */
 rssm_status rssm_flush_step(const rssm_cache *cache, const void *x, const float *dt, const float *A, const void *B,
                             const void *C, const float *D, const float *dt_bias, const int32_t *slot_idx,
@@ -238,10 +261,12 @@ rssm_status rssm_flush_step(const rssm_cache *cache, const void *x, const float 
  * The two halves of rssm_flush_step, exposed for profiling: rssm_flush_step
  * == rssm_flush_step_classify followed by rssm_flush_step_main with the same
  * arguments and scratch.
- *   classify: per row: the flush decision and the ring the step works on.
- *   main:     per (row, head): folds flushed heads, the flush's bookkeeping,
- *             the step's replay terms and ring appends, streams S0 once,
- *             forms y.
+ *   classify: per (row, group): the flush decision, dt', cumulative A dt', the
+ *             C.B contraction and the replay terms over the whole live prefix
+ *             (as rssm_step_precompute), the ring appends, and for flushed
+ *             rows the fold weights in canonical fp32.
+ *   main:     per (row, head): streams S0 once, forms y, folds flushed heads
+ *             and writes their checkpoints; the flush's bookkeeping.
  */
 rssm_status rssm_flush_step_classify(const rssm_cache *cache, const void *x, const float *dt, const float *A,
                                      const void *B, const void *C, const float *D, const float *dt_bias,

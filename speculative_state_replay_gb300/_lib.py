@@ -27,6 +27,8 @@ class RssmCacheStruct(ctypes.Structure):
         ("read_state", ctypes.c_void_p), ("read_slot_stride", ctypes.c_int64),
         ("read_scale", ctypes.c_void_p), ("read_scale_slot_stride", ctypes.c_int64),
         ("read_dtype", ctypes.c_int32),
+        ("read_sf", ctypes.c_void_p), ("read_sf_slot_stride", ctypes.c_int64),
+        ("read_gs", ctypes.c_void_p),
     ]
 
 

@@ -13,11 +13,12 @@ import torch
 
 from . import _lib
 
-F32, BF16, F16, I8, E4M3 = 0, 1, 2, 3, 4
+F32, BF16, F16, I8, E4M3, NVFP4 = 0, 1, 2, 3, 4, 5
 NEAREST, STOCHASTIC = 0, 1
 ERRBIT_PNAT, ERRBIT_SEQLEN, ERRBIT_ACCEPT, ERRBIT_TIMEOUT = 1, 2, 4, 8
 DIM, DSTATE = 64, 128
-STATE_TORCH = {F32: torch.float32, BF16: torch.int16, F16: torch.int16, I8: torch.int8, E4M3: torch.uint8}
+STATE_TORCH = {F32: torch.float32, BF16: torch.int16, F16: torch.int16, I8: torch.int8, E4M3: torch.uint8,
+               NVFP4: torch.uint8}
 
 
 class RssmError(RuntimeError):
@@ -70,7 +71,9 @@ class RssmCache:
     Every tensor is 2-D [slot, slot_stride]; `slot_pad_bytes` adds padding
     after each slot's page.  bf16/f16 data is held as raw 16-bit words.
     `read_dtype` (I8 or E4M3) adds a separate 8-bit read checkpoint
-    (`read_state`, `read_scale`) that the step's readout reads S0 from.
+    (`read_state`, `read_scale`) that the step's readout reads S0 from;
+    NVFP4 adds an NVFP4 one (`read_state` codes two per byte, `read_sf` block
+    scales, `read_gs` per-slot global scales).
     """
 
     def __init__(self, num_slots, nheads, ngroups, max_window, npredicted, state_dtype, rounding=NEAREST,
@@ -96,11 +99,14 @@ class RssmCache:
         self.flush_epoch = z((num_slots,), torch.int32)
         self.error_word = z((1,), torch.int32)
         self.read_dtype = read_dtype
-        if read_dtype is not None:
+        self.read_state = self.read_scale = self.read_sf = self.read_gs = None
+        if read_dtype == NVFP4:
+            self.read_state = z((num_slots, stride(nheads * DIM * DSTATE // 2, 1)), torch.uint8)
+            self.read_sf = z((num_slots, stride(nheads * DIM * DSTATE // 16, 1)), torch.uint8)
+            self.read_gs = torch.ones((num_slots,), dtype=torch.float32, device=dev)
+        elif read_dtype is not None:
             self.read_state = z((num_slots, stride(nheads * DIM * DSTATE, 1)), STATE_TORCH[read_dtype])
             self.read_scale = torch.ones((num_slots, stride(nheads * DIM, 4)), dtype=torch.float32, device=dev)
-        else:
-            self.read_state = self.read_scale = None
         self._struct = None
 
     def struct(self):
@@ -120,8 +126,12 @@ class RssmCache:
             c.error_word = self.error_word.data_ptr()
             if self.read_state is not None:
                 c.read_state, c.read_slot_stride = self.read_state.data_ptr(), self.read_state.shape[1]
-                c.read_scale, c.read_scale_slot_stride = self.read_scale.data_ptr(), self.read_scale.shape[1]
                 c.read_dtype = self.read_dtype
+                if self.read_dtype == NVFP4:
+                    c.read_sf, c.read_sf_slot_stride = self.read_sf.data_ptr(), self.read_sf.shape[1]
+                    c.read_gs = self.read_gs.data_ptr()
+                else:
+                    c.read_scale, c.read_scale_slot_stride = self.read_scale.data_ptr(), self.read_scale.shape[1]
             self._struct = c
         return ctypes.byref(self._struct)
 

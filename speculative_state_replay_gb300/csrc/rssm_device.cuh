@@ -489,4 +489,60 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
   }
 }
 
+// --------------------------------------------------------------------------
+// NVFP4 read checkpoint: FP4 E2M1 codes (magnitudes 0, 0.5, 1, 1.5, 2, 3, 4,
+// 6; code = sign << 3 | magnitude index), one E4M3 scale per 16 consecutive
+// dstate values, one FP32 global scale gs per slot.
+// --------------------------------------------------------------------------
+// E2M1 nearest (ties to the even code), saturating at 6, keeping the sign of
+// v (also for values that round to zero): the grid step is 0.5 below 2, 1 in
+// [2, 4), 2 from 4 on, so |v| / step and the rounding are exact operations.
+__device__ __forceinline__ uint32_t e2m1_nearest(float v) {
+  const float a = fabsf(v);
+  const float q = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
+  const float mag = fminf(__fmul_rn(rintf(__fdiv_rn(a, q)), q), 6.0f);  // a grid point
+  const uint32_t m = (mag > 0.25f ? 1u : 0u) + (mag > 0.75f ? 1u : 0u) + (mag > 1.25f ? 1u : 0u) +
+                     (mag > 1.75f ? 1u : 0u) + (mag > 2.5f ? 1u : 0u) + (mag > 3.5f ? 1u : 0u) +
+                     (mag > 5.0f ? 1u : 0u);
+  return m | ((__float_as_uint(v) >> 28) & 8u);
+}
+
+// Four E2M1 codes (the nibbles of w, lowest first) as two fp16 pairs, exactly:
+// the fp16 value of each magnitude has a zero low byte, so its high byte comes
+// from an 8-entry table by byte permutation, and the code's sign bit becomes
+// the fp16 sign bit.
+__device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t mags = __byte_perm(0x3E3C3800u, 0x46444240u, w & 0x7777u);  // high bytes of 0,.5,1,1.5 | 2,3,4,6
+  const uint32_t sgn = ((w & 0x8u) << 4) | ((w & 0x80u) << 8) | ((w & 0x800u) << 12) | ((w & 0x8000u) << 16);
+  const uint32_t hb = mags | sgn;
+  lo = __byte_perm(hb, 0u, 0x1404u);  // (codes 0, 1)
+  hi = __byte_perm(hb, 0u, 0x3424u);  // (codes 2, 3)
+}
+
+// NVFP4 encoding of the lane's 4 x 8 fp32 values (rows r0..r0+3, columns
+// c0..c0+7 of a [64][128] head; lanes 2k and 2k+1 hold the two halves of a
+// 16-value block) into the head's codes [64][64 bytes] and block scales
+// [64][8]: sf = e4m3 nearest of (block max / (6 gs)), code = e2m1 nearest of
+// (v / (gs * sf)) (0 where sf is 0).
+__device__ __forceinline__ void quantize_store_nvfp4(const float (&acc)[4][8], int r0, int c0, int lane,
+                                                     uint8_t* head_codes, uint8_t* head_sf, float gs) {
+  const float den = __fmul_rn(6.0f, gs);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float m = 0.0f;
+#pragma unroll
+    for (int q = 0; q < 8; ++q) m = fmaxf(m, fabsf(acc[i][q]));
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    const uint8_t sc = static_cast<uint8_t>(__nv_cvt_float_to_fp8(__fdiv_rn(m, den), __NV_SATFINITE, __NV_E4M3));
+    const float qs = __fmul_rn(e4m3_to_f32(sc), gs);
+    uint32_t word = 0u;
+    if (qs > 0.0f) {
+#pragma unroll
+      for (int q = 0; q < 8; ++q) word |= e2m1_nearest(__fdiv_rn(acc[i][q], qs)) << (4 * q);
+    }
+    *reinterpret_cast<uint32_t*>(head_codes + (r0 + i) * 64 + c0 / 2) = word;
+    if (!(lane & 1)) head_sf[(r0 + i) * 8 + c0 / 16] = sc;
+  }
+}
+
 }  // namespace rssm

@@ -162,6 +162,13 @@ constexpr int kMmaMinP = 9;
 // 8-bit read format with nearest rounding and per-row scales
 __device__ __forceinline__ void store_read_checkpoint(const Cache& c, float (&acc)[4][8], int r0, int c0, int lane,
                                                       int s, int h) {
+  if (c.read_dtype == RSSM_NVFP4) {  // codes [64][64 bytes] and block scales [64][8] of the head
+    uint8_t* rs = static_cast<uint8_t*>(c.read_state) + static_cast<long long>(s) * c.read_stride +
+                  static_cast<long long>(h) * (kHeadElems / 2);
+    uint8_t* sf = c.read_sf + static_cast<long long>(s) * c.read_sf_stride + h * kDim * 8;
+    quantize_store_nvfp4(acc, r0, c0, lane, rs, sf, c.read_gs[s]);
+    return;
+  }
   uint8_t* rs = static_cast<uint8_t*>(c.read_state) +
                 static_cast<long long>(s) * c.read_stride + static_cast<long long>(h) * kHeadElems;
   float* rsc = c.read_scale + static_cast<long long>(s) * c.read_scale_stride + h * kDim;
@@ -583,6 +590,40 @@ __global__ void __launch_bounds__(kConsumerThreads) init_quant_kernel(InitArgs a
   if (c.read_state) store_read_checkpoint(c, acc, r0, c0, lane, s, h);
 }
 
+// NVFP4 read checkpoint: each initialised slot's global scale = the largest
+// magnitude of its FP32 prefill state (all heads) / (6 * 448), 1 for a zero
+// state.  Three steps: zero the slot's word; per (state, head) the head's
+// largest magnitude merged by an integer atomic max on the float's bits (the
+// bit patterns of non-negative floats order like their values); the scale.
+__global__ void __launch_bounds__(64) init_gs_zero_kernel(InitArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  const int s = a.ids[i];
+  if (s >= 1 && s < a.c.S) a.c.read_gs[s] = 0.0f;
+}
+__global__ void __launch_bounds__(256) init_gs_max_kernel(InitArgs a) {
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int s = a.ids[i];
+  if (s < 1 || s >= a.c.S) return;
+  const float4* src = reinterpret_cast<const float4*>(a.states + (static_cast<long long>(i) * a.c.H + h) * kHeadElems);
+  float m = 0.0f;
+  for (int k = threadIdx.x; k < kHeadElems / 4; k += blockDim.x) {
+    const float4 v = src[k];
+    m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+  if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned*>(a.c.read_gs + s), __float_as_uint(m));
+}
+__global__ void __launch_bounds__(64) init_gs_scale_kernel(InitArgs a) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= a.n) return;
+  const int s = a.ids[i];
+  if (s < 1 || s >= a.c.S) return;
+  const float m = a.c.read_gs[s];
+  a.c.read_gs[s] = m > 0.0f ? __fdiv_rn(m, 2688.0f) : 1.0f;
+}
+
 __global__ void __launch_bounds__(256) init_clear_kernel(InitArgs a) {
   const Cache& c = a.c;
   const int s = a.ids[blockIdx.x];
@@ -717,6 +758,14 @@ int launch_flush(const FlushArgs& a, int num_sms, void* stream) {
 int launch_init(const InitArgs& a, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dim3 grid(a.n, a.c.H);
+  if (a.c.read_state && a.c.read_dtype == RSSM_NVFP4) {  // the slots' global scales first
+    const int nb = (a.n + 63) / 64;
+    init_gs_zero_kernel<<<nb, 64, 0, st>>>(a);
+    init_gs_max_kernel<<<grid, 256, 0, st>>>(a);
+    init_gs_scale_kernel<<<nb, 64, 0, st>>>(a);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
   switch (a.c.dtype) {
     case RSSM_F32: init_quant_kernel<RSSM_F32><<<grid, kConsumerThreads, 0, st>>>(a); break;
     case RSSM_BF16: init_quant_kernel<RSSM_BF16><<<grid, kConsumerThreads, 0, st>>>(a); break;

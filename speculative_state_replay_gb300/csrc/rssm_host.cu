@@ -33,7 +33,7 @@ rssm_status check_cache(const rssm_cache* c, Cache* out) {
   if (c->max_window < 0 || c->npredicted < 1) return RSSM_ERR_INVALID_ARGUMENT;
   const int L = c->max_window + c->npredicted;
   if (L > kMaxL) return RSSM_ERR_UNSUPPORTED;
-  const int esz = elem_bytes(c->state_dtype);
+  const int esz = c->state_dtype == RSSM_NVFP4 ? 0 : elem_bytes(c->state_dtype);  // NVFP4: read format only
   if (!esz) return RSSM_ERR_INVALID_ARGUMENT;
   if (c->rounding != RSSM_ROUND_NEAREST && c->rounding != RSSM_ROUND_STOCHASTIC) return RSSM_ERR_INVALID_ARGUMENT;
   const bool q8 = c->state_dtype == RSSM_I8 || c->state_dtype == RSSM_E4M3;
@@ -52,11 +52,19 @@ rssm_status check_cache(const rssm_cache* c, Cache* out) {
   if (c->B_slot_stride < G * L * kDstate || (c->B_slot_stride * 2) % 16) return RSSM_ERR_INVALID_ARGUMENT;
   if (c->dt_slot_stride < H * L) return RSSM_ERR_INVALID_ARGUMENT;
   if (c->read_state) {
-    if (c->read_dtype != RSSM_I8 && c->read_dtype != RSSM_E4M3) return RSSM_ERR_INVALID_ARGUMENT;
-    if (!c->read_scale || !aligned16(c->read_state) || !aligned16(c->read_scale)) return RSSM_ERR_INVALID_ARGUMENT;
-    if (c->read_slot_stride < H * kHeadElems || c->read_slot_stride % 16) return RSSM_ERR_INVALID_ARGUMENT;
-    if (c->read_scale_slot_stride < H * kDim || (c->read_scale_slot_stride * 4) % 16)
-      return RSSM_ERR_INVALID_ARGUMENT;
+    if (c->read_dtype == RSSM_NVFP4) {
+      if (!c->read_sf || !c->read_gs || !aligned16(c->read_state) || !aligned16(c->read_sf) ||
+          (reinterpret_cast<uintptr_t>(c->read_gs) & 3u))
+        return RSSM_ERR_INVALID_ARGUMENT;
+      if (c->read_slot_stride < H * kHeadElems / 2 || c->read_slot_stride % 16) return RSSM_ERR_INVALID_ARGUMENT;
+      if (c->read_sf_slot_stride < H * kDim * 8 || c->read_sf_slot_stride % 16) return RSSM_ERR_INVALID_ARGUMENT;
+    } else {
+      if (c->read_dtype != RSSM_I8 && c->read_dtype != RSSM_E4M3) return RSSM_ERR_INVALID_ARGUMENT;
+      if (!c->read_scale || !aligned16(c->read_state) || !aligned16(c->read_scale)) return RSSM_ERR_INVALID_ARGUMENT;
+      if (c->read_slot_stride < H * kHeadElems || c->read_slot_stride % 16) return RSSM_ERR_INVALID_ARGUMENT;
+      if (c->read_scale_slot_stride < H * kDim || (c->read_scale_slot_stride * 4) % 16)
+        return RSSM_ERR_INVALID_ARGUMENT;
+    }
   }
   if (out) {
     Cache& v = *out;
@@ -87,6 +95,11 @@ rssm_status check_cache(const rssm_cache* c, Cache* out) {
     v.read_scale = c->read_state ? c->read_scale : nullptr;
     v.read_scale_stride = c->read_state ? c->read_scale_slot_stride : 0;
     v.read_dtype = c->read_state ? c->read_dtype : -1;
+    const bool fp4 = c->read_state && c->read_dtype == RSSM_NVFP4;
+    v.read_sf = fp4 ? static_cast<uint8_t*>(c->read_sf) : nullptr;
+    v.read_sf_stride = fp4 ? c->read_sf_slot_stride : 0;
+    v.read_gs = fp4 ? c->read_gs : nullptr;
+    if (fp4) v.read_scale = nullptr;
   }
   return RSSM_OK;
 }
@@ -148,8 +161,7 @@ rssm_status step_common(const rssm_cache* cache, const void* x, const float* dt,
   a->flush_mode = 0;
   a->seed = 0;
   a->pnat_rw = nullptr;
-  a->work = nullptr;
-  a->gdone = nullptr;
+  a->fw = nullptr;
   a->rwork = static_cast<unsigned*>(scratch) + 2;  // a word of the scratch head (the flush uses words 0, 1)
   uint8_t* sc = static_cast<uint8_t*>(scratch) + kScratchHead;  // past the flush's ticket word
   a->rows = reinterpret_cast<RowRec*>(sc);
@@ -297,9 +309,8 @@ rssm_status flush_step_args(const rssm_cache* cache, const void* x, const float*
   a->flush_mode = 1 + force;
   a->seed = seed;
   a->pnat_rw = pnat;
-  a->work = reinterpret_cast<unsigned*>(static_cast<uint8_t*>(scratch) +
-                                        step_scratch_bytes(batch, cache->nheads, cache->ngroups, a->c.L, T));
-  a->gdone = a->work + 64;  // 256 bytes past the work counter
+  a->fw = reinterpret_cast<float*>(static_cast<uint8_t*>(scratch) +
+                                   step_scratch_bytes(batch, cache->nheads, cache->ngroups, a->c.L, T));
   return RSSM_OK;
 }
 }  // namespace
@@ -314,7 +325,8 @@ rssm_status rssm_flush_step_classify(const rssm_cache* cache, const void* x, con
   rssm_status st = flush_step_args(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force,
                                    seed, out, scratch, scratch_bytes, &a, &sms);
   if (st != RSSM_OK || batch == 0) return st;
-  return launch_classify(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+  if (static_cast<long long>(batch) * a.c.G > 0x7fffffffLL) return RSSM_ERR_UNSUPPORTED;
+  return launch_precompute(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
 rssm_status rssm_flush_step_main(const rssm_cache* cache, const void* x, const float* dt, const float* A,
@@ -327,7 +339,7 @@ rssm_status rssm_flush_step_main(const rssm_cache* cache, const void* x, const f
   rssm_status st = flush_step_args(cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, cu_seqlens, batch, T, force,
                                    seed, out, scratch, scratch_bytes, &a, &sms);
   if (st != RSSM_OK || batch == 0) return st;
-  return launch_flush_step(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+  return launch_readout_fold(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
 rssm_status rssm_flush_step(const rssm_cache* cache, const void* x, const float* dt, const float* A, const void* B,

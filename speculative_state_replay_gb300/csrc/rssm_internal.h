@@ -14,7 +14,12 @@ constexpr int kDstate = 128;  // state dim
 constexpr int kHeadElems = kDim * kDstate;
 constexpr int kMaxL = 32;     // ring length the kernels are built for (one lane per ring slot)
 constexpr int kMaxT = 8;      // draft tokens per step
-constexpr int kRStride = 72;  // row stride (floats) of the ring-term block R[t][64]: rows 8 banks apart
+constexpr int kRStride = 72;  // row stride (floats) of the one-call path's ring-term rows in shared memory
+// ring-term block of one (row, head) in the step's scratch: kRDec decay floats
+// (decay[t] for t < T, padded), then one 64-float row R[t][.] per token, the
+// 32-byte chunk c of row t stored at chunk c ^ t (conflict-free reads of one
+// column chunk across the rows); only the row's T_b rows are written and read
+constexpr int kRDec = 8;
 constexpr int kConsumerWarps = 8;
 constexpr int kConsumerThreads = kConsumerWarps * 32;
 constexpr int kThreads = kConsumerThreads + 32;  // + one producer warp
@@ -37,12 +42,16 @@ struct Cache {
   int* ring_start;
   unsigned* epoch;
   unsigned* err;
-  // separate read checkpoint (8-bit codes + row scales, nearest), or null
+  // separate read checkpoint (8-bit codes + row scales, or NVFP4 codes +
+  // block scales + per-slot global scale; nearest), or null
   void* read_state;
   long long read_stride;
   float* read_scale;
   long long read_scale_stride;
   int read_dtype;
+  uint8_t* read_sf;
+  long long read_sf_stride;
+  float* read_gs;
 };
 
 // one flagged row of a flush (written by the flag kernel), 32 bytes
@@ -53,14 +62,19 @@ struct FlushRec {
 };
 
 // one row of a step (written by the precompute, read by the readout), 32 bytes.
-// r and p are the ring start and live count the step works on (after the
-// flush when the flush is part of the call).
+// r and p are the ring start and live count the step works on: the live
+// prefix the outputs replay and, for a row flushed in the same call, the
+// prefix the fold folds.
 struct RowRec {
   int s, r, p, Tb, tok0;
-  int flags;           // bit 0: compute the row's outputs (else zeros for Tb tokens); bit 1: fold it first
-  int p_old;           // live count before the flush (bit 1 set)
+  int flags;           // bit 0: compute the row's outputs (else zeros for Tb tokens); bit 1: fold its live prefix
   unsigned epoch_new;  // epoch of the checkpoint the fold writes (bit 1 set)
+  float gs;            // global scale of the slot's NVFP4 read checkpoint (1 otherwise)
 };
+
+// fold weights of one flushed (row, head) in the one-call path's scratch:
+// w_j = e^{c_end - c_j} dt'_j for j < p (canonical fp32), then e^{c_end} at 32
+constexpr int kFoldW = 40;
 
 struct FlushArgs {
   Cache c;
@@ -92,15 +106,14 @@ struct StepArgs {
   int KB;  // ring rows padded to a multiple of 4
   uint16_t* out;
   const uint16_t* z;         // output gate [tok][H][64] bf16, or null: y * silu(z) (the readout)
-  int flush_mode;            // rssm_flush_step: 1 flush rows with p + T_b > W first; 2 every active row
+  int flush_mode;            // rssm_flush_step: 1 fold rows with p + T_b > W; 2 every active row; 0 none
   unsigned long long seed;   // stochastic-rounding key of the fold (flush_mode != 0)
   int* pnat_rw;              // pnat, written by the fold's bookkeeping (flush_mode != 0)
-  unsigned* work;            // scratch: dynamic work counter of the step kernel (rssm_flush_step)
+  float* fw;                 // scratch [batch][H][kFoldW]: fold weights of flushed rows (flush_mode != 0)
   unsigned* rwork;           // scratch word: the readout's chunk counter, zeroed by the precompute
-  unsigned* gdone;           // scratch [batch][G]: heads of a (row, group) whose ring rows have landed
   RowRec* rows;  // scratch [batch]
   uint16_t* cf;  // scratch [batch][G][8][128]: C rows in the readout's MMA operand type
-  float* rblk;   // scratch [batch][H][TP*kRStride + TP]: ring term R[t][d] (rows padded), then decay[t]
+  float* rblk;   // scratch [batch][H][kRDec + TP*64]: decay[t], then the ring term R[t][d] (chunk-swizzled rows)
 };
 
 struct InitArgs {
@@ -111,7 +124,7 @@ struct InitArgs {
   unsigned long long seed;
 };
 
-inline int ring_pad(int L) { return (L + 3) & ~3; }
+__host__ __device__ inline int ring_pad(int L) { return (L + 3) & ~3; }
 inline int t_pad(int T) { return T <= 4 ? 4 : 8; }
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -124,24 +137,24 @@ inline size_t step_cf_bytes(int batch, int G, int T) {
   (void)T;
   return align_up((size_t)batch * G * 8 * 128 * 2, 256);
 }
-inline size_t step_rblk_floats(int T) { return (size_t)t_pad(T) * kRStride + t_pad(T); }
+inline size_t step_rblk_floats(int T) { return kRDec + (size_t)t_pad(T) * kDim; }
+// float offset of R[t][d] inside a ring-term block
+__host__ __device__ inline int rblk_offset(int t, int d) { return kRDec + t * kDim + ((((d >> 3) ^ t) & 7) << 3) + (d & 7); }
 inline size_t step_scratch_bytes(int batch, int H, int G, int L, int T) {
   (void)L;
   const size_t blk = step_rblk_floats(T) * sizeof(float);
   return kScratchHead + step_rows_bytes(batch) + step_cf_bytes(batch, G, T) + align_up(blk * (size_t)batch * H, 256);
 }
-// the flush+step call: the step's scratch, then the work counter, then the
-// per-(row, group) landed-head counters
+// the flush+step call: the step's scratch, then the fold weights
 inline size_t flush_step_scratch_bytes(int batch, int H, int G, int L, int T) {
-  return step_scratch_bytes(batch, H, G, L, T) + 256 + align_up((size_t)batch * G * 4, 256);
+  return step_scratch_bytes(batch, H, G, L, T) + align_up((size_t)batch * H * kFoldW * sizeof(float), 256);
 }
 
 // launchers (defined in the .cu files); return a cudaError_t as int
 int launch_flush(const FlushArgs& a, int num_sms, void* stream);
 int launch_precompute(const StepArgs& a, void* stream);
 int launch_readout(const StepArgs& a, int num_sms, void* stream);
-int launch_classify(const StepArgs& a, void* stream);
-int launch_flush_step(const StepArgs& a, int num_sms, void* stream);
+int launch_readout_fold(const StepArgs& a, int num_sms, void* stream);
 int launch_accept(const Cache& c, const int* slot_idx, int* pnat, const int* accepted, const int* cu, int batch,
                   int T, void* stream);
 int launch_init(const InitArgs& a, void* stream);

@@ -48,32 +48,48 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2,
 constexpr int kReadChunk = 4;  // (row, head) units per work grab of the readout
 
 struct ReadMeta {
-  int b, h, s, r, p, Tb, tok0, flags;
+  int b, h, s, r, p, Tb, tok0, flags;  // flags: 1 outputs, 2 new C block, 8 no more work, 16 fold
+  unsigned epoch;                      // epoch of the checkpoint a fold writes
+  float gs;                            // NVFP4: the slot's global scale
+  int pad[2];
 };
 
 struct ReadLayout {
   int ns;
   uint32_t s0_bytes, scale_off, c_off, r_off, r_bytes, stage_bytes;
+  uint32_t fx_off, fb_off, fw_off;  // fold area (fold_kb > 0): live x rows, live B rows, fold weights
   uint32_t stages_off, total;
 };
 
 // one stage of a unit of `hpu` consecutive heads of one group: S0 as esz
-// boxes of 64*hpu rows x 128 bytes | 8-bit scales | C block | ring terms
-__host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int hpu = 1) {
+// boxes of 64*hpu rows x 128 bytes | 8-bit scales | C block | ring-term blocks
+// [| fold area: the heads' live x rows [hpu][fold_kb][64], the group's live B
+// rows [fold_kb][128], the heads' fold weights [hpu][kFoldW]]
+__host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int hpu = 1, int fold_kb = 0) {
   ReadLayout f;
   f.ns = ns;
   const int esz = dtype == RSSM_F32 ? 4 : (dtype == RSSM_BF16 || dtype == RSSM_F16) ? 2 : 1;
-  f.s0_bytes = kHeadElems * esz * hpu;
+  f.s0_bytes = dtype == RSSM_NVFP4 ? kHeadElems / 2 * hpu : kHeadElems * esz * hpu;
   uint32_t o = f.s0_bytes;
-  f.scale_off = o;
+  f.scale_off = o;  // 8-bit: row scales [64 hpu] f32; NVFP4: block scales [64 hpu][8] e4m3
   if (dtype == RSSM_I8 || dtype == RSSM_E4M3) o += 256 * hpu;
+  if (dtype == RSSM_NVFP4) o += 512 * hpu;
   f.c_off = o;
   o += 8 * kDstate * 2;
   f.r_off = o;
-  f.r_bytes = (TP * kRStride + TP) * 4 * hpu;
+  f.r_bytes = (kRDec + TP * kDim) * 4 * hpu;  // room for the full ring-term blocks (a unit copies its T_b rows)
   o += f.r_bytes;
+  f.fx_off = f.fb_off = f.fw_off = 0;
+  if (fold_kb > 0) {
+    f.fx_off = o;
+    o += hpu * fold_kb * kDim * 2;
+    f.fb_off = o;
+    o += fold_kb * kDstate * 2;
+    f.fw_off = o;
+    o += hpu * kFoldW * 4;
+  }
   f.stage_bytes = (o + 1023) & ~1023u;  // the swizzled boxes need 1024-byte alignment
-  f.stages_off = 1024;                  // barriers and per-stage metadata
+  f.stages_off = 1024;                  // barriers and per-stage metadata (8 x 48 bytes at 256)
   f.total = f.stages_off + ns * f.stage_bytes + 1024;  // + slack to align the base
   return f;
 }
@@ -109,8 +125,10 @@ __device__ __forceinline__ void load_c_frags(const uint16_t* cblk, int g, int c,
 // S0 . C over dstate for state rows d (lane's B column) of this warp; even and
 // odd k steps accumulate in separate chains, added at the end
 // (BOXB: bytes between the column boxes of a 2- or 4-byte state)
+// (NVFP4: sfrow = the 8 block scales of row d)
 template <int DT, int BOXB = 8192>
-__device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8], int d, int c, float (&acc)[4]) {
+__device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8], int d, int c, float (&acc)[4],
+                                         uint64_t sfrow = 0) {
   float a2[2][4] = {{0.0f, 0.0f, 0.0f, 0.0f}, {0.0f, 0.0f, 0.0f, 0.0f}};
 #pragma unroll
   for (int ks = 0; ks < 8; ++ks) {
@@ -131,6 +149,19 @@ __device__ __forceinline__ void s0_dot_c(const uint8_t* s0, const uint2 (&af)[8]
       const uint32_t l23 = pack_bf16(f.z - bf16_lo_f(h23), f.w - bf16_hi_f(h23));
       mma_bf16(a2[0], av.x, av.y, h01, h23);
       mma_bf16(a2[1], av.x, av.y, l01, l23);
+    } else if constexpr (DT == RSSM_NVFP4) {
+      // rows d and d + 1 share one 128-byte tensor row (64 bytes of codes
+      // each); 4 codes = 2 bytes; the block scale of these 16 values is
+      // byte ks of the row's 8 (sfrow), applied exactly in fp16
+      const uint32_t w = *reinterpret_cast<const uint16_t*>(s0 + swz(d >> 1, (d & 1) * 64 + 8 * ks + 2 * c));
+      uint32_t lo, hi;
+      e2m1x4_to_f16x2(w, lo, hi);
+      const __half_raw sr = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>((sfrow >> (8 * ks)) & 0xffu),
+                                                    __NV_E4M3);
+      const __half2 s2 = __halves2half2(__half(sr), __half(sr));
+      const __half2 h01 = __hmul2(*reinterpret_cast<const __half2*>(&lo), s2);
+      const __half2 h23 = __hmul2(*reinterpret_cast<const __half2*>(&hi), s2);
+      mma_f16(ac, av.x, av.y, *reinterpret_cast<const uint32_t*>(&h01), *reinterpret_cast<const uint32_t*>(&h23));
     } else {
       const uint32_t w = *reinterpret_cast<const uint32_t*>(s0 + swz(d, ks * 16 + 4 * c));
       uint32_t b0, b1;
@@ -176,6 +207,17 @@ inline PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 inline bool encode_state_map(const Cache& c, CUtensorMap* map, int hpu = 1) {
   auto enc = tensor_map_encoder();
   if (!enc) return false;
+  if (c.dtype == RSSM_NVFP4) {
+    // codes as [slot][H*32 rows][128 bytes] (two state rows per tensor row);
+    // boxes of 32*hpu tensor rows (hpu heads) x 128 bytes, 128-byte swizzle
+    const cuuint64_t dims[3] = {128, static_cast<cuuint64_t>(c.H) * 32, static_cast<cuuint64_t>(c.S)};
+    const cuuint64_t strides[2] = {128, static_cast<cuuint64_t>(c.state_stride)};
+    const cuuint32_t box[3] = {128, static_cast<cuuint32_t>(32 * hpu), 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, c.state, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  }
   const int esz = c.dtype == RSSM_F32 ? 4 : (c.dtype == RSSM_BF16 || c.dtype == RSSM_F16) ? 2 : 1;
   const CUtensorMapDataType dt = esz == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                           : (esz == 2 ? CU_TENSOR_MAP_DATA_TYPE_UINT16 : CU_TENSOR_MAP_DATA_TYPE_UINT8);

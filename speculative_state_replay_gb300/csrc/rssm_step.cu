@@ -9,8 +9,8 @@
 //           coef[k][t] = e^{c_{p+t} - c_k} dt'_k CB[t][k]  (+ D on k = p+t)
 //       which it applies at once to the head's x rows:
 //           R[t][d] = sum_k coef[k][t] x_k[d],   decay[t] = e^{c_{p+t}}
-//       written to scratch with the C rows (in the readout's MMA type).
-//       Appends B, x and dt'.
+//       written to scratch (the row's T_b rows) with the C rows (in the
+//       readout's MMA type).  Appends B, x and dt'.
 //   readout_kernel  persistent, one (row, head) unit at a time:
 //           y_t[d] = decay[t] (S0[d] . C_t) + R[t][d]
 //       streaming S0 once through a multi-stage shared-memory ring filled by
@@ -39,6 +39,9 @@ __host__ __device__ inline int head_chunk(int hpg) { return hpg < kHeadChunk ? h
 inline size_t precompute_smem(int hpg, int L) {
   return static_cast<size_t>(head_chunk(hpg)) * L * kDim * 2 + static_cast<size_t>(L) * kDstate * 2 + 8 * kDstate * 2;
 }
+// element offset of chunk q (8 elements) of x row k in xs
+__device__ __forceinline__ int xs_chunk(int k, int q) { return k * kDim + (q << 3); }
+
 
 template <int TP>
 __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepArgs a) {
@@ -47,7 +50,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   __shared__ float dts[kHeadChunk][kMaxL];  // dt' of the live tokens; dt of the new ones (before bias, softplus)
   __shared__ float hp[3][kHeadChunk];       // A, D, dt_bias of the chunk's heads
   __shared__ __align__(16) float cfs[8][kMaxL][TP];  // per warp: coef[k][t] of its current head
-  __shared__ int meta[6];
+  __shared__ int meta[7];
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -68,6 +71,8 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
     const int tok0 = __shfl_sync(0xffffffffu, v, 2), tok1 = __shfl_sync(0xffffffffu, v, 3);
     if (lane == 0) {
       int Tb = tok1 - tok0, flags = 0, p = 0, r = 0;
+      unsigned ep = 0u;
+      float gs = 1.0f;
       const bool tb_ok = Tb >= 0 && Tb <= a.T;
       if (s >= 1 && s < c.S) {
         if (!tb_ok) {
@@ -77,18 +82,27 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
         } else {
           p = pn;
           r = c.ring_start[s];
+          if (c.dtype == RSSM_NVFP4) gs = c.read_gs[s];
           flags = 1;
+          // the one-call path: the flush decision (the flush's rule); the row's
+          // outputs still replay its whole live prefix from the old checkpoint
+          // and the readout folds that prefix into the new one
+          if (a.flush_mode && (a.flush_mode == 2 || pn + Tb > c.W)) {
+            flags |= 2;
+            ep = c.epoch[s] + 1u;
+          }
         }
       }
       if (!tb_ok) Tb = 0;
-      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags;
-      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, p, 0u};
+      meta[0] = s; meta[1] = r; meta[2] = p; meta[3] = Tb; meta[4] = tok0; meta[5] = flags & 1; meta[6] = flags & 2;
+      if (g == 0) a.rows[b] = RowRec{s, r, p, Tb, tok0, flags, ep, gs};
       if (blockIdx.x == 0) *a.rwork = 0u;  // the readout's chunk counter
     }
   }
   __syncthreads();
   const int s = meta[0], r = meta[1], p = meta[2], Tb = meta[3], tok0 = meta[4];
-  if (!meta[5] || Tb == 0) return;
+  const bool fold = meta[6] != 0;
+  if (!meta[5] || (Tb == 0 && !fold)) return;
   const int K = p + Tb;  // logical tokens: p live ring rows, then the Tb new ones
   auto ring = [&](int k) {  // ring slot of logical token k < L
     const int q = r + k;
@@ -108,7 +122,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
     const int t = tid >> 4, q = tid & 15;
     cp_async16(cs + t * kDstate + q * 8, a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate + q * 8);
   }
-  const bool c_f16 = c.dtype == RSSM_F16 || c.dtype == RSSM_I8 || c.dtype == RSSM_E4M3;
+  const bool c_f16 = c.dtype == RSSM_F16 || c.dtype == RSSM_I8 || c.dtype == RSSM_E4M3 || c.dtype == RSSM_NVFP4;
   for (int h0 = 0; h0 < hpg; h0 += kHeadChunk) {
     const int hc = hpg - h0 < kHeadChunk ? hpg - h0 : kHeadChunk, hb = g * hpg + h0;
     if (h0) __syncthreads();  // every warp is done with the previous chunk's rows
@@ -118,7 +132,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
         const int k = q >> 3, part = q & 7;
         const uint16_t* src = k < p ? xslot + (static_cast<long long>(hb + hh) * L + ring(k)) * kDim
                                     : a.x + (static_cast<long long>(tok0 + k - p) * H + hb + hh) * kDim;
-        cp_async16(xs + (hh * L + k) * kDim + part * 8, src + part * 8);
+        cp_async16(xs + hh * L * kDim + xs_chunk(k, part), src + part * 8);
       }
     }
     for (int idx = tid; idx < hc * 32; idx += 256) {
@@ -194,13 +208,29 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       const int hh = idx >> 6, t = (idx >> 3) & 7, q = idx & 7;
       if (t < Tb)
         reinterpret_cast<uint4*>(xslot + (static_cast<long long>(hb + hh) * L + ring(p + t)) * kDim)[q] =
-            reinterpret_cast<const uint4*>(xs + (hh * L + p + t) * kDim)[q];
+            *reinterpret_cast<const uint4*>(xs + hh * L * kDim + xs_chunk(p + t, q));
     }
     if (h0) __syncthreads();  // the chunk's dt' (the first chunk synchronised above)
     for (int hh = warp; hh < hc; hh += 8) {
       const int h = hb + hh;
       const float Ah = hp[0][hh], Dh = hp[1][hh];
       const float dtp = lane < K ? dts[hh][lane] : 0.0f;
+      if (fold) {
+        // the fold's weights in the flush's canonical fp32 order (they decide
+        // stored bits): c_j = sum_{i<=j} A dt'_i sequentially over the live
+        // prefix, w_j = e^{c_end - c_j} dt'_j, and e^{c_end}
+        const float aj = lane < p ? __fmul_rn(Ah, dtp) : 0.0f;
+        float cj = 0.0f;
+        for (int k = 0; k < p; ++k) {
+          const float ak = __shfl_sync(0xffffffffu, aj, k);
+          if (lane >= k) cj = __fadd_rn(cj, ak);
+        }
+        const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
+        float* fwb = a.fw + (static_cast<long long>(b) * H + h) * kFoldW;
+        fwb[lane] = lane < p ? __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtp) : 0.0f;
+        if (lane == 0) fwb[32] = spec_exp(c_end);
+      }
+      if (Tb == 0) continue;  // nothing to read out (a fold of a row without tokens)
       // inclusive prefix sum of A dt' over the lanes (these sums only feed the
       // outputs, so any summation order is fine here)
       float cum = lane < K ? Ah * dtp : 0.0f;
@@ -223,8 +253,17 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
         cf[t] = v;
         dec[t] = t < Tb ? __expf(cpt) : 0.0f;
       }
+      float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (kRDec + TP * kDim);
+      if (lane == 0) {
+        float4* d4 = reinterpret_cast<float4*>(blk);
+        d4[0] = make_float4(dec[0], dec[1], dec[2], dec[3]);
+        d4[1] = TP == 8 ? make_float4(dec[TP > 4 ? 4 : 0], dec[TP > 5 ? 5 : 0], dec[TP > 6 ? 6 : 0],
+                                      dec[TP > 7 ? 7 : 0])
+                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      }
       // ring term of this head: R[t][d] = sum_k coef[k][t] x_k[d]; lane k
-      // holds coef[k][.], shared through cfs; lane l accumulates d = 2l, 2l + 1
+      // holds coef[k][.], shared through cfs; lane l accumulates d = 2l, 2l + 1;
+      // blocks of 4 tokens at or past T_b are skipped (zero coefficients)
 #pragma unroll
       for (int t4 = 0; t4 < TP; t4 += 4)
         *reinterpret_cast<float4*>(&cfs[warp][lane][t4]) = make_float4(cf[t4], cf[t4 + 1], cf[t4 + 2], cf[t4 + 3]);
@@ -233,12 +272,14 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 #pragma unroll
       for (int t = 0; t < TP; ++t) R[t] = make_float2(0.0f, 0.0f);
       const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + hh * L * kDim) + lane;
+      const bool hi4 = TP > 4 && Tb > 4;
 #pragma unroll 4
       for (int k = 0; k < K; ++k) {
         const uint32_t w = xr[k * (kDim / 2)];
         const float2 xv = make_float2(bf16lo(w), bf16hi(w));
 #pragma unroll
         for (int t4 = 0; t4 < TP; t4 += 4) {
+          if (t4 > 0 && !hi4) continue;
           const float4 cv = *reinterpret_cast<const float4*>(&cfs[warp][k][t4]);
           R[t4 + 0] = __ffma2_rn(make_float2(cv.x, cv.x), xv, R[t4 + 0]);
           R[t4 + 1] = __ffma2_rn(make_float2(cv.y, cv.y), xv, R[t4 + 1]);
@@ -246,16 +287,107 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
           R[t4 + 3] = __ffma2_rn(make_float2(cv.w, cv.w), xv, R[t4 + 3]);
         }
       }
+      // the row's T_b rows, chunk-swizzled (rblk_offset)
+#pragma unroll
+      for (int t = 0; t < TP; ++t)
+        if (t < Tb) *reinterpret_cast<float2*>(blk + rblk_offset(t, 2 * lane)) = R[t];
       __syncwarp();  // cfs is rewritten for the warp's next head
-      float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (TP * kRStride + TP);
-#pragma unroll
-      for (int t = 0; t < TP; ++t) reinterpret_cast<float2*>(blk + t * kRStride)[lane] = R[t];
-      if (lane == 0) {
-#pragma unroll
-        for (int t4 = 0; t4 < TP; t4 += 4)
-          *reinterpret_cast<float4*>(blk + TP * kRStride + t4) = make_float4(dec[t4], dec[t4 + 1], dec[t4 + 2], dec[t4 + 3]);
-      }
     }
+  }
+}
+
+// ---------------------------------------------------------------------------
+// the one-call path's fold, from a readout stage
+// ---------------------------------------------------------------------------
+// Folds the unit's HPU heads in the flush's canonical fp32 order and stores the
+// new checkpoints (and 8-bit row scales): for each of the warp's 8 state rows
+// (lane: rows r0..r0+3, columns c0..c0+7)
+//     acc = e^{c_end} S0f;  acc = fma(w_j x_j[d], B_j[n], acc) for j ascending
+// with S0f read from the stage's TMA boxes (the checkpoint the outputs were
+// just read from), the live x and B rows and the weights from the stage's fold
+// area, then the flush's quantiser -- the operations rssm_flush performs.
+template <int DT, int HPU>
+__device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& lay, int fold_kb, const ReadMeta& m,
+                                           int warp, int lane, const StepArgs& a) {
+  const Cache& c = a.c;
+  constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
+  constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
+  const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
+  const int p = m.p;
+  const uint16_t* bs = reinterpret_cast<const uint16_t*>(sb + lay.fb_off);
+#pragma unroll 1
+  for (int j = 0; j < HPU; ++j) {
+    const float* fw = reinterpret_cast<const float*>(sb + lay.fw_off) + j * kFoldW;
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.fx_off) + j * fold_kb * kDim;
+    const float decay = fw[32];
+    float2 acc[4][4];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4) {
+      const int row = 64 * j + r0 + i4;  // row of the stage's box (two heads' rows for HPU = 2)
+      float v[8];
+      if constexpr (DT == RSSM_F32) {
+        const float4 x0 = *reinterpret_cast<const float4*>(sb + swizzled_offset<4>(row, c0));
+        const float4 x1 = *reinterpret_cast<const float4*>(sb + swizzled_offset<4>(row, c0 + 4));
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+      } else if constexpr (DT == RSSM_BF16) {
+        const uint4 q = *reinterpret_cast<const uint4*>(sb + swizzled_offset<2>(row, c0));
+        v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+        v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
+      } else if constexpr (DT == RSSM_F16) {
+        const uint4 q = *reinterpret_cast<const uint4*>(sb + swizzled_offset<2>(row, c0));
+        const float2 t0 = h2f2(q.x), t1 = h2f2(q.y), t2 = h2f2(q.z), t3 = h2f2(q.w);
+        v[0] = t0.x; v[1] = t0.y; v[2] = t1.x; v[3] = t1.y; v[4] = t2.x; v[5] = t2.y; v[6] = t3.x; v[7] = t3.y;
+      } else {
+        const uint2 q = *reinterpret_cast<const uint2*>(sb + swizzled_offset<1>(row, c0));
+        const float sc = reinterpret_cast<const float*>(sb + lay.scale_off)[row];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t w = e < 4 ? q.x : q.y;
+          float code;
+          if constexpr (DT == RSSM_I8) {
+            // code q as fp32 without a conversion instruction:
+            // (2^23 + (q + 128)) - (2^23 + 128), every step exact
+            const uint32_t bits = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | (e & 3));
+            code = __fsub_rn(__uint_as_float(bits), 8388736.0f);
+          } else {
+            code = e4m3_to_f32(static_cast<uint8_t>((w >> (8 * (e & 3))) & 0xffu));
+          }
+          v[e] = __fmul_rn(code, sc);
+        }
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) acc[i4][q] = make_float2(__fmul_rn(decay, v[2 * q]), __fmul_rn(decay, v[2 * q + 1]));
+    }
+#pragma unroll 4
+    for (int jt = 0; jt < p; ++jt) {
+      const float w = fw[jt];
+      const uint2 xw = *reinterpret_cast<const uint2*>(xs + jt * kDim + r0);
+      const float u0v = __fmul_rn(w, bf16lo(xw.x)), u1v = __fmul_rn(w, bf16hi(xw.x));
+      const float u2v = __fmul_rn(w, bf16lo(xw.y)), u3v = __fmul_rn(w, bf16hi(xw.y));
+      const uint4 bw = *reinterpret_cast<const uint4*>(bs + jt * kDstate + c0);
+      const float2 bb[4] = {make_float2(bf16lo(bw.x), bf16hi(bw.x)), make_float2(bf16lo(bw.y), bf16hi(bw.y)),
+                            make_float2(bf16lo(bw.z), bf16hi(bw.z)), make_float2(bf16lo(bw.w), bf16hi(bw.w))};
+      const float2 uu[4] = {make_float2(u0v, u0v), make_float2(u1v, u1v), make_float2(u2v, u2v), make_float2(u3v, u3v)};
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4)
+#pragma unroll
+        for (int q = 0; q < 4; ++q) acc[i4][q] = __ffma2_rn(uu[i4], bb[q], acc[i4][q]);
+    }
+    float accf[4][8];
+#pragma unroll
+    for (int i4 = 0; i4 < 4; ++i4)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        accf[i4][2 * q] = acc[i4][q].x;
+        accf[i4][2 * q + 1] = acc[i4][q].y;
+      }
+    const int h = m.h + j;
+    void* head_state = static_cast<uint8_t*>(c.state) +
+                       (static_cast<long long>(m.s) * c.state_stride + static_cast<long long>(h) * kHeadElems) * esz;
+    float* head_scale = k8bit ? c.scale + static_cast<long long>(m.s) * c.scale_stride + h * kDim : nullptr;
+    quantize_store<DT>(accf, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(h),
+                       static_cast<uint32_t>(m.s), m.epoch, a.seed);
   }
 }
 
@@ -263,16 +395,26 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 // readout
 // ---------------------------------------------------------------------------
 // HPU: heads per unit (2 for 8-bit states when a group has an even number of
-// heads: the unit's copies then carry twice the bytes for the same work)
-template <int DT, int TP, int HPU, bool GATE>
-__global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
+// heads: the unit's copies then carry twice the bytes for the same work).
+// FOLD (the one-call path, rssm_flush_step): units of rows the precompute
+// flagged for a flush also fold their live prefix into a new checkpoint, from
+// the same stage the outputs are read from (the outputs replay the whole live
+// prefix from the old checkpoint, as an unflushed row's do), and the unit of
+// head 0 of such a row writes the flush's bookkeeping.
+template <int DT, int TP, int HPU, bool GATE, bool FOLD>
+__global__ void __maxnreg__(FOLD ? 112 : 96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Cache& c = a.c;
-  const ReadLayout lay = read_layout(DT, TP, ns, HPU);
+  const int fold_kb = FOLD ? ring_pad(c.L) : 0;
+  const ReadLayout lay = read_layout(DT, TP, ns, HPU, fold_kb);
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
-  constexpr int kBox = 8192 * HPU;  // bytes of one column box of S0 (64*HPU rows x 128 bytes)
+  constexpr bool kFp4 = DT == RSSM_NVFP4;  // an NVFP4 read checkpoint (two state rows per 128-byte box row)
+  constexpr int kBox = 8192 * HPU;         // bytes of one column box of S0 (64*HPU rows x 128 bytes)
+  constexpr int kNBox = kFp4 ? 1 : esz;    // column boxes per unit
+  constexpr int kHeadOff = kFp4 ? 4096 : 8192;  // bytes between the heads of a unit inside a box
+  constexpr int kRowsPerHead = kFp4 ? 32 : kDim;  // box rows per head
   const int H = c.H, HU = H / HPU;
 
   // Units are taken in chunks of consecutive (row, head) pairs: each CTA's
@@ -323,7 +465,8 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         uint8_t* sb = smem + lay.stages_off + i * lay.stage_bytes;
         mbar_expect_tx(&full[i], lay.s0_bytes);
 #pragma unroll
-        for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * kBox, &s0map, bx * (128 / esz), phh * kDim, s, &full[i]);
+        for (int bx = 0; bx < kNBox; ++bx)
+          tma_load_3d(sb + bx * kBox, &s0map, bx * (128 / esz), phh * kRowsPerHead, s, &full[i]);
         pre |= 1u << i;
       }
     }
@@ -338,7 +481,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     // advance by increments (no division on the per-unit path)
     int st = 0, g = h / c.hpg, hh = h % c.hpg;
     uint32_t ph = 0;
-    const int rstride = TP * kRStride + TP;
+    const int rstride = kRDec + TP * kDim;  // floats per ring-term block
     for (int i = 0;; ++i) {
       if (u >= cend) {  // next chunk
         const unsigned ch = gridDim.x + next;
@@ -363,28 +506,68 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         cur_b = b;
       }
       const bool active = (rr.flags & 1) && rr.Tb > 0;
+      const bool fold = FOLD && (rr.flags & 2);
       const int bg = b * c.G + g;
       // the C block is copied only when the (row, group) changes: consumers
       // keep its fragments in registers (flags bit 1 tells them to reload)
       const bool newc = active && bg != cur_bg;
       if (active) cur_bg = bg;
-      meta[st] = ReadMeta{b, h, rr.s, rr.r, rr.p, rr.Tb, rr.tok0, (active ? 1 : 0) | (newc ? 2 : 0)};
-      if (active) {
+      meta[st] = ReadMeta{b, h, rr.s, rr.r, rr.p, rr.Tb, rr.tok0,
+                          (active ? 1 : 0) | (newc ? 2 : 0) | (fold ? 16 : 0), rr.epoch_new,
+                          rr.gs, {0, 0}};
+      if (active || fold) {
         const int s = rr.s;
         uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
         const bool have_s0 = i < npre && ((pre >> i) & 1u);
-        const uint32_t bytes =
-            (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u * HPU : 0u) + (newc ? 8u * kDstate * 2 : 0u) + lay.r_bytes;
+        // ring terms: the decay floats and the row's T_b rows of the last head's
+        // block (the blocks of the unit's heads are consecutive)
+        const uint32_t r_bytes =
+            active ? static_cast<uint32_t>(((HPU - 1) * rstride + kRDec + rr.Tb * kDim) * 4) : 0u;
+        const int pf = fold ? rr.p : 0;  // live rows the fold reads
+        const uint32_t f_bytes = fold ? static_cast<uint32_t>(HPU * pf * kDim * 2 + pf * kDstate * 2 + HPU * kFoldW * 4)
+                                      : 0u;
+        const uint32_t bytes = (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u * HPU : 0u) + (kFp4 ? 512u * HPU : 0u) +
+                               (newc ? 8u * kDstate * 2 : 0u) + r_bytes + f_bytes;
         mbar_arrive_expect_tx(&full[st], bytes);
         if (!have_s0) {
 #pragma unroll
-          for (int bx = 0; bx < esz; ++bx) tma_load_3d(sb + bx * kBox, &s0map, bx * (128 / esz), h * kDim, s, &full[st]);
+          for (int bx = 0; bx < kNBox; ++bx)
+            tma_load_3d(sb + bx * kBox, &s0map, bx * (128 / esz), h * kRowsPerHead, s, &full[st]);
         }
         if (k8bit)
           bulk_g2s(sb + lay.scale_off, c.scale + static_cast<long long>(s) * c.scale_stride + h * kDim, 256 * HPU,
                    &full[st]);
+        if (kFp4)  // the heads' block scales [64 hpu][8]
+          bulk_g2s(sb + lay.scale_off, c.read_sf + static_cast<long long>(s) * c.read_sf_stride + h * kDim * 8,
+                   512 * HPU, &full[st]);
         if (newc) bulk_g2s(sb + lay.c_off, a.cf + static_cast<long long>(bg) * 8 * kDstate, 8 * kDstate * 2, &full[st]);
-        bulk_g2s(sb + lay.r_off, a.rblk + static_cast<long long>(u) * HPU * rstride, lay.r_bytes, &full[st]);
+        if (active) bulk_g2s(sb + lay.r_off, a.rblk + static_cast<long long>(u) * HPU * rstride, r_bytes, &full[st]);
+        if constexpr (FOLD) {
+          if (fold) {
+            // the live prefix (at most two contiguous ring segments) of the
+            // heads' x rows and the group's B rows, and the fold weights
+            const int L = c.L, r0 = rr.r, n1 = min(pf, L - r0);
+            const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * L * kDim;
+            const uint16_t* bgp = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
+#pragma unroll
+            for (int j = 0; j < HPU; ++j) {
+              uint8_t* xd = sb + lay.fx_off + j * fold_kb * kDim * 2;
+              const uint16_t* xj = xg + static_cast<long long>(j) * L * kDim;
+              if (n1 > 0) bulk_g2s(xd, xj + r0 * kDim, n1 * kDim * 2, &full[st]);
+              if (pf > n1) bulk_g2s(xd + n1 * kDim * 2, xj, (pf - n1) * kDim * 2, &full[st]);
+            }
+            if (n1 > 0) bulk_g2s(sb + lay.fb_off, bgp + r0 * kDstate, n1 * kDstate * 2, &full[st]);
+            if (pf > n1) bulk_g2s(sb + lay.fb_off + n1 * kDstate * 2, bgp, (pf - n1) * kDstate * 2, &full[st]);
+            bulk_g2s(sb + lay.fw_off, a.fw + (static_cast<long long>(b) * H + h) * kFoldW, HPU * kFoldW * 4, &full[st]);
+            if (h == 0) {
+              // the flush's bookkeeping (nothing in this kernel reads it; the
+              // outputs use the row records)
+              c.ring_start[s] = r0 + pf >= L ? r0 + pf - L : r0 + pf;
+              a.pnat_rw[b] = 0;
+              c.epoch[s] = rr.epoch_new;
+            }
+          }
+        }
       } else {
         mbar_arrive(&full[st]);
       }
@@ -438,7 +621,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     const ReadMeta m = meta[st];
     if (m.flags & 8) return;  // no more work
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
-    if (!(m.flags & 1)) {
+    if (!(m.flags & (1 | 16))) {
       // inactive or rejected row: zero outputs, no cache update
       for (int idx = lane; idx < m.Tb * 4 * HPU; idx += 32) {
         const int t = idx / (4 * HPU), j = (idx >> 2) % HPU, q = idx & 3;
@@ -448,6 +631,14 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[st]);
       continue;
+    }
+    if constexpr (FOLD) {
+      if (!(m.flags & 1)) {  // a fold of a row without tokens: no outputs
+        fold_stage<DT, HPU>(sb, lay, fold_kb, m, warp, lane, a);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+        continue;
+      }
     }
     if (m.flags & 2) load_c_frags(reinterpret_cast<const uint16_t*>(sb + lay.c_off), g, cq, af);
     // output gate (GATE): this lane's z pair per head, requested before the contraction
@@ -466,11 +657,14 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
 #pragma unroll
     for (int j = 0; j < HPU; ++j) {  // head m.h + j: rows 64 j .. of the stage's boxes
       float acc[4];
-      s0_dot_c<DT, kBox>(sb + j * 8192, af, d, cq, acc);
-      const float* rb = reinterpret_cast<const float*>(sb + lay.r_off) + j * (TP * kRStride + TP);
-      const float2 rv = g < TP ? *reinterpret_cast<const float2*>(rb + g * kRStride + dout) : make_float2(0.0f, 0.0f);
-      const float dec = g < TP ? rb[TP * kRStride + g] : 0.0f;
+      uint64_t sfrow = 0;
+      if constexpr (kFp4) sfrow = *reinterpret_cast<const uint64_t*>(sb + lay.scale_off + (64 * j + d) * 8);
+      s0_dot_c<DT, kBox>(sb + j * kHeadOff, af, d, cq, acc, sfrow);
+      const float* rb = reinterpret_cast<const float*>(sb + lay.r_off) + j * (kRDec + TP * kDim);
+      const float2 rv = g < m.Tb ? *reinterpret_cast<const float2*>(rb + rblk_offset(g, dout)) : make_float2(0.0f, 0.0f);
+      const float dec = g < m.Tb ? rb[g] : 0.0f;
       float sc0 = 1.0f, sc1 = 1.0f;
+      if constexpr (kFp4) sc0 = sc1 = m.gs;
       if constexpr (k8bit) {
         const float2 scv = *reinterpret_cast<const float2*>(sb + lay.scale_off + j * 256 + dout * 4);
         sc0 = scv.x;
@@ -483,6 +677,9 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
         y[j][0] *= z0 / (1.0f + __expf(-z0));
         y[j][1] *= z1 / (1.0f + __expf(-z1));
       }
+    }
+    if constexpr (FOLD) {
+      if (m.flags & 16) fold_stage<DT, HPU>(sb, lay, fold_kb, m, warp, lane, a);
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
@@ -514,21 +711,22 @@ int launch_precompute(const StepArgs& a, void* stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int DT, int TP, int HPU, bool GATE>
+template <int DT, int TP, int HPU, bool GATE, bool FOLD>
 static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   // as many stages as fit two CTAs per SM (>= 3), else one CTA with up to 8
+  const int fold_kb = FOLD ? ring_pad(a.c.L) : 0;
   int ns = 8, ctas = 2;
   for (; ns >= 3; --ns)
-    if (read_layout(DT, TP, ns, HPU).total <= 113 * 1024) break;
+    if (read_layout(DT, TP, ns, HPU, fold_kb).total <= 113 * 1024) break;
   if (ns < 3) {
     ctas = 1;
     for (ns = 8; ns > 2; --ns)
-      if (read_layout(DT, TP, ns, HPU).total <= 225 * 1024) break;
+      if (read_layout(DT, TP, ns, HPU, fold_kb).total <= 225 * 1024) break;
   }
-  const ReadLayout lay = read_layout(DT, TP, ns, HPU);
+  const ReadLayout lay = read_layout(DT, TP, ns, HPU, fold_kb);
   CUtensorMap map;
   if (!encode_state_map(a.c, &map, HPU)) return cudaErrorInvalidValue;
-  auto kern = readout_kernel<DT, TP, HPU, GATE>;
+  auto kern = readout_kernel<DT, TP, HPU, GATE, FOLD>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, lay.total);
   if (e != cudaSuccess) return e;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
@@ -545,29 +743,44 @@ static int launch_readout_t(const StepArgs& a, int num_sms, cudaStream_t st) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, bool FOLD>
 static int launch_readout_dt(const StepArgs& a, int num_sms, cudaStream_t st) {
-  constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
+  constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3 || DT == RSSM_NVFP4;
   const bool pair = k8bit && a.c.hpg % 2 == 0;
-  if (a.z) {
-    if (a.TP == 4)
-      return pair ? launch_readout_t<DT, 4, 2, true>(a, num_sms, st) : launch_readout_t<DT, 4, 1, true>(a, num_sms, st);
-    return pair ? launch_readout_t<DT, 8, 2, true>(a, num_sms, st) : launch_readout_t<DT, 8, 1, true>(a, num_sms, st);
+  if constexpr (!FOLD) {
+    if (a.z) {
+      if (a.TP == 4)
+        return pair ? launch_readout_t<DT, 4, 2, true, false>(a, num_sms, st)
+                    : launch_readout_t<DT, 4, 1, true, false>(a, num_sms, st);
+      return pair ? launch_readout_t<DT, 8, 2, true, false>(a, num_sms, st)
+                  : launch_readout_t<DT, 8, 1, true, false>(a, num_sms, st);
+    }
   }
   if (a.TP == 4)
-    return pair ? launch_readout_t<DT, 4, 2, false>(a, num_sms, st) : launch_readout_t<DT, 4, 1, false>(a, num_sms, st);
-  return pair ? launch_readout_t<DT, 8, 2, false>(a, num_sms, st) : launch_readout_t<DT, 8, 1, false>(a, num_sms, st);
+    return pair ? launch_readout_t<DT, 4, 2, false, FOLD>(a, num_sms, st)
+                : launch_readout_t<DT, 4, 1, false, FOLD>(a, num_sms, st);
+  return pair ? launch_readout_t<DT, 8, 2, false, FOLD>(a, num_sms, st)
+              : launch_readout_t<DT, 8, 1, false, FOLD>(a, num_sms, st);
 }
 
-int launch_readout(const StepArgs& a, int num_sms, void* stream) {
+template <bool FOLD>
+static int launch_readout_any(const StepArgs& a, int num_sms, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   switch (a.c.dtype) {
-    case RSSM_F32: return launch_readout_dt<RSSM_F32>(a, num_sms, st);
-    case RSSM_BF16: return launch_readout_dt<RSSM_BF16>(a, num_sms, st);
-    case RSSM_F16: return launch_readout_dt<RSSM_F16>(a, num_sms, st);
-    case RSSM_I8: return launch_readout_dt<RSSM_I8>(a, num_sms, st);
-    default: return launch_readout_dt<RSSM_E4M3>(a, num_sms, st);
+    case RSSM_F32: return launch_readout_dt<RSSM_F32, FOLD>(a, num_sms, st);
+    case RSSM_BF16: return launch_readout_dt<RSSM_BF16, FOLD>(a, num_sms, st);
+    case RSSM_F16: return launch_readout_dt<RSSM_F16, FOLD>(a, num_sms, st);
+    case RSSM_I8: return launch_readout_dt<RSSM_I8, FOLD>(a, num_sms, st);
+    case RSSM_NVFP4:  // a read-checkpoint format: the one-call path keeps one checkpoint
+      if constexpr (FOLD) return cudaErrorInvalidValue;
+      else return launch_readout_dt<RSSM_NVFP4, false>(a, num_sms, st);
+    default: return launch_readout_dt<RSSM_E4M3, FOLD>(a, num_sms, st);
   }
+}
+
+int launch_readout(const StepArgs& a, int num_sms, void* stream) { return launch_readout_any<false>(a, num_sms, stream); }
+int launch_readout_fold(const StepArgs& a, int num_sms, void* stream) {
+  return launch_readout_any<true>(a, num_sms, stream);
 }
 
 }  // namespace rssm

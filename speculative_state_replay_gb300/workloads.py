@@ -19,10 +19,10 @@ import math
 
 import numpy as np
 
-F32, BF16, F16, I8, E4M3 = 0, 1, 2, 3, 4
+F32, BF16, F16, I8, E4M3, NVFP4 = 0, 1, 2, 3, 4, 5
 NEAREST, STOCHASTIC = 0, 1
-DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I8: "int8", E4M3: "e4m3"}
-DTYPE_BYTES = {F32: 4, BF16: 2, F16: 2, I8: 1, E4M3: 1}
+DTYPE_NAMES = {F32: "f32", BF16: "bf16", F16: "f16", I8: "int8", E4M3: "e4m3", NVFP4: "nvfp4"}
+DTYPE_BYTES = {F32: 4, BF16: 2, F16: 2, I8: 1, E4M3: 1, NVFP4: 0.5}
 P_DIM, N_DIM = 64, 128
 BASE_SEED = 20261202
 
@@ -74,9 +74,10 @@ class Workload:
 
 def config(name: str, **overrides) -> Workload:
     """The five decode configurations (sizes of the benchmark definitions),
-    and "separate": the sweep's largest batch with the separate checkpoints of
-    vLLM PR #65660 (Overview: an FP16 recurrence checkpoint with stochastic
-    rounding, an FP8 read checkpoint the readout streams)."""
+    and "separate" / "separate_nvfp4": the sweep's largest batch with the
+    separate checkpoints of vLLM PR #65660 (Overview: an FP16 recurrence
+    checkpoint with stochastic rounding, an FP8 or NVFP4 read checkpoint the
+    readout streams)."""
     base = {
         "tiny": dict(num_slots=5, nheads=8, ngroups=1, max_window=16, npredicted=4, state_dtype=F32, batch=4,
                      T=4, steps=12, pad_row=True, config_id=1),
@@ -93,9 +94,13 @@ def config(name: str, **overrides) -> Workload:
                          state_dtype=F16, rounding=STOCHASTIC, sr_seed=7, read_dtype=E4M3, batch=1024, T=5,
                          steps=32, varlen=True, ring_start_random=True, prefill_live=16, slot_pad_bytes=4096,
                          config_id=6),
+        "separate_nvfp4": dict(num_slots=2 * 1024 + 1, nheads=128, ngroups=8, max_window=16, npredicted=5,
+                               state_dtype=F16, rounding=STOCHASTIC, sr_seed=7, read_dtype=NVFP4, batch=1024, T=5,
+                               steps=32, varlen=True, ring_start_random=True, prefill_live=16, slot_pad_bytes=4096,
+                               config_id=7),
     }[name]
     base.update(overrides)
-    if name in ("sweep", "separate") and "batch" in overrides and "num_slots" not in overrides:
+    if name in ("sweep", "separate", "separate_nvfp4") and "batch" in overrides and "num_slots" not in overrides:
         base["num_slots"] = 2 * overrides["batch"] + 1
     return Workload(name=name, **base)
 

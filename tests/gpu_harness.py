@@ -54,7 +54,10 @@ def gpu_cache_from(oc, device="cuda"):
 
 
 def cache_arrays(oc):
-    return CACHE_ARRAYS + (("read_state", "read_scale") if getattr(oc, "read_dtype", None) is not None else ())
+    rd = getattr(oc, "read_dtype", None)
+    if rd is None:
+        return CACHE_ARRAYS
+    return CACHE_ARRAYS + (("read_state", "read_sf", "read_gs") if rd == W.NVFP4 else ("read_state", "read_scale"))
 
 
 def sync_gpu_from(gc, oc):
@@ -205,8 +208,9 @@ class Pair:
         if oc.state_dtype in (W.I8, W.E4M3):
             assert np.array_equal(host_of(gc.scale, oc.scale), oc.scale), "scales"
         if getattr(oc, "read_dtype", None) is not None:  # the read checkpoint: nearest codes, bit for bit
-            assert np.array_equal(host_of(gc.read_state, oc.read_state), oc.read_state), "read checkpoint"
-            assert np.array_equal(host_of(gc.read_scale, oc.read_scale), oc.read_scale), "read scales"
+            for name in cache_arrays(oc)[len(CACHE_ARRAYS):]:
+                o = getattr(oc, name)
+                assert np.array_equal(host_of(getattr(gc, name), o), o), name
         if np.array_equal(gs, oc.state):
             self.exact_state_steps += 1
         if self.resync:  # continue from identical state

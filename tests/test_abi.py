@@ -147,3 +147,28 @@ def test_wait_selftest_rejects_bad_arguments(lib):
     assert lib.rssm_selftest_wait_timeout(p, 0, None) == 1
     assert lib.rssm_selftest_wait_timeout(p, 20000, None) == 1
     assert lib.rssm_selftest_wait_timeout(ctypes.c_void_p((1 << 20) + 2), 50, None) == 1
+
+
+def test_read_checkpoint_fields_are_validated(lib):
+    """A read checkpoint's format, pointers and strides are checked before any
+    launch; NVFP4 is a read format only."""
+    base = 1 << 20
+    ok8 = _cache(read_state=base, read_slot_stride=8 * 64 * 128, read_scale=base, read_scale_slot_stride=8 * 64,
+                 read_dtype=4)
+    assert lib.rssm_scratch_bytes(ctypes.byref(ok8), 4, 4) > 0
+    ok4 = _cache(read_state=base, read_slot_stride=8 * 64 * 64, read_sf=base, read_sf_slot_stride=8 * 64 * 8,
+                 read_gs=base, read_dtype=5)
+    assert lib.rssm_scratch_bytes(ctypes.byref(ok4), 4, 4) > 0
+    bad = [
+        _cache(read_state=base, read_slot_stride=8 * 64 * 128, read_scale=base, read_scale_slot_stride=8 * 64,
+               read_dtype=2),                                     # not a read format
+        _cache(read_state=base, read_slot_stride=8 * 64 * 128, read_dtype=3),  # 8-bit without scales
+        _cache(read_state=base, read_slot_stride=8 * 64 * 64, read_gs=base, read_dtype=5),  # NVFP4 without block scales
+        _cache(read_state=base, read_slot_stride=8 * 64 * 64, read_sf=base, read_sf_slot_stride=8 * 64 * 8,
+               read_dtype=5),                                     # NVFP4 without global scales
+        _cache(read_state=base, read_slot_stride=8 * 64 * 32, read_sf=base, read_sf_slot_stride=8 * 64 * 8,
+               read_gs=base, read_dtype=5),                       # codes stride too small
+        _cache(state_dtype=5),                                    # NVFP4 recurrence state
+    ]
+    for c in bad:
+        assert lib.rssm_scratch_bytes(ctypes.byref(c), 4, 4) == 0

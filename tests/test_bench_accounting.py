@@ -61,3 +61,12 @@ def test_bytes_with_a_separate_read_checkpoint(bench):
     row = (1, 0, 0, 5, 0, 1)
     assert bench.algorithmic_bytes(wl, [row], None, 1) == 128 * (8192 + 256 + 5 * 256 / 16 + 5 * 128)
     assert bench.flush_bytes(wl, [16], 2) == 128 * (2 * 16384 + 16 * 132 + 16 * 256 / 16 + 8192 + 256)
+
+
+def test_bytes_with_an_nvfp4_read_checkpoint(bench):
+    """NVFP4 read copy: 4096 bytes of codes + 512 of block scales per (row,
+    head) for the readout; a fold also writes them."""
+    wl = W.config("separate_nvfp4")
+    row = (1, 0, 0, 5, 0, 1)
+    assert bench.algorithmic_bytes(wl, [row], None, 0.5) == 128 * (4096 + 512 + 5 * 256 / 16 + 5 * 128)
+    assert bench.flush_bytes(wl, [16], 2) == 128 * (2 * 16384 + 16 * 132 + 16 * 256 / 16 + 4096 + 512)

@@ -1,11 +1,15 @@
 """rssm_flush_step (flush and step in one call) vs the oracle's flush then
 step, on the same seeded inputs (needs a GPU).
 
-Same bar as the two-call path: bf16 outputs within atol 2e-2 / rtol 1e-2;
-f32 checkpoints within 1e-4 relative, 2-byte ones within the bf16 tolerance;
-8-bit codes and scales, rings, ring_start, pnat, flush epochs and error bits
-bit-exact.  The flushed checkpoints come out of the fused kernel's own copy of
-the fold and must match the oracle exactly wherever the two-call path does.
+The one call folds every flushed checkpoint in the flush's canonical fp32
+order (for every format), from the stage its readout streams: checkpoints,
+8-bit scales, rings, ring_start, pnat, flush epochs and error bits bit for bit
+against the oracle.  A flushed row's outputs replay its whole live prefix
+from the old checkpoint (the fold's fp32 values before their rounding), where
+the oracle reads the rounded new checkpoint: bf16 outputs within atol 2e-2 /
+rtol 1e-2.  Rows whose live prefix and new tokens do not fit the ring
+together (pnat + T_b > L, which the decode protocol never produces when
+max_window >= npredicted) are refused with RSSM_ERRBIT_PNAT.
 """
 import numpy as np
 import pytest
@@ -48,6 +52,7 @@ def test_fused_tiny_all_dtypes(orc, dtype):
     wl = W.config("tiny", state_dtype=dtype, prefill_live=14, ring_start_random=True)
     pair = run_fused(orc, wl)
     assert pair.oc.flush_epoch.max() >= 1
+    assert pair.exact_state_steps == wl.steps
 
 
 def test_fused_tiny_config_f32_full(orc):
@@ -71,11 +76,13 @@ def test_fused_mamba2_decode_reduced(orc):
     wl = W.config("mamba2_decode", batch=12, steps=20)
     pair = run_fused(orc, wl)
     assert pair.oc.flush_epoch.max() >= 1
+    assert pair.exact_state_steps == wl.steps
 
 
 def test_fused_large_batch_reduced(orc):
     wl = W.config("large_batch", batch=24, steps=16)
-    run_fused(orc, wl)
+    pair = run_fused(orc, wl)
+    assert pair.exact_state_steps == wl.steps
 
 
 def test_fused_sweep_reduced_varlen_padded(orc):
@@ -88,37 +95,62 @@ def test_fused_sweep_reduced_varlen_padded(orc):
 def test_fused_forced_full_window_flush(orc, dtype):
     """Every active row flushes a full window (p = 16 = W) every step."""
     wl = W.config("mamba2_decode", batch=6, state_dtype=dtype, prefill_live=16, ring_start_random=True, steps=3)
-    run_fused(orc, wl, force_every=1, pnat_override=16)
+    pair = run_fused(orc, wl, force_every=1, pnat_override=16)
+    assert pair.exact_state_steps == wl.steps
 
 
-@pytest.mark.parametrize("T,W_,G", [(1, 16, 8), (8, 24, 8), (3, 0, 128), (8, 0, 1)])
+@pytest.mark.parametrize("T,W_,G", [(1, 16, 8), (8, 24, 8), (3, 3, 128), (8, 8, 1)])
 def test_fused_shape_edges(orc, T, W_, G):
+    """T = 1; the largest ring (L = 32) with T = 8; one head per group with
+    max_window = T (a row flushes about every other step); one group for all
+    heads."""
     H = 128 if G == 128 else 16
     wl = W.Workload(name="edge", num_slots=9, nheads=H, ngroups=G, max_window=W_, npredicted=T,
                     state_dtype=W.BF16, batch=6, T=T, steps=6, pad_row=True, ring_start_random=True,
                     config_id=9)
-    run_fused(orc, wl)
+    pair = run_fused(orc, wl)
+    assert pair.exact_state_steps == wl.steps
 
 
 @pytest.mark.parametrize("dtype", [W.BF16, W.I8])
-def test_fused_appends_overlapping_the_folded_prefix(orc, dtype):
-    """Flushed rows whose new tokens land on live slots the fold reads (p + T_b
-    > L): the fused call appends them only after the fold has its copy, so the
-    result is still exactly the two-call one.  One row starts with a nearly
-    full ring (p = L - 1); with max_window < T every flush does it."""
-    wl = W.config("tiny", state_dtype=dtype, prefill_live=14, ring_start_random=True)
+def test_fused_refuses_rows_that_overflow_the_ring(orc, dtype):
+    """A row whose live prefix and new tokens do not fit the ring together
+    (pnat + T_b > L: the new tokens would land on live slots the fold reads) is
+    refused: RSSM_ERRBIT_PNAT, zero outputs, its caches untouched; the other
+    rows are computed as usual.  (rssm_flush + rssm_step folds such a row
+    first; the decode protocol never produces one when max_window >=
+    npredicted.)"""
+    wl = W.config("tiny", state_dtype=dtype, prefill_live=14, ring_start_random=True, steps=1)
     gen = W.Generator(wl)
     oc, ids, pnat = oracle_cache(orc, wl, gen)
     rows = np.nonzero(ids > 0)[0]
-    pnat[rows[0]] = wl.L - 1
-    pair = Pair(orc, wl, oc, ids, pnat, fused=True)
-    for k in range(4):
-        pair.step(gen.step(k))
-    assert int(pair.oc.error_word[0]) == 0
-    wl2 = W.Workload(name="edge", num_slots=9, nheads=16, ngroups=4, max_window=1, npredicted=6,
-                     state_dtype=dtype, batch=6, T=6, steps=8, pad_row=True, ring_start_random=True, config_id=9)
-    pair2 = run_fused(orc, wl2)
-    assert pair2.oc.flush_epoch.max() >= 4
+    bad = rows[0]
+    pnat[bad] = wl.L - 1
+    gc = gpu_cache_from(oc)
+    A, D, dtb = gen.params()
+    g = lambda a: dev_of(a, "cuda")  # noqa: E731
+    gp = g(pnat)
+    inp = gen.step(0)
+    out = torch.full((inp.ntok, wl.nheads, 64), 0x3F80, dtype=torch.int16, device="cuda")
+    before = {n: getattr(gc, n).clone() for n in ("state", "x_cache", "ring_start", "flush_epoch")}
+    sc = api.alloc_scratch(gc, ids.size, wl.T)
+    api.rssm_flush_step(gc, g(inp.x), g(inp.dt), g(A), g(inp.B), g(inp.C), g(D), g(dtb), g(ids), gp, wl.T, out, sc)
+    torch.cuda.synchronize()
+    assert int(gc.error_word.item()) & api.ERRBIT_PNAT
+    assert not out[bad * wl.T:(bad + 1) * wl.T].any()
+    s = int(ids[bad])
+    for n, v in before.items():
+        assert torch.equal(getattr(gc, n)[s], v[s]), n
+    assert int(gp[bad].item()) == wl.L - 1
+    # the other rows match the oracle (the bad row left out on both sides)
+    good = np.array([b for b in range(ids.size) if b != bad])
+    ps = pnat[good].copy()
+    tok = (good[:, None] * wl.T + np.arange(wl.T)[None]).reshape(-1)
+    oc.flush(A, ids[good], ps, wl.T)
+    yo = oc.step(inp.x[tok], inp.dt[tok], A, inp.B[tok], inp.C[tok], D, dtb, ids[good], ps, wl.T)
+    yg = out.cpu().numpy().view(np.uint16)[tok]
+    assert np.allclose(bf16_f32(yg), bf16_f32(yo), atol=2e-2, rtol=1e-2)
+    assert np.array_equal(gp.cpu().numpy()[good], ps)
 
 
 def test_fused_batch_beyond_one_cta(orc):
@@ -134,7 +166,8 @@ def test_fused_batch_beyond_one_cta(orc):
 def test_fused_matches_two_calls_bit_for_bit():
     """rssm_flush_step and rssm_flush + rssm_step on twin GPU caches: the same
     checkpoint bits, rings and bookkeeping, step after step (outputs within
-    float reassociation of the two readouts)."""
+    the bf16 tolerance: a flushed row's outputs come from the fold's values
+    before their rounding)."""
     wl = W.config("eight_bit", batch=16, state_dtype=W.E4M3, rounding=W.STOCHASTIC, sr_seed=11, steps=8)
     gen = W.Generator(wl)
     A, D, dtb = gen.params()

@@ -22,7 +22,8 @@ from tests.harness import oracle_cache
 pytestmark = pytest.mark.gpu
 
 PAIRS = [(W.F16, W.STOCHASTIC, W.E4M3), (W.F16, W.STOCHASTIC, W.I8), (W.BF16, W.NEAREST, W.E4M3),
-         (W.F32, W.NEAREST, W.I8), (W.BF16, W.STOCHASTIC, W.E4M3)]
+         (W.F32, W.NEAREST, W.I8), (W.BF16, W.STOCHASTIC, W.E4M3), (W.F16, W.STOCHASTIC, W.NVFP4),
+         (W.F32, W.NEAREST, W.NVFP4), (W.BF16, W.NEAREST, W.NVFP4)]
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -50,7 +51,11 @@ def test_init_writes_both_checkpoints_bit_exact(orc, dtype, rounding, read):
                        read_dtype=read)
     api.rssm_init_state(gc, dev_of(states, "cuda"), dev_of(ids, "cuda"), seed=wl.sr_seed)
     torch.cuda.synchronize()
-    for name in ("state", "scale", "read_state", "read_scale", "ring_start", "flush_epoch"):
+    from tests.gpu_harness import cache_arrays
+
+    for name in cache_arrays(oc):
+        if name == "error_word":
+            continue
         o = getattr(oc, name)
         assert np.array_equal(host_of(getattr(gc, name), o), o), name
 
@@ -70,7 +75,7 @@ def test_decode_steps_with_a_read_checkpoint(orc, dtype, rounding, read):
     assert pair.exact_state_steps == wl.steps
 
 
-@pytest.mark.parametrize("read", [W.E4M3, W.I8])
+@pytest.mark.parametrize("read", [W.E4M3, W.I8, W.NVFP4])
 def test_separate_sweep_without_resync(orc, read):
     """The separate-checkpoint benchmark workload reduced (varlen rows, padded
     slot pages, fp16 recurrence with stochastic rounding), 16 steps with each
