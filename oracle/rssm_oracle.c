@@ -367,8 +367,9 @@ static int read_dtype_ok(int dt) { return dt == ORC_I8 || dt == ORC_E4M3 || dt =
  * times the E4M3 maximum), 1 for an all-zero state; it is set at init and kept
  * by the slot's later flushes.  Each block of 16 consecutive dstate values
  * takes an E4M3 scale sf = e4m3_nearest(block max / (6 gs)) (saturating at
- * 448), and each value the E2M1 code nearest to v / (gs * sf) (saturating at
- * 6; a block whose scale rounds to 0 is all zeros).  Decoded value:
+ * 448), and each value the E2M1 code nearest to v * (1 / (gs * sf)) (one
+ * rounded reciprocal per block, as the 8-bit row scales; saturating at 6; a
+ * block whose scale rounds to 0 is all zeros).  Decoded value:
  * e2m1(code) * sf * gs.  Nearest rounding throughout ([vS] Claims: read
  * checkpoints use nearest encoding).                                       */
 /* ------------------------------------------------------------------------- */
@@ -381,11 +382,12 @@ static void quantize_row_nvfp4(const float *acc, float gs, uint8_t *codes /* 64 
     uint8_t sc = orc_f32_to_e4m3(bmax / (6.0f * gs));
     sf[blk] = sc;
     float q = orc_e4m3_decode(sc) * gs;
+    float inv = q > 0.0f ? 1.0f / q : 0.0f; /* one reciprocal per block, as the 8-bit row scales */
     for (int i = 0; i < NVFP4_BLOCK; i += 2) {
       uint8_t c0 = 0, c1 = 0;
       if (q > 0.0f) {
-        c0 = orc_f32_to_e2m1(v[i] / q);
-        c1 = orc_f32_to_e2m1(v[i + 1] / q);
+        c0 = orc_f32_to_e2m1(v[i] * inv);
+        c1 = orc_f32_to_e2m1(v[i + 1] * inv);
       }
       codes[(blk * NVFP4_BLOCK + i) / 2] = (uint8_t)(c0 | c1 << 4); /* even element in the low nibble */
     }
