@@ -151,8 +151,8 @@ typedef struct {
    * largest magnitude of its FP32 prefill state / (6 * 448) (1 for a zero
    * state); the slot's flushes keep it.  Block scale = e4m3 nearest of
    * (block max / (6 * global)), saturating; code = e2m1 nearest of
-   * (v / (global * block scale)), saturating at 6 (0 where the block scale is
-   * 0). */
+   * (v * (1 / (global * block scale))) (one rounded reciprocal per block),
+   * saturating at 6 (0 where the block scale is 0). */
   void *read_sf;       int64_t read_sf_slot_stride;
   float *read_gs;
 } rssm_cache;

@@ -496,11 +496,13 @@ __device__ __forceinline__ void quantize_store(float (&acc)[4][8], int r0, int c
 // --------------------------------------------------------------------------
 // E2M1 nearest (ties to the even code), saturating at 6, keeping the sign of
 // v (also for values that round to zero): the grid step is 0.5 below 2, 1 in
-// [2, 4), 2 from 4 on, so |v| / step and the rounding are exact operations.
+// [2, 4), 2 from 4 on, so |v| / step (a multiplication by a power of two) and
+// the rounding are exact operations.
 __device__ __forceinline__ uint32_t e2m1_nearest(float v) {
   const float a = fabsf(v);
+  const float inv_q = a < 2.0f ? 2.0f : (a < 4.0f ? 1.0f : 0.5f);
   const float q = a < 2.0f ? 0.5f : (a < 4.0f ? 1.0f : 2.0f);
-  const float mag = fminf(__fmul_rn(rintf(__fdiv_rn(a, q)), q), 6.0f);  // a grid point
+  const float mag = fminf(__fmul_rn(rintf(__fmul_rn(a, inv_q)), q), 6.0f);  // a grid point
   const uint32_t m = (mag > 0.25f ? 1u : 0u) + (mag > 0.75f ? 1u : 0u) + (mag > 1.25f ? 1u : 0u) +
                      (mag > 1.75f ? 1u : 0u) + (mag > 2.5f ? 1u : 0u) + (mag > 3.5f ? 1u : 0u) +
                      (mag > 5.0f ? 1u : 0u);
@@ -523,7 +525,7 @@ __device__ __forceinline__ void e2m1x4_to_f16x2(uint32_t w, uint32_t& lo, uint32
 // c0..c0+7 of a [64][128] head; lanes 2k and 2k+1 hold the two halves of a
 // 16-value block) into the head's codes [64][64 bytes] and block scales
 // [64][8]: sf = e4m3 nearest of (block max / (6 gs)), code = e2m1 nearest of
-// (v / (gs * sf)) (0 where sf is 0).
+// (v * (1 / (gs * sf))) (0 where sf is 0).
 __device__ __forceinline__ void quantize_store_nvfp4(const float (&acc)[4][8], int r0, int c0, int lane,
                                                      uint8_t* head_codes, uint8_t* head_sf, float gs) {
   const float den = __fmul_rn(6.0f, gs);
@@ -537,8 +539,9 @@ __device__ __forceinline__ void quantize_store_nvfp4(const float (&acc)[4][8], i
     const float qs = __fmul_rn(e4m3_to_f32(sc), gs);
     uint32_t word = 0u;
     if (qs > 0.0f) {
+      const float inv = __frcp_rn(qs);
 #pragma unroll
-      for (int q = 0; q < 8; ++q) word |= e2m1_nearest(__fdiv_rn(acc[i][q], qs)) << (4 * q);
+      for (int q = 0; q < 8; ++q) word |= e2m1_nearest(__fmul_rn(acc[i][q], inv)) << (4 * q);
     }
     *reinterpret_cast<uint32_t*>(head_codes + (r0 + i) * 64 + c0 / 2) = word;
     if (!(lane & 1)) head_sf[(r0 + i) * 8 + c0 / 16] = sc;

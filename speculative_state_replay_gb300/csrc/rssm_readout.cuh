@@ -57,14 +57,13 @@ struct ReadMeta {
 struct ReadLayout {
   int ns;
   uint32_t s0_bytes, scale_off, c_off, r_off, r_bytes, stage_bytes;
-  uint32_t fx_off, fb_off, fw_off;  // fold area (fold_kb > 0): live x rows, live B rows, fold weights
+  uint32_t fw_off;  // fold area (fold_kb > 0): the heads' fold weights
   uint32_t stages_off, total;
 };
 
 // one stage of a unit of `hpu` consecutive heads of one group: S0 as esz
 // boxes of 64*hpu rows x 128 bytes | 8-bit scales | C block | ring-term blocks
-// [| fold area: the heads' live x rows [hpu][fold_kb][64], the group's live B
-// rows [fold_kb][128], the heads' fold weights [hpu][kFoldW]]
+// [| fold area: the heads' fold weights [hpu][kFoldW]]
 __host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int hpu = 1, int fold_kb = 0) {
   ReadLayout f;
   f.ns = ns;
@@ -79,12 +78,8 @@ __host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int
   f.r_off = o;
   f.r_bytes = (kRDec + TP * kDim) * 4 * hpu;  // room for the full ring-term blocks (a unit copies its T_b rows)
   o += f.r_bytes;
-  f.fx_off = f.fb_off = f.fw_off = 0;
+  f.fw_off = 0;
   if (fold_kb > 0) {
-    f.fx_off = o;
-    o += hpu * fold_kb * kDim * 2;
-    f.fb_off = o;
-    o += fold_kb * kDstate * 2;
     f.fw_off = o;
     o += hpu * kFoldW * 4;
   }
@@ -92,6 +87,11 @@ __host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int
   f.stages_off = 1024;                  // barriers and per-stage metadata (8 x 48 bytes at 256)
   f.total = f.stages_off + ns * f.stage_bytes + 1024;  // + slack to align the base
   return f;
+}
+
+// hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `src` into L2
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, int c0, int c1, int c2,

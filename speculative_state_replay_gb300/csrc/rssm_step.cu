@@ -304,8 +304,10 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 // (lane: rows r0..r0+3, columns c0..c0+7)
 //     acc = e^{c_end} S0f;  acc = fma(w_j x_j[d], B_j[n], acc) for j ascending
 // with S0f read from the stage's TMA boxes (the checkpoint the outputs were
-// just read from), the live x and B rows and the weights from the stage's fold
-// area, then the flush's quantiser -- the operations rssm_flush performs.
+// just read from), the weights from the stage's fold area and the live x and B
+// rows straight from the rings (the producer hinted them into L2 when it
+// issued the unit), then the flush's quantiser -- the operations rssm_flush
+// performs.
 template <int DT, int HPU>
 __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& lay, int fold_kb, const ReadMeta& m,
                                            int warp, int lane, const StepArgs& a) {
@@ -313,12 +315,14 @@ __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& 
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
   const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
-  const int p = m.p;
-  const uint16_t* bs = reinterpret_cast<const uint16_t*>(sb + lay.fb_off);
+  const int p = m.p, L = c.L, rs = m.r;
+  const uint16_t* bg = c.B_cache + static_cast<long long>(m.s) * c.B_stride +
+                       static_cast<long long>(m.h / c.hpg) * L * kDstate + c0;
 #pragma unroll 1
   for (int j = 0; j < HPU; ++j) {
     const float* fw = reinterpret_cast<const float*>(sb + lay.fw_off) + j * kFoldW;
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.fx_off) + j * fold_kb * kDim;
+    const uint16_t* xg = c.x_cache + static_cast<long long>(m.s) * c.x_stride +
+                         static_cast<long long>(m.h + j) * L * kDim + r0;
     const float decay = fw[32];
     float2 acc[4][4];
 #pragma unroll
@@ -361,11 +365,12 @@ __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& 
     }
 #pragma unroll 4
     for (int jt = 0; jt < p; ++jt) {
+      const int q = rs + jt >= L ? rs + jt - L : rs + jt;  // ring slot of live token jt
       const float w = fw[jt];
-      const uint2 xw = *reinterpret_cast<const uint2*>(xs + jt * kDim + r0);
+      const uint2 xw = __ldg(reinterpret_cast<const uint2*>(xg + q * kDim));
       const float u0v = __fmul_rn(w, bf16lo(xw.x)), u1v = __fmul_rn(w, bf16hi(xw.x));
       const float u2v = __fmul_rn(w, bf16lo(xw.y)), u3v = __fmul_rn(w, bf16hi(xw.y));
-      const uint4 bw = *reinterpret_cast<const uint4*>(bs + jt * kDstate + c0);
+      const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bg + q * kDstate));
       const float2 bb[4] = {make_float2(bf16lo(bw.x), bf16hi(bw.x)), make_float2(bf16lo(bw.y), bf16hi(bw.y)),
                             make_float2(bf16lo(bw.z), bf16hi(bw.z)), make_float2(bf16lo(bw.w), bf16hi(bw.w))};
       const float2 uu[4] = {make_float2(u0v, u0v), make_float2(u1v, u1v), make_float2(u2v, u2v), make_float2(u3v, u3v)};
@@ -402,7 +407,7 @@ __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& 
 // prefix from the old checkpoint, as an unflushed row's do), and the unit of
 // head 0 of such a row writes the flush's bookkeeping.
 template <int DT, int TP, int HPU, bool GATE, bool FOLD>
-__global__ void __maxnreg__(FOLD ? 112 : 96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
+__global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorMap s0map, StepArgs a, int ns) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const Cache& c = a.c;
@@ -524,8 +529,7 @@ __global__ void __maxnreg__(FOLD ? 112 : 96) readout_kernel(const __grid_constan
         const uint32_t r_bytes =
             active ? static_cast<uint32_t>(((HPU - 1) * rstride + kRDec + rr.Tb * kDim) * 4) : 0u;
         const int pf = fold ? rr.p : 0;  // live rows the fold reads
-        const uint32_t f_bytes = fold ? static_cast<uint32_t>(HPU * pf * kDim * 2 + pf * kDstate * 2 + HPU * kFoldW * 4)
-                                      : 0u;
+        const uint32_t f_bytes = fold ? static_cast<uint32_t>(HPU * kFoldW * 4) : 0u;
         const uint32_t bytes = (have_s0 ? 0u : lay.s0_bytes) + (k8bit ? 256u * HPU : 0u) + (kFp4 ? 512u * HPU : 0u) +
                                (newc ? 8u * kDstate * 2 : 0u) + r_bytes + f_bytes;
         mbar_arrive_expect_tx(&full[st], bytes);
@@ -544,20 +548,20 @@ __global__ void __maxnreg__(FOLD ? 112 : 96) readout_kernel(const __grid_constan
         if (active) bulk_g2s(sb + lay.r_off, a.rblk + static_cast<long long>(u) * HPU * rstride, r_bytes, &full[st]);
         if constexpr (FOLD) {
           if (fold) {
-            // the live prefix (at most two contiguous ring segments) of the
-            // heads' x rows and the group's B rows, and the fold weights
+            // the fold weights into the stage; the live prefix (at most two
+            // contiguous ring segments) of the heads' x rows and the group's B
+            // rows hinted into L2 for the consumers' reads
             const int L = c.L, r0 = rr.r, n1 = min(pf, L - r0);
             const uint16_t* xg = c.x_cache + static_cast<long long>(s) * c.x_stride + static_cast<long long>(h) * L * kDim;
             const uint16_t* bgp = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
 #pragma unroll
             for (int j = 0; j < HPU; ++j) {
-              uint8_t* xd = sb + lay.fx_off + j * fold_kb * kDim * 2;
               const uint16_t* xj = xg + static_cast<long long>(j) * L * kDim;
-              if (n1 > 0) bulk_g2s(xd, xj + r0 * kDim, n1 * kDim * 2, &full[st]);
-              if (pf > n1) bulk_g2s(xd + n1 * kDim * 2, xj, (pf - n1) * kDim * 2, &full[st]);
+              if (n1 > 0) prefetch_l2(xj + r0 * kDim, n1 * kDim * 2);
+              if (pf > n1) prefetch_l2(xj, (pf - n1) * kDim * 2);
             }
-            if (n1 > 0) bulk_g2s(sb + lay.fb_off, bgp + r0 * kDstate, n1 * kDstate * 2, &full[st]);
-            if (pf > n1) bulk_g2s(sb + lay.fb_off + n1 * kDstate * 2, bgp, (pf - n1) * kDstate * 2, &full[st]);
+            if (n1 > 0) prefetch_l2(bgp + r0 * kDstate, n1 * kDstate * 2);
+            if (pf > n1) prefetch_l2(bgp, (pf - n1) * kDstate * 2);
             bulk_g2s(sb + lay.fw_off, a.fw + (static_cast<long long>(b) * H + h) * kFoldW, HPU * kFoldW * 4, &full[st]);
             if (h == 0) {
               // the flush's bookkeeping (nothing in this kernel reads it; the
@@ -756,11 +760,16 @@ static int launch_readout_dt(const StepArgs& a, int num_sms, cudaStream_t st) {
                   : launch_readout_t<DT, 8, 1, true, false>(a, num_sms, st);
     }
   }
-  if (a.TP == 4)
-    return pair ? launch_readout_t<DT, 4, 2, false, FOLD>(a, num_sms, st)
-                : launch_readout_t<DT, 4, 1, false, FOLD>(a, num_sms, st);
-  return pair ? launch_readout_t<DT, 8, 2, false, FOLD>(a, num_sms, st)
-              : launch_readout_t<DT, 8, 1, false, FOLD>(a, num_sms, st);
+  if constexpr (FOLD) {  // one head per unit (a two-head fold does not fit the register budget)
+    return a.TP == 4 ? launch_readout_t<DT, 4, 1, false, true>(a, num_sms, st)
+                     : launch_readout_t<DT, 8, 1, false, true>(a, num_sms, st);
+  } else {
+    if (a.TP == 4)
+      return pair ? launch_readout_t<DT, 4, 2, false, false>(a, num_sms, st)
+                  : launch_readout_t<DT, 4, 1, false, false>(a, num_sms, st);
+    return pair ? launch_readout_t<DT, 8, 2, false, false>(a, num_sms, st)
+                : launch_readout_t<DT, 8, 1, false, false>(a, num_sms, st);
+  }
 }
 
 template <bool FOLD>
