@@ -47,6 +47,12 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a2,
 // conflict-free.
 constexpr int kReadChunk = 4;  // (row, head) units per work grab of the readout
 
+// the one-call path's fold rows: two buffers of 8 live tokens, x [8][64] bf16
+// then B [8][128] bf16 each
+constexpr uint32_t kFoldChunk = 8;
+constexpr uint32_t kFoldBufX = kFoldChunk * kDim * 2, kFoldBufOne = kFoldBufX + kFoldChunk * kDstate * 2;
+constexpr uint32_t kFoldBuf = 2 * kFoldBufOne;
+
 struct ReadMeta {
   int b, h, s, r, p, Tb, tok0, flags;  // flags: 1 outputs, 2 new C block, 8 no more work, 16 fold
   unsigned epoch;                      // epoch of the checkpoint a fold writes
@@ -58,6 +64,7 @@ struct ReadLayout {
   int ns;
   uint32_t s0_bytes, scale_off, c_off, r_off, r_bytes, stage_bytes;
   uint32_t fw_off;  // fold area (fold_kb > 0): the heads' fold weights
+  uint32_t fbuf_off;  // fold_kb > 0: the CTA's fold-row buffer (two chunks of 8 live tokens' x and B rows)
   uint32_t stages_off, total;
 };
 
@@ -85,7 +92,8 @@ __host__ __device__ inline ReadLayout read_layout(int dtype, int TP, int ns, int
   }
   f.stage_bytes = (o + 1023) & ~1023u;  // the swizzled boxes need 1024-byte alignment
   f.stages_off = 1024;                  // barriers and per-stage metadata (8 x 48 bytes at 256)
-  f.total = f.stages_off + ns * f.stage_bytes + 1024;  // + slack to align the base
+  f.fbuf_off = f.stages_off + ns * f.stage_bytes;
+  f.total = f.fbuf_off + (fold_kb > 0 ? kFoldBuf : 0u) + 1024;  // + slack to align the base
   return f;
 }
 

@@ -305,24 +305,53 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
 //     acc = e^{c_end} S0f;  acc = fma(w_j x_j[d], B_j[n], acc) for j ascending
 // with S0f read from the stage's TMA boxes (the checkpoint the outputs were
 // just read from), the weights from the stage's fold area and the live x and B
-// rows straight from the rings (the producer hinted them into L2 when it
-// issued the unit), then the flush's quantiser -- the operations rssm_flush
-// performs.
+// rows brought by the consumer threads into the CTA's fold buffer, 8 tokens at
+// a time, double buffered (the producer hinted the rows into L2 when it issued
+// the unit), then the flush's quantiser -- the operations rssm_flush performs.
+// Every consumer warp calls it for the unit; the warps meet at the mbarrier
+// fsync (8 arrivals a phase, bounded waits: returns false if a wait ran out,
+// with RSSM_ERRBIT_TIMEOUT set; the caller then stops).
 template <int DT, int HPU>
-__device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& lay, int fold_kb, const ReadMeta& m,
-                                           int warp, int lane, const StepArgs& a) {
+__device__ __forceinline__ bool fold_stage(const uint8_t* sb, uint8_t* fbuf, uint64_t* fsync, uint32_t& fph,
+                                           const ReadLayout& lay, int fold_kb, const ReadMeta& m, int warp, int lane,
+                                           const StepArgs& a) {
   const Cache& c = a.c;
   constexpr int esz = DT == RSSM_F32 ? 4 : (DT == RSSM_BF16 || DT == RSSM_F16) ? 2 : 1;
   constexpr bool k8bit = DT == RSSM_I8 || DT == RSSM_E4M3;
+  static_assert(HPU == 1, "the fold takes one head per unit");
   const int r0 = 8 * warp + 4 * (lane >> 4), c0 = 8 * (lane & 15);
-  const int p = m.p, L = c.L, rs = m.r;
+  const int p = m.p, L = c.L, rs = m.r, tid = threadIdx.x;
   const uint16_t* bg = c.B_cache + static_cast<long long>(m.s) * c.B_stride +
-                       static_cast<long long>(m.h / c.hpg) * L * kDstate + c0;
-#pragma unroll 1
-  for (int j = 0; j < HPU; ++j) {
+                       static_cast<long long>(m.h / c.hpg) * L * kDstate;
+  const uint16_t* xg = c.x_cache + static_cast<long long>(m.s) * c.x_stride + static_cast<long long>(m.h) * L * kDim;
+  // chunk ch of the live rows into buffer ch & 1: thread t < 64 copies 16 bytes
+  // of an x row, 64 <= t < 192 of a B row (rows past the prefix are skipped)
+  auto issue = [&](int ch) {
+    uint8_t* dst = fbuf + (ch & 1) * kFoldBufOne;
+    const int jj = tid < 64 ? tid >> 3 : (tid - 64) >> 4, jt = static_cast<int>(kFoldChunk) * ch + jj;
+    if (tid < 192 && jt < p) {
+      const int q = rs + jt >= L ? rs + jt - L : rs + jt;  // ring slot of live token jt
+      if (tid < 64)
+        cp_async16(dst + jj * kDim * 2 + (tid & 7) * 16, xg + q * kDim + (tid & 7) * 8);
+      else
+        cp_async16(dst + kFoldBufX + jj * kDstate * 2 + ((tid - 64) & 15) * 16, bg + q * kDstate + ((tid - 64) & 15) * 8);
+    }
+    asm volatile("cp.async.commit_group;" ::: "memory");
+  };
+  // all consumer warps at one point (each thread's copies waited for first)
+  auto cons_sync = [&]() -> bool {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(fsync);
+    const bool ok = mbar_wait(fsync, fph);
+    fph ^= 1u;
+    if (!ok && lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+    return ok;
+  };
+  const int nch = (p + static_cast<int>(kFoldChunk) - 1) / static_cast<int>(kFoldChunk);
+  if (nch > 0) issue(0);
+  {
+    const int j = 0;
     const float* fw = reinterpret_cast<const float*>(sb + lay.fw_off) + j * kFoldW;
-    const uint16_t* xg = c.x_cache + static_cast<long long>(m.s) * c.x_stride +
-                         static_cast<long long>(m.h + j) * L * kDim + r0;
     const float decay = fw[32];
     float2 acc[4][4];
 #pragma unroll
@@ -363,14 +392,24 @@ __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& 
 #pragma unroll
       for (int q = 0; q < 4; ++q) acc[i4][q] = make_float2(__fmul_rn(decay, v[2 * q]), __fmul_rn(decay, v[2 * q + 1]));
     }
+    for (int ch = 0; ch < nch; ++ch) {
+      if (ch + 1 < nch) {
+        issue(ch + 1);
+        asm volatile("cp.async.wait_group 1;" ::: "memory");
+      } else {
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+      }
+      if (!cons_sync()) return false;  // every consumer thread's copies of chunk ch have landed
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(fbuf + (ch & 1) * kFoldBufOne);
+      const uint16_t* bs = reinterpret_cast<const uint16_t*>(fbuf + (ch & 1) * kFoldBufOne + kFoldBufX);
+      const int jend = min(static_cast<int>(kFoldChunk), p - static_cast<int>(kFoldChunk) * ch);
 #pragma unroll 4
-    for (int jt = 0; jt < p; ++jt) {
-      const int q = rs + jt >= L ? rs + jt - L : rs + jt;  // ring slot of live token jt
-      const float w = fw[jt];
-      const uint2 xw = __ldg(reinterpret_cast<const uint2*>(xg + q * kDim));
+    for (int jj = 0; jj < jend; ++jj) {
+      const float w = fw[static_cast<int>(kFoldChunk) * ch + jj];
+      const uint2 xw = *reinterpret_cast<const uint2*>(xs + jj * kDim + r0);
       const float u0v = __fmul_rn(w, bf16lo(xw.x)), u1v = __fmul_rn(w, bf16hi(xw.x));
       const float u2v = __fmul_rn(w, bf16lo(xw.y)), u3v = __fmul_rn(w, bf16hi(xw.y));
-      const uint4 bw = __ldg(reinterpret_cast<const uint4*>(bg + q * kDstate));
+      const uint4 bw = *reinterpret_cast<const uint4*>(bs + jj * kDstate + c0);
       const float2 bb[4] = {make_float2(bf16lo(bw.x), bf16hi(bw.x)), make_float2(bf16lo(bw.y), bf16hi(bw.y)),
                             make_float2(bf16lo(bw.z), bf16hi(bw.z)), make_float2(bf16lo(bw.w), bf16hi(bw.w))};
       const float2 uu[4] = {make_float2(u0v, u0v), make_float2(u1v, u1v), make_float2(u2v, u2v), make_float2(u3v, u3v)};
@@ -378,6 +417,8 @@ __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& 
       for (int i4 = 0; i4 < 4; ++i4)
 #pragma unroll
         for (int q = 0; q < 4; ++q) acc[i4][q] = __ffma2_rn(uu[i4], bb[q], acc[i4][q]);
+    }
+      if (!cons_sync()) return false;  // the buffer of chunk ch is refilled by chunk ch + 2
     }
     float accf[4][8];
 #pragma unroll
@@ -394,6 +435,7 @@ __device__ __forceinline__ void fold_stage(const uint8_t* sb, const ReadLayout& 
     quantize_store<DT>(accf, r0, c0, lane, head_state, head_scale, c.rounding, static_cast<uint32_t>(h),
                        static_cast<uint32_t>(m.s), m.epoch, a.seed);
   }
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -449,6 +491,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       mbar_init(&full[st], 1);
       mbar_init(&empty[st], kConsumerWarps);
     }
+    if (FOLD) mbar_init(full + 16, kConsumerWarps);  // the fold's consumer barrier
     fence_barrier_init();
   }
   __syncthreads();
@@ -611,6 +654,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
   const int d = 8 * warp + g;        // B column (row of S0) this lane loads
   const int dout = 8 * warp + 2 * cq;  // output rows this lane writes (dout, dout + 1)
   uint2 af[8];                          // C block fragments of the current (row, group)
+  uint32_t fph = 0;                     // phase of the fold's consumer barrier
   int st = 0;
   uint32_t ph = 0;
   for (int i = 0;; ++i) {
@@ -638,7 +682,7 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
     }
     if constexpr (FOLD) {
       if (!(m.flags & 1)) {  // a fold of a row without tokens: no outputs
-        fold_stage<DT, HPU>(sb, lay, fold_kb, m, warp, lane, a);
+        if (!fold_stage<DT, HPU>(sb, smem + lay.fbuf_off, full + 16, fph, lay, fold_kb, m, warp, lane, a)) return;
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
         continue;
@@ -683,7 +727,9 @@ __global__ void __maxnreg__(96) readout_kernel(const __grid_constant__ CUtensorM
       }
     }
     if constexpr (FOLD) {
-      if (m.flags & 16) fold_stage<DT, HPU>(sb, lay, fold_kb, m, warp, lane, a);
+      if (m.flags & 16) {
+        if (!fold_stage<DT, HPU>(sb, smem + lay.fbuf_off, full + 16, fph, lay, fold_kb, m, warp, lane, a)) return;
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with the stage
