@@ -39,8 +39,6 @@ __host__ __device__ inline int head_chunk(int hpg) { return hpg < kHeadChunk ? h
 inline size_t precompute_smem(int hpg, int L) {
   return static_cast<size_t>(head_chunk(hpg)) * L * kDim * 2 + static_cast<size_t>(L) * kDstate * 2 + 8 * kDstate * 2;
 }
-// element offset of chunk q (8 elements) of x row k in xs
-__device__ __forceinline__ int xs_chunk(int k, int q) { return k * kDim + (q << 3); }
 
 
 template <int TP>
@@ -51,6 +49,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   __shared__ float hp[3][kHeadChunk];       // A, D, dt_bias of the chunk's heads
   __shared__ __align__(16) float cfs[8][kMaxL][TP];  // per warp: coef[k][t] of its current head
   __shared__ int meta[7];
+  __shared__ __align__(8) uint64_t pbar;  // completion of the chunk's bulk row copies
   const Cache& c = a.c;
   const int b = blockIdx.x / c.G, g = blockIdx.x % c.G;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -58,6 +57,10 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   uint16_t* xs = reinterpret_cast<uint16_t*>(psm);
   uint16_t* bs = xs + head_chunk(hpg) * L * kDim;
   uint16_t* cs = bs + L * kDstate;
+  if (tid == 0) {
+    mbar_init(&pbar, 1);
+    fence_barrier_init();
+  }
   pdl_wait();  // the flush's bookkeeping and checkpoints are complete from here on
   pdl_trigger();
   if (warp == 0) {
@@ -111,28 +114,37 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
   uint16_t* bring = c.B_cache + static_cast<long long>(s) * c.B_stride + static_cast<long long>(g) * L * kDstate;
   uint16_t* xslot = c.x_cache + static_cast<long long>(s) * c.x_stride;
   float* dslot = c.dt_cache + static_cast<long long>(s) * c.dt_stride;
-  // B and C rows of the group
-  for (int idx = tid; idx < K * 16; idx += 256) {
-    const int k = idx >> 4, q = idx & 15;
-    const uint16_t* src = k < p ? bring + ring(k) * kDstate
-                                : a.B + (static_cast<long long>(tok0 + k - p) * G + g) * kDstate;
-    cp_async16(bs + k * kDstate + q * 8, src + q * 8);
-  }
-  if (tid < Tb * 16) {
-    const int t = tid >> 4, q = tid & 15;
-    cp_async16(cs + t * kDstate + q * 8, a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate + q * 8);
-  }
+  const int n1 = p < L - r ? p : L - r;  // live tokens before the ring wraps
   const bool c_f16 = c.dtype == RSSM_F16 || c.dtype == RSSM_I8 || c.dtype == RSSM_E4M3 || c.dtype == RSSM_NVFP4;
-  for (int h0 = 0; h0 < hpg; h0 += kHeadChunk) {
+  for (int h0 = 0, ph = 0; h0 < hpg; h0 += kHeadChunk, ph ^= 1) {
     const int hc = hpg - h0 < kHeadChunk ? hpg - h0 : kHeadChunk, hb = g * hpg + h0;
     if (h0) __syncthreads();  // every warp is done with the previous chunk's rows
-    // x rows: warp w brings the rows of the heads it works on (w, w + 8), 16 bytes a lane
-    for (int hh = warp; hh < hc; hh += 8) {
-      for (int q = lane; q < K * 8; q += 32) {
-        const int k = q >> 3, part = q & 7;
-        const uint16_t* src = k < p ? xslot + (static_cast<long long>(hb + hh) * L + ring(k)) * kDim
-                                    : a.x + (static_cast<long long>(tok0 + k - p) * H + hb + hh) * kDim;
-        cp_async16(xs + hh * L * kDim + xs_chunk(k, part), src + part * 8);
+    // the rows by 1-D bulk copies, counted on pbar: lane hh < hc of warp 0 the
+    // x rows of head hb + hh (the live prefix: at most two ring segments; then
+    // the new rows), lane 16 the group's B rows, lane 17 its C rows (first chunk)
+    if (warp == 0) {
+      if (lane == 0) {
+        const uint32_t bytes = static_cast<uint32_t>(hc * K * kDim * 2 + (h0 == 0 ? (K + Tb) * kDstate * 2 : 0));
+        mbar_arrive_expect_tx(&pbar, bytes);
+      }
+      __syncwarp();
+      if (lane < hc) {
+        uint16_t* dst = xs + lane * L * kDim;
+        const uint16_t* xh = xslot + static_cast<long long>(hb + lane) * L * kDim;
+        if (n1 > 0) bulk_g2s(dst, xh + r * kDim, n1 * kDim * 2, &pbar);
+        if (p > n1) bulk_g2s(dst + n1 * kDim, xh, (p - n1) * kDim * 2, &pbar);
+        for (int t = 0; t < Tb; ++t)
+          bulk_g2s(dst + (p + t) * kDim, a.x + (static_cast<long long>(tok0 + t) * H + hb + lane) * kDim, kDim * 2,
+                   &pbar);
+      } else if (lane == 16 && h0 == 0) {
+        if (n1 > 0) bulk_g2s(bs, bring + r * kDstate, n1 * kDstate * 2, &pbar);
+        if (p > n1) bulk_g2s(bs + n1 * kDstate, bring, (p - n1) * kDstate * 2, &pbar);
+        for (int t = 0; t < Tb; ++t)
+          bulk_g2s(bs + (p + t) * kDstate, a.B + (static_cast<long long>(tok0 + t) * G + g) * kDstate, kDstate * 2,
+                   &pbar);
+      } else if (lane == 17 && h0 == 0) {
+        for (int t = 0; t < Tb; ++t)
+          bulk_g2s(cs + t * kDstate, a.C + (static_cast<long long>(tok0 + t) * G + g) * kDstate, kDstate * 2, &pbar);
       }
     }
     for (int idx = tid; idx < hc * 32; idx += 256) {
@@ -149,6 +161,10 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       cp_async4(&hp[2][tid], a.dt_bias + hb + tid);
     }
     cp_async_wait_all();
+    if (!mbar_wait(&pbar, static_cast<uint32_t>(ph))) {
+      if (tid == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+      return;
+    }
     __syncthreads();
     // dt' = softplus(dt + dt_bias) of every (head, new token) of the chunk at
     // once (the exact sequence: these values go into the ring), in place
@@ -203,12 +219,14 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
       }
       __syncthreads();
     }
-    // ring appends of the chunk's new x rows
-    for (int idx = tid; idx < hc * 64; idx += 256) {
-      const int hh = idx >> 6, t = (idx >> 3) & 7, q = idx & 7;
-      if (t < Tb)
-        reinterpret_cast<uint4*>(xslot + (static_cast<long long>(hb + hh) * L + ring(p + t)) * kDim)[q] =
-            *reinterpret_cast<const uint4*>(xs + hh * L * kDim + xs_chunk(p + t, q));
+    // ring appends of the chunk's new x rows: lane hh < hc of warp 1, one bulk
+    // copy a row out of shared memory (completed at the end of the chunk)
+    if (warp == 1 && lane < hc && Tb > 0) {
+      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+      for (int t = 0; t < Tb; ++t)
+        bulk_s2g(xslot + (static_cast<long long>(hb + lane) * L + ring(p + t)) * kDim,
+                 xs + lane * L * kDim + (p + t) * kDim, kDim * 2);
+      bulk_commit();
     }
     if (h0) __syncthreads();  // the chunk's dt' (the first chunk synchronised above)
     for (int hh = warp; hh < hc; hh += 8) {
@@ -293,6 +311,7 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
         if (t < Tb) *reinterpret_cast<float2*>(blk + rblk_offset(t, 2 * lane)) = R[t];
       __syncwarp();  // cfs is rewritten for the warp's next head
     }
+    if (warp == 1 && lane < hc) bulk_wait_all();  // the chunk's x appends are written (xs is reused next)
   }
 }
 
