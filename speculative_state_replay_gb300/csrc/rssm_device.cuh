@@ -105,16 +105,6 @@ __device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gmem_src, u
       "l"(gmem_src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
-// 1-D bulk copy shared -> global in the thread's bulk group (both addresses
-// 16-byte aligned, size a multiple of 16); bulk_commit() closes the group,
-// bulk_wait_all() waits until every committed copy of the thread is complete.
-__device__ __forceinline__ void bulk_s2g(void* gmem_dst, const void* smem_src, uint32_t bytes) {
-  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gmem_dst), "r"(smem_addr(smem_src)),
-               "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // Per-thread asynchronous copies global -> shared (16 bytes through L2 only,
 // or 4 bytes), all of a thread's copies completed by cp_async_wait_all().
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
