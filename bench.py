@@ -1,9 +1,10 @@
 """Benchmark: one decode step of the ReplaySSM checkpointing SSU on GB300.
 
-A step = flush + step + accept over one batch of synthetic decode inputs:
-by default (--path split) rssm_flush (classify + fold + bookkeeping) -> rssm_step
-(precompute + readout) -> rssm_accept; with --path fused, rssm_flush_step
-(flush decision + precompute, then the fused fold + readout) -> rssm_accept.
+A step = accept + flush + step over one batch of synthetic decode inputs:
+by default (--path split) rssm_accept_flush (the previous step's accepted
+drafts, then classify + fold + bookkeeping) -> rssm_step (precompute +
+readout); with --path fused, rssm_flush_step (flush decision + precompute,
+then the fused fold + readout) -> rssm_accept.
 Default workload: the largest batch of the decode sweep -- 1024 rows of 2049
 slots, 128 heads in 8 groups, bf16 checkpoints, window 16, 1..5 draft tokens
 per row through cu_seqlens, padded slot pages, prefilled rings.
@@ -341,8 +342,11 @@ def run_gpu(args, rank, ws, local):
     shapes = dict(x=((max_tok, wl.nheads, 64), torch.int16), dt=((max_tok, wl.nheads), torch.float32),
                   B=((max_tok, wl.ngroups, 128), torch.int16), C=((max_tok, wl.ngroups, 128), torch.int16),
                   acc=((ids.size,), torch.int32))
+    fused = args.path == "fused"
     if wl.varlen:
         shapes["cu"] = ((ids.size + 1,), torch.int32)
+        if not fused:  # the sequence bounds of the acceptance the step's rssm_accept_flush applies
+            shapes["pcu"] = ((ids.size + 1,), torch.int32)
     esize = {torch.int16: 2, torch.int32: 4, torch.float32: 4}
     offs, total = {}, 0
     for key, (shp, dtp) in shapes.items():
@@ -353,14 +357,27 @@ def run_gpu(args, rank, ws, local):
         v = {key: raw[offs[key]: offs[key] + int(np.prod(shp)) * esize[dtp]].view(dtp).view(shp)
              for key, (shp, dtp) in shapes.items()}
         v.setdefault("cu", None)
+        v.setdefault("pcu", None)
         return v
 
     dbuf = torch.zeros(total, dtype=torch.uint8, device=dev)
     buf = views(dbuf)
     pin = lambda a: torch.from_numpy(np.ascontiguousarray(a))  # noqa: E731  (host copies of the inputs)
-    hin = [dict(x=pin(i.x.view(np.int16)), dt=pin(i.dt), B=pin(i.B.view(np.int16)), C=pin(i.C.view(np.int16)),
-                acc=pin(i.accepted), cu=None if i.cu_seqlens is None else pin(i.cu_seqlens), ntok=i.ntok)
-           for i in host]
+    # the acceptance a step's launches apply: with --path fused this step's
+    # (rssm_accept after the step); otherwise the previous step's, applied by
+    # this step's rssm_accept_flush (none before the first step, and none under
+    # --full-window, whose rows fold exactly max_window tokens)
+    hin = []
+    for k, i in enumerate(host):
+        if fused:
+            acc, pcu = i.accepted, None
+        else:
+            prev = host[k - 1] if k > 0 and not args.full_window else None
+            acc = prev.accepted if prev is not None else np.zeros_like(i.accepted)
+            pcu = None if i.cu_seqlens is None else (prev.cu_seqlens if prev is not None else i.cu_seqlens)
+        hin.append(dict(x=pin(i.x.view(np.int16)), dt=pin(i.dt), B=pin(i.B.view(np.int16)), C=pin(i.C.view(np.int16)),
+                        acc=pin(acc), cu=None if i.cu_seqlens is None else pin(i.cu_seqlens),
+                        pcu=None if pcu is None else pin(pcu), ntok=i.ntok))
     dev_inp = [{k: (v.to(dev) if torch.is_tensor(v) else v) for k, v in hi.items()} for hi in hin]
     out = torch.zeros((max_tok, wl.nheads, 64), dtype=torch.int16, device=dev)
     scr_flush = api.alloc_scratch(gc, ids.size, wl.T)
@@ -392,15 +409,16 @@ def run_gpu(args, rank, ws, local):
         buf["acc"].copy_(src["acc"], non_blocking=non_blocking)
         if cu is not None:
             cu.copy_(src["cu"], non_blocking=non_blocking)
-
-    fused = args.path == "fused"
+        if buf["pcu"] is not None:
+            buf["pcu"].copy_(src["pcu"], non_blocking=non_blocking)
 
     def step_groups(bv, yv):
         """The launch groups of one step on input buffers `bv` and output `yv`."""
         cuv = bv["cu"]
 
         def g_flush():
-            api.rssm_flush(gc, gA, gids, pnat, wl.T, scr_flush, cu_seqlens=cuv, force=force, seed=wl.sr_seed)
+            api.rssm_accept_flush(gc, gA, gids, pnat, bv["acc"], wl.T, wl.T, scr_flush, accept_cu_seqlens=bv["pcu"],
+                                  cu_seqlens=cuv, force=force, seed=wl.sr_seed)
 
         def g_pre():
             api.rssm_step_precompute(gc, bv["x"], bv["dt"], gA, bv["B"], bv["C"], gD, gb, gids, pnat, wl.T, yv,
@@ -421,14 +439,14 @@ def run_gpu(args, rank, ws, local):
             api.rssm_flush_step_main(gc, bv["x"], bv["dt"], gA, bv["B"], bv["C"], gD, gb, gids, pnat, wl.T, yv,
                                      scr_step, cu_seqlens=cuv, force=force, seed=wl.sr_seed)
 
-        return [g_fpre, g_fread, g_acc] if fused else [g_flush, g_pre, g_read, g_acc]
+        return [g_fpre, g_fread, g_acc] if fused else [g_flush, g_pre, g_read]
 
     # the launch groups of one step; `rg` is the dominant kernel's group
     groups = step_groups(buf, out)
     if fused:
         names, rg = ["precompute", "readout_fold", "accept"], 1
     else:
-        names, rg = ["flush", "precompute", "readout", "accept"], 2
+        names, rg = ["accept_flush", "precompute", "readout"], 2
     # a second set of device inputs and output: the end-to-end leg alternates
     # between the two so one step's copies overlap the neighbouring steps' work
     dbuf_b = torch.zeros(total, dtype=torch.uint8, device=dev) if not args.no_e2e else None
@@ -584,6 +602,8 @@ def run_gpu(args, rank, ws, local):
             hv["acc"].copy_(hi["acc"])
             if cu is not None:
                 hv["cu"].copy_(hi["cu"])
+            if hv["pcu"] is not None:
+                hv["pcu"].copy_(hi["pcu"])
         yh = [torch.empty((max_tok, wl.nheads, 64), dtype=torch.int16, pin_memory=True) for _ in range(2)]
         e2e_units = sum(host_units(k) for k in ks)
         d2h_sum = sum(hin[k]["ntok"] for k in ks) * wl.nheads * 64 * 2
@@ -653,7 +673,8 @@ def run_gpu(args, rank, ws, local):
         e2e = {"value": sum_over_ranks(e2e_units, ws, dev) / (t_e2e / 1e3), "unit": UNIT,
                "h2d_bytes_per_step": int(total), "d2h_bytes_per_step": int(d2h_sum // n_e2e),
                "ms_per_step": t_e2e / n_e2e,
-               "mode": "rssm_flush -> rssm_step -> rssm_accept on a compute stream, every step's inputs copied in "
+               "mode": ("rssm_flush_step -> rssm_accept" if fused else "rssm_accept_flush -> rssm_step") +
+                       " on a compute stream, every step's inputs copied in "
                        "from pinned host memory (one H2D copy per step) and its y copied back (one D2H copy), "
                        "copies on two other streams overlapping the neighbouring steps' kernels; two device "
                        f"input/output sets alternate; {n_stage} pinned input sets (the inputs of the first "
@@ -696,7 +717,7 @@ def run_gpu(args, rank, ws, local):
     fold_achieved = fold_bytes / (sum(flush_ms) / 1e3) / 1e9 if sum(flush_ms) > 0 else 0.0
     flush_roofline = None
     if not fused:
-        flush_roofline = {"bound": "hbm", "kernel": "flush_kernel", "achieved": fold_achieved,
+        flush_roofline = {"bound": "hbm", "kernel": "flush_kernel (rssm_accept_flush)", "achieved": fold_achieved,
                           "peak": peak, "unit": "GB/s", "frac": fold_achieved / peak,
                           "avg_us": 1e3 * statistics.mean(flush_ms),
                           "algorithmic_bytes_per_step": fold_bytes / args.steps}
@@ -730,8 +751,8 @@ def run_gpu(args, rank, ws, local):
         "flush_roofline": flush_roofline,
         "flush_roofline_full_window": fw_roofline,
         "e2e": e2e,
-        # per timed step: precompute, readout with fold, accept (split: flush, precompute, readout, accept)
-        "gpu_launches": (3 if fused else 4) * args.steps,
+        # per timed step: precompute, readout with fold, accept (split: accept + flush, precompute, readout)
+        "gpu_launches": 3 * args.steps,
         "clocks": clk,
         "device_time_ms": dict({"step": statistics.mean(step_ms)},
                                **{n: statistics.mean(v) for n, v in zip(names, grp_ms)}),

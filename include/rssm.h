@@ -62,6 +62,8 @@
  *                     prefix into S0, advance ring_start, reset pnat
  *     rssm_step    -- outputs for the drafts; appends them to the rings
  *     rssm_accept  -- pnat += accepted drafts (after verification)
+ * (rssm_accept_flush takes a step's rssm_accept and the next step's
+ * rssm_flush in one launch.)
  */
 #ifndef RSSM_H
 #define RSSM_H
@@ -203,6 +205,27 @@ rssm_status rssm_init_state(const rssm_cache *cache, const float *states, const 
 rssm_status rssm_flush(const rssm_cache *cache, const float *A, const int32_t *slot_idx, int32_t *pnat,
                        const int32_t *cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
                        void *scratch, size_t scratch_bytes, void *stream);
+
+/*
+ * The previous step's acceptance and this step's flush in one launch: the
+ * same results, bit for bit (pnat, checkpoints, 8-bit scales, rings,
+ * ring_start, flush_epoch, error bits), as
+ *   rssm_accept(cache, slot_idx, pnat, accepted, accept_cu_seqlens, batch, accept_T, stream)
+ *   rssm_flush(cache, A, slot_idx, pnat, cu_seqlens, batch, T, force, seed, scratch, scratch_bytes, stream)
+ * A row whose acceptance fails rssm_accept's checks keeps its pnat (and sets
+ * the error bit, as rssm_accept does) and is then classified like any other.
+ * The decode loop becomes: rssm_accept_flush (the drafts verified after the
+ * previous rssm_step), then rssm_step; one launch fewer per step.
+ *   accepted          [batch] i32 (device, required)
+ *   accept_cu_seqlens [batch+1] i32 (device) or NULL: the previous step's
+ *                     sequence bounds (NULL: accept_T tokens a row)
+ *   accept_T          the previous step's T
+ * The other arguments as in rssm_flush.
+ */
+rssm_status rssm_accept_flush(const rssm_cache *cache, const float *A, const int32_t *slot_idx, int32_t *pnat,
+                              const int32_t *accepted, const int32_t *accept_cu_seqlens, int32_t accept_T,
+                              const int32_t *cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
+                              void *scratch, size_t scratch_bytes, void *stream);
 
 /*
  * Step: replay/readout and ring append ([FI] Description items 1-2).  For

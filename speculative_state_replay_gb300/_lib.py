@@ -33,7 +33,7 @@ class RssmCacheStruct(ctypes.Structure):
 
 
 EXPORTS = ("rssm_scratch_bytes", "rssm_init_state", "rssm_flush", "rssm_step", "rssm_step_precompute",
-           "rssm_step_readout", "rssm_step_gated", "rssm_step_readout_gated", "rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main", "rssm_accept", "rssm_eval_spec_math", "rssm_selftest_wait_timeout",
+           "rssm_step_readout", "rssm_step_gated", "rssm_step_readout_gated", "rssm_flush_step", "rssm_flush_step_classify", "rssm_flush_step_main", "rssm_accept", "rssm_accept_flush", "rssm_eval_spec_math", "rssm_selftest_wait_timeout",
            "rssm_status_string")
 
 
@@ -69,6 +69,8 @@ def load(path: str | None = None):
             getattr(lib, name).argtypes = [cp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, u64, vp, vp, sz, vp]
         lib.rssm_accept.restype = ctypes.c_int
         lib.rssm_accept.argtypes = [cp, vp, vp, vp, vp, i32, i32, vp]
+        lib.rssm_accept_flush.restype = ctypes.c_int
+        lib.rssm_accept_flush.argtypes = [cp, vp, vp, vp, vp, vp, i32, vp, i32, i32, i32, u64, vp, sz, vp]
         lib.rssm_eval_spec_math.restype = ctypes.c_int
         lib.rssm_eval_spec_math.argtypes = [vp, vp, vp, i64, vp]
         lib.rssm_selftest_wait_timeout.restype = ctypes.c_int

@@ -176,6 +176,14 @@ def rssm_flush(cache, A, slot_idx, pnat, T, scratch, cu_seqlens=None, force=0, s
                                                 _ptr(scratch), scratch.numel(), _stream(stream)))
 
 
+def rssm_accept_flush(cache, A, slot_idx, pnat, accepted, accept_T, T, scratch, accept_cu_seqlens=None,
+                      cu_seqlens=None, force=0, seed=0, stream=None):
+    """rssm_accept(accepted, accept_cu_seqlens, accept_T) then rssm_flush(...), one launch."""
+    _check("rssm_accept_flush", _lib.load().rssm_accept_flush(
+        cache.struct(), _ptr(A), _ptr(slot_idx), _ptr(pnat), _ptr(accepted), _ptr(accept_cu_seqlens), accept_T,
+        _ptr(cu_seqlens), slot_idx.numel(), T, force, seed, _ptr(scratch), scratch.numel(), _stream(stream)))
+
+
 def _step(fn, cache, x, dt, A, B, C, D, dt_bias, slot_idx, pnat, T, out, scratch, cu_seqlens, stream):
     _check_tokens(fn, cache, slot_idx, T, cu_seqlens, x=x, dt=dt, B=B, C=C, out=out)
     f = getattr(_lib.load(), fn)

@@ -25,25 +25,46 @@ namespace rssm {
 // ---------------------------------------------------------------------------
 struct RowFlag {
   int flag, s, p;
+  int book;  // the acceptance applied: pnat[b] becomes p (0 if flagged)
 };
 
 // a row's flush decision: active rows with p + T_b > max_window (all active
-// rows under force); rows failing a check set an error bit (when `errors`)
+// rows under force); rows failing a check set an error bit (when `errors`).
+// With an acceptance (rssm_accept_flush) p is first pnat + accepted, under
+// rssm_accept's checks (a row failing them keeps its pnat).
 __device__ __forceinline__ RowFlag row_flag(const FlushArgs& a, int b, bool errors) {
   const Cache& c = a.c;
-  RowFlag f = {0, 0, 0};
+  RowFlag f = {0, 0, 0, 0};
   // the row's loads are independent: issue them together (one round trip)
   const int s = a.slot_idx[b];
-  const int p = a.pnat[b];
+  int p = a.pnat[b];
   const int Tb = a.cu ? a.cu[b + 1] - a.cu[b] : a.T;
-  if (s >= 1 && s < c.S) {
-    if (Tb < 0 || Tb > a.T) {
+  int acc = 0, Ta = 0;
+  if (a.accepted) {
+    acc = a.accepted[b];
+    Ta = a.acu ? a.acu[b + 1] - a.acu[b] : a.aT;
+  }
+  if (s < 1 || s >= c.S) return f;
+  if (a.accepted) {
+    if (Ta < 0 || Ta > a.aT) {
       if (errors) set_error(c.err, RSSM_ERRBIT_SEQLEN);
-    } else if (p < 0 || p > c.L) {
+    } else if (acc < 0 || acc > Ta) {
+      if (errors) set_error(c.err, RSSM_ERRBIT_ACCEPT);
+    } else if (p < 0 || p + acc > c.L) {
       if (errors) set_error(c.err, RSSM_ERRBIT_PNAT);
-    } else if (a.force || p + Tb > c.W) {
-      f = RowFlag{1, s, p};
+    } else {
+      p += acc;
+      f.book = 1;
     }
+  }
+  f.s = s;
+  f.p = p;
+  if (Tb < 0 || Tb > a.T) {
+    if (errors) set_error(c.err, RSSM_ERRBIT_SEQLEN);
+  } else if (p < 0 || p > c.L) {
+    if (errors) set_error(c.err, RSSM_ERRBIT_PNAT);
+  } else if (a.force || p + Tb > c.W) {
+    f.flag = 1;
   }
   return f;
 }
@@ -220,14 +241,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   int count = 0;
   for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
     const int b = b0 + tid;
-    const RowFlag f = b < a.batch ? row_flag(a, b, blockIdx.x == 0) : RowFlag{0, 0, 0};
+    const RowFlag f = b < a.batch ? row_flag(a, b, blockIdx.x == 0) : RowFlag{0, 0, 0, 0};
     if (f.flag) {
       asm volatile("prefetch.global.L1 [%0];" ::"l"(c.ring_start + f.s));
       asm volatile("prefetch.global.L1 [%0];" ::"l"(c.epoch + f.s));
     }
     count += __syncthreads_count(f.flag);
   }
-  if (count == 0) {  // nothing to fold or book (every CTA sees the same count)
+  if (count == 0 && !a.accepted) {  // nothing to fold or book (every CTA sees the same count)
     if (blockIdx.x == 0 && tid == 0) *a.count = 0;
     return;
   }
@@ -243,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     int base = 0;
     for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
       const int b = b0 + tid;
-      const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0};
+      const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0, 0};
       int tot = 0;
       const int pos = base + block_excl_scan(f.flag, wsum, tot);
       if (f.flag && pos >= li_first && pos <= li_last) {
@@ -258,19 +279,38 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();  // barriers initialised, records in place, this CTA's reads of pnat, ring_start, epoch done
   // The bookkeeping may replace those values once every CTA has read them: the
   // CTA that takes the last ticket writes it (self-resetting ticket), from the
-  // flush records, while its producer issues the first copies.
-  if (tid == 0) {
-    __threadfence();  // this CTA's records are visible before its ticket
-    s_last = atomicInc(a.ticket, gridDim.x - 1) == gridDim.x - 1;
-  }
-  __syncthreads();
-  if (s_last && tid < kConsumerThreads) {
-    __threadfence();
-    for (int k = tid; k < count; k += kConsumerThreads) {
-      const FlushRec rec = a.recs[k];
-      c.ring_start[rec.s] = rec.r + rec.p >= L ? rec.r + rec.p - L : rec.r + rec.p;  // (r + p) mod L
-      a.pnat[rec.b] = 0;
-      c.epoch[rec.s] = rec.epoch;
+  // flush records, with its consumer warps -- while its producer issues the
+  // first copies (the ticket's round trip is off the producer's path).
+  if (warp < kConsumerWarps) {
+    if (tid == 0) {
+      __threadfence();  // this CTA's records are visible before its ticket
+      s_last = atomicInc(a.ticket, gridDim.x - 1) == gridDim.x - 1;
+    }
+    consumer_sync();
+    if (s_last) {
+      __threadfence();
+      if (a.accepted) {
+        // every active row's accepted live count (the flagged rows' 0 below);
+        // a thread's rows are loaded before any of them is written
+        for (int b0 = tid; b0 < a.batch; b0 += 4 * kConsumerThreads) {
+          RowFlag f[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int b = b0 + u * kConsumerThreads;
+            f[u] = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0, 0};
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+            if (f[u].book && !f[u].flag) a.pnat[b0 + u * kConsumerThreads] = f[u].p;
+        }
+        consumer_sync();  // pnat of the flagged rows is read above before it is reset below
+      }
+      for (int k = tid; k < count; k += kConsumerThreads) {
+        const FlushRec rec = a.recs[k];
+        c.ring_start[rec.s] = rec.r + rec.p >= L ? rec.r + rec.p - L : rec.r + rec.p;  // (r + p) mod L
+        a.pnat[rec.b] = 0;
+        c.epoch[rec.s] = rec.epoch;
+      }
     }
   }
 

@@ -207,13 +207,15 @@ rssm_status rssm_init_state(const rssm_cache* cache, const float* states, const 
   return launch_init(a, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
-rssm_status rssm_flush(const rssm_cache* cache, const float* A, const int32_t* slot_idx, int32_t* pnat,
-                       const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
-                       void* scratch, size_t scratch_bytes, void* stream) {
+namespace {
+rssm_status flush_common(const rssm_cache* cache, const float* A, const int32_t* slot_idx, int32_t* pnat,
+                         const int32_t* accepted, const int32_t* accept_cu_seqlens, int32_t accept_T,
+                         const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
+                         void* scratch, size_t scratch_bytes, void* stream) {
   FlushArgs a;
   rssm_status st = check_cache(cache, &a.c);
   if (st != RSSM_OK) return st;
-  if (batch < 0 || T < 0 || (force != 0 && force != 1)) return RSSM_ERR_INVALID_ARGUMENT;
+  if (batch < 0 || T < 0 || accept_T < 0 || (force != 0 && force != 1)) return RSSM_ERR_INVALID_ARGUMENT;
   if (batch == 0) return RSSM_OK;
   if (!A || !slot_idx || !pnat || !scratch || !aligned16(scratch)) return RSSM_ERR_INVALID_ARGUMENT;
   if (scratch_bytes < flush_scratch_bytes(batch)) return RSSM_ERR_SCRATCH_TOO_SMALL;
@@ -227,10 +229,30 @@ rssm_status rssm_flush(const rssm_cache* cache, const float* A, const int32_t* s
   a.T = T;
   a.force = force;
   a.seed = seed;
+  a.accepted = accepted;
+  a.acu = accepted ? accept_cu_seqlens : nullptr;
+  a.aT = accepted ? accept_T : 0;
   a.ticket = static_cast<unsigned*>(scratch);
   a.count = static_cast<int*>(scratch) + 1;
   a.recs = reinterpret_cast<FlushRec*>(static_cast<uint8_t*>(scratch) + kScratchHead);
   return launch_flush(a, sms, stream) == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
+}
+}  // namespace
+
+rssm_status rssm_flush(const rssm_cache* cache, const float* A, const int32_t* slot_idx, int32_t* pnat,
+                       const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
+                       void* scratch, size_t scratch_bytes, void* stream) {
+  return flush_common(cache, A, slot_idx, pnat, nullptr, nullptr, 0, cu_seqlens, batch, T, force, seed, scratch,
+                      scratch_bytes, stream);
+}
+
+rssm_status rssm_accept_flush(const rssm_cache* cache, const float* A, const int32_t* slot_idx, int32_t* pnat,
+                              const int32_t* accepted, const int32_t* accept_cu_seqlens, int32_t accept_T,
+                              const int32_t* cu_seqlens, int32_t batch, int32_t T, int32_t force, uint64_t seed,
+                              void* scratch, size_t scratch_bytes, void* stream) {
+  if (!accepted && batch > 0) return RSSM_ERR_INVALID_ARGUMENT;
+  return flush_common(cache, A, slot_idx, pnat, accepted, accept_cu_seqlens, accept_T, cu_seqlens, batch, T, force,
+                      seed, scratch, scratch_bytes, stream);
 }
 
 rssm_status rssm_step_precompute(const rssm_cache* cache, const void* x, const float* dt, const float* A,

@@ -84,6 +84,10 @@ struct FlushArgs {
   const int* cu;
   int batch, T, force;
   unsigned long long seed;
+  // the previous step's acceptance, applied first (rssm_accept_flush); NULL: none
+  const int* accepted;
+  const int* acu;  // its sequence bounds (NULL: aT tokens a row)
+  int aT;
   unsigned* ticket;  // scratch word: CTAs done with the flush (zero between calls)
   int* count;        // scratch: number of flagged rows (written at the end, for diagnostics)
   FlushRec* recs;    // scratch: flagged rows (written at the end, for diagnostics)

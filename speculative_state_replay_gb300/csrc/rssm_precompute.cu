@@ -34,6 +34,89 @@ inline size_t precompute_smem(int hpg, int L) {
   return static_cast<size_t>(head_chunk(hpg)) * L * kDim * 2 + static_cast<size_t>(L) * kDstate * 2 + 8 * kDstate * 2;
 }
 
+// Replay coefficients and ring term of one head (one warp) for a row with
+// T_b <= 2 NP new tokens, taken as NP token pairs; lane k < K holds dt'_k.
+//   coef[k][t] = e^{c_{p+t} - c_k} dt'_k CB[t][k] (+ D on k = p + t), k <= p + t
+//   R[t][d] = sum_k coef[k][t] x_k[d],  decay[t] = e^{c_{p+t}}
+// Lane k puts coef[k][.] in the warp's cfw row k; lane l then accumulates
+// d = 2l and 2l + 1 for every pair: (R[2j][d], R[2j+1][d]) += (coef[k][2j],
+// coef[k][2j+1]) x_k[d], one f32x2 FMA each.  Writes the T_b rows of the
+// row's ring-term block (chunk-swizzled) and its decays.
+template <int NP, int TP>
+__device__ __forceinline__ void head_ring_term(const float (*CB)[kMaxL], float (*cfw)[TP], const uint32_t* xr,
+                                               float* blk, int lane, int p, int Tb, int K, float Ah, float Dh,
+                                               float dtp) {
+  static_assert(2 * NP <= TP, "token pairs beyond the padded token count");
+  // inclusive prefix sum of A dt' over the lanes (these sums only feed the
+  // outputs, so any summation order is fine here)
+  float cum = lane < K ? Ah * dtp : 0.0f;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const float x = __shfl_up_sync(0xffffffffu, cum, off);
+    if (lane >= off) cum += x;
+  }
+  float cf[2 * NP], dec[8];
+#pragma unroll
+  for (int t = 0; t < 8; ++t) dec[t] = 0.0f;
+#pragma unroll
+  for (int t = 0; t < 2 * NP; ++t) {
+    const int kt = p + t < 31 ? p + t : 31;
+    const float cpt = __shfl_sync(0xffffffffu, cum, kt);
+    float v = 0.0f;
+    if (t < Tb && lane <= p + t) {
+      v = __expf(cpt - cum) * dtp * CB[t][lane];
+      if (lane == p + t) v += Dh;
+    }
+    cf[t] = v;
+    if (t < Tb) dec[t] = __expf(cpt);
+  }
+  if (lane == 0) {
+    float4* d4 = reinterpret_cast<float4*>(blk);
+    d4[0] = make_float4(dec[0], dec[1], dec[2], dec[3]);
+    if (TP == 8) d4[1] = make_float4(dec[4], dec[5], dec[6], dec[7]);
+  }
+#pragma unroll
+  for (int j = 0; j < NP; j += 2) {
+    if (j + 1 < NP)
+      *reinterpret_cast<float4*>(&cfw[lane][2 * j]) = make_float4(cf[2 * j], cf[2 * j + 1], cf[2 * j + 2], cf[2 * j + 3]);
+    else
+      *reinterpret_cast<float2*>(&cfw[lane][2 * j]) = make_float2(cf[2 * j], cf[2 * j + 1]);
+  }
+  __syncwarp();
+  float2 P0[NP], P1[NP];  // (R[2j][2l], R[2j+1][2l]), (R[2j][2l+1], R[2j+1][2l+1])
+#pragma unroll
+  for (int j = 0; j < NP; ++j) P0[j] = P1[j] = make_float2(0.0f, 0.0f);
+#pragma unroll 2
+  for (int k = 0; k < K; ++k) {
+    const uint32_t w = xr[k * (kDim / 2)];
+    const float x0 = bf16lo(w), x1 = bf16hi(w);
+    const float2 X0 = make_float2(x0, x0), X1 = make_float2(x1, x1);
+#pragma unroll
+    for (int j = 0; j < NP; j += 2) {
+      float2 c0, c1;
+      if (j + 1 < NP) {
+        const float4 c4 = *reinterpret_cast<const float4*>(&cfw[k][2 * j]);
+        c0 = make_float2(c4.x, c4.y);
+        c1 = make_float2(c4.z, c4.w);
+      } else {
+        c0 = *reinterpret_cast<const float2*>(&cfw[k][2 * j]);
+      }
+      P0[j] = __ffma2_rn(c0, X0, P0[j]);
+      P1[j] = __ffma2_rn(c0, X1, P1[j]);
+      if (j + 1 < NP) {
+        P0[j + 1] = __ffma2_rn(c1, X0, P0[j + 1]);
+        P1[j + 1] = __ffma2_rn(c1, X1, P1[j + 1]);
+      }
+    }
+  }
+#pragma unroll
+  for (int t = 0; t < 2 * NP; ++t)
+    if (t < Tb)
+      *reinterpret_cast<float2*>(blk + rblk_offset(t, 2 * lane)) =
+          t & 1 ? make_float2(P0[t >> 1].y, P1[t >> 1].y) : make_float2(P0[t >> 1].x, P1[t >> 1].x);
+  __syncwarp();  // cfw is rewritten for the warp's next head
+}
+
 
 template <int TP>
 __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepArgs a) {
@@ -225,67 +308,17 @@ __global__ void __launch_bounds__(256, TP == 4 ? 4 : 3) precompute_kernel(StepAr
         if (lane == 0) fwb[32] = spec_exp(c_end);
       }
       if (Tb == 0) continue;  // nothing to read out (a fold of a row without tokens)
-      // inclusive prefix sum of A dt' over the lanes (these sums only feed the
-      // outputs, so any summation order is fine here)
-      float cum = lane < K ? Ah * dtp : 0.0f;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const float x = __shfl_up_sync(0xffffffffu, cum, off);
-        if (lane >= off) cum += x;
-      }
-      float cf[TP];
-      float dec[TP];
-#pragma unroll
-      for (int t = 0; t < TP; ++t) {
-        const int kt = p + t < 31 ? p + t : 31;
-        const float cpt = __shfl_sync(0xffffffffu, cum, kt);
-        float v = 0.0f;
-        if (t < Tb && lane <= p + t) {
-          v = __expf(cpt - cum) * dtp * CB[t][lane];
-          if (lane == p + t) v += Dh;
-        }
-        cf[t] = v;
-        dec[t] = t < Tb ? __expf(cpt) : 0.0f;
-      }
       float* blk = a.rblk + (static_cast<long long>(b) * H + h) * (kRDec + TP * kDim);
-      if (lane == 0) {
-        float4* d4 = reinterpret_cast<float4*>(blk);
-        d4[0] = make_float4(dec[0], dec[1], dec[2], dec[3]);
-        d4[1] = TP == 8 ? make_float4(dec[TP > 4 ? 4 : 0], dec[TP > 5 ? 5 : 0], dec[TP > 6 ? 6 : 0],
-                                      dec[TP > 7 ? 7 : 0])
-                        : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      }
-      // ring term of this head: R[t][d] = sum_k coef[k][t] x_k[d]; lane k
-      // holds coef[k][.], shared through cfs; lane l accumulates d = 2l, 2l + 1;
-      // blocks of 4 tokens at or past T_b are skipped (zero coefficients)
-#pragma unroll
-      for (int t4 = 0; t4 < TP; t4 += 4)
-        *reinterpret_cast<float4*>(&cfs[warp][lane][t4]) = make_float4(cf[t4], cf[t4 + 1], cf[t4 + 2], cf[t4 + 3]);
-      __syncwarp();
-      float2 R[TP];
-#pragma unroll
-      for (int t = 0; t < TP; ++t) R[t] = make_float2(0.0f, 0.0f);
       const uint32_t* xr = reinterpret_cast<const uint32_t*>(xs + hh * L * kDim) + lane;
-      const bool hi4 = TP > 4 && Tb > 4;
-#pragma unroll 4
-      for (int k = 0; k < K; ++k) {
-        const uint32_t w = xr[k * (kDim / 2)];
-        const float2 xv = make_float2(bf16lo(w), bf16hi(w));
-#pragma unroll
-        for (int t4 = 0; t4 < TP; t4 += 4) {
-          if (t4 > 0 && !hi4) continue;
-          const float4 cv = *reinterpret_cast<const float4*>(&cfs[warp][k][t4]);
-          R[t4 + 0] = __ffma2_rn(make_float2(cv.x, cv.x), xv, R[t4 + 0]);
-          R[t4 + 1] = __ffma2_rn(make_float2(cv.y, cv.y), xv, R[t4 + 1]);
-          R[t4 + 2] = __ffma2_rn(make_float2(cv.z, cv.z), xv, R[t4 + 2]);
-          R[t4 + 3] = __ffma2_rn(make_float2(cv.w, cv.w), xv, R[t4 + 3]);
-        }
-      }
-      // the row's T_b rows, chunk-swizzled (rblk_offset)
-#pragma unroll
-      for (int t = 0; t < TP; ++t)
-        if (t < Tb) *reinterpret_cast<float2*>(blk + rblk_offset(t, 2 * lane)) = R[t];
-      __syncwarp();  // cfs is rewritten for the warp's next head
+      const int np = (Tb + 1) >> 1;  // token pairs the row needs
+      if (np == 1)
+        head_ring_term<1, TP>(CB, cfs[warp], xr, blk, lane, p, Tb, K, Ah, Dh, dtp);
+      else if (np == 2 || TP == 4)
+        head_ring_term<2, TP>(CB, cfs[warp], xr, blk, lane, p, Tb, K, Ah, Dh, dtp);
+      else if (np == 3)
+        head_ring_term<(TP > 4 ? 3 : 2), TP>(CB, cfs[warp], xr, blk, lane, p, Tb, K, Ah, Dh, dtp);
+      else
+        head_ring_term<(TP > 4 ? 4 : 2), TP>(CB, cfs[warp], xr, blk, lane, p, Tb, K, Ah, Dh, dtp);
     }
   }
 }

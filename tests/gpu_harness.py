@@ -138,8 +138,15 @@ def state_close(dtype, g, o, ulps=HALF_STATE_ULPS, carried=False):
 class Pair:
     """Oracle + GPU replicas of one workload."""
 
-    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False, gate=False, resync=True):
+    def __init__(self, orc, wl, oc, ids, pnat, device="cuda", seed=None, fused=False, gate=False, resync=True,
+                 accept_flush=False):
         self.fused = fused  # GPU side through rssm_flush_step instead of rssm_flush + rssm_step
+        # accept_flush: the GPU side applies each step's acceptance in the next
+        # step's rssm_accept_flush (the oracle: flush, step, accept); between
+        # steps the GPU's pnat lacks the pending acceptance
+        self.accept_flush = accept_flush
+        self.pending = None
+        assert not (fused and accept_flush)
         self.gate = gate    # output gate z (seeded N(0, 1), bf16) on both sides, split path only
         # resync: after each comparison the GPU cache is overwritten with the
         # oracle's; without it both sides carry their own checkpoints on (2-byte
@@ -181,11 +188,20 @@ class Pair:
             api.rssm_flush_step(gc, d(inp.x), d(inp.dt), self.gA, d(inp.B), d(inp.C), self.gD, self.gb, self.gids,
                                 self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu, force=force, seed=self.seed)
         else:
-            api.rssm_flush(gc, self.gA, self.gids, self.gpnat, wl.T, self.scratch, cu_seqlens=cu, force=force,
-                           seed=self.seed)
+            if self.accept_flush and self.pending is not None:
+                acc_prev, cu_prev = self.pending
+                api.rssm_accept_flush(gc, self.gA, self.gids, self.gpnat, acc_prev, wl.T, wl.T, self.scratch,
+                                      accept_cu_seqlens=cu_prev, cu_seqlens=cu, force=force, seed=self.seed)
+            else:
+                api.rssm_flush(gc, self.gA, self.gids, self.gpnat, wl.T, self.scratch, cu_seqlens=cu, force=force,
+                               seed=self.seed)
             api.rssm_step(gc, d(inp.x), d(inp.dt), self.gA, d(inp.B), d(inp.C), self.gD, self.gb, self.gids,
                           self.gpnat, wl.T, out, self.scratch, cu_seqlens=cu, z=None if z is None else d(z))
-        api.rssm_accept(gc, self.gids, self.gpnat, d(inp.accepted), wl.T, cu_seqlens=cu)
+        if self.accept_flush:
+            self.pending = (d(inp.accepted), cu)
+            self.pending_host = np.where(self.ids > 0, inp.accepted, 0).astype(np.int32)
+        else:
+            api.rssm_accept(gc, self.gids, self.gpnat, d(inp.accepted), wl.T, cu_seqlens=cu)
         torch.cuda.synchronize()
         y_g = out[: inp.ntok].cpu().numpy().view(np.uint16)
         if check:
@@ -197,7 +213,10 @@ class Pair:
         yg, yo = bf16_f32(y_g), bf16_f32(y_o)
         bad = ~(np.abs(yg - yo) <= Y_ATOL + Y_RTOL * np.abs(yo))
         assert not bad.any(), f"y mismatch at {np.argwhere(bad)[:5].tolist()}: gpu {yg[bad][:5]} oracle {yo[bad][:5]}"
-        assert np.array_equal(self.gpnat.cpu().numpy(), self.pnat), "pnat"
+        gp = self.gpnat.cpu().numpy()
+        if self.accept_flush:  # the acceptance the next step applies
+            gp = gp + self.pending_host
+        assert np.array_equal(gp, self.pnat), "pnat"
         for name in ("ring_start", "flush_epoch", "error_word"):
             assert np.array_equal(host_of(getattr(gc, name), getattr(oc, name)), getattr(oc, name)), name
         for name in ("x_cache", "B_cache", "dt_cache"):
@@ -215,7 +234,8 @@ class Pair:
             self.exact_state_steps += 1
         if self.resync:  # continue from identical state
             sync_gpu_from(gc, oc)
-            self.gpnat.copy_(dev_of(self.pnat, self.device))
+            pn = self.pnat - self.pending_host if self.accept_flush else self.pnat
+            self.gpnat.copy_(dev_of(np.ascontiguousarray(pn, np.int32), self.device))
 
 
 def init_gpu_cache_like_bench(wl, gen, ids, device="cuda"):
