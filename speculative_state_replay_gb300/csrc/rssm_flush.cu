@@ -133,7 +133,7 @@ struct FoldMeta {
 struct FoldLayout {
   int ns, KB;
   uint32_t s0_bytes, scale_off, x_off, b_off, dt_off, sc_off, stage_bytes;
-  uint32_t meta_off, rows_off, stages_off, u2_off, total;
+  uint32_t meta_off, rows_off, stages_off, total;
 };
 
 // 2-byte states: S0 arrives as the readout's TMA boxes (64 rows x 128 bytes,
@@ -145,9 +145,8 @@ __host__ __device__ constexpr int fold_xs(int dtype) { return fold_2byte(dtype) 
 __host__ __device__ constexpr int fold_bs(int dtype) { return fold_2byte(dtype) ? kDstate + 8 : kDstate; }  // B row stride (elements)
 
 // barriers | per-stage metadata | the records of the flushed rows this CTA
-// folds (up to `maxrows`) | stages | per consumer warp, the canonical fold's
-// u_j of its 8 rows as (u, u) pairs [KB][8] float2; one stage: S0 | 8-bit
-// scales | live x rows | live B rows | live dt' | A of the head
+// folds (up to `maxrows`) | stages; one stage: S0 | 8-bit scales | live x rows
+// | live B rows | live dt' | A of the head
 __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int maxrows) {
   FoldLayout f;
   f.ns = ns;
@@ -170,8 +169,7 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int 
   f.meta_off = 256;  // after the barriers
   f.rows_off = 512;
   f.stages_off = (f.rows_off + maxrows * static_cast<uint32_t>(sizeof(FlushRec)) + align - 1) & ~(align - 1);
-  f.u2_off = f.stages_off + f.ns * f.stage_bytes;
-  f.total = f.u2_off + kConsumerWarps * f.KB * 8 * 8 + (align == 1024u ? 1024u : 0u);  // + slack to align the base
+  f.total = f.stages_off + f.ns * f.stage_bytes + (align == 1024u ? 1024u : 0u);  // + slack to align the base
   return f;
 }
 
@@ -522,80 +520,60 @@ __global__ void __launch_bounds__(kThreads, 2)
         continue;
       }
     }
-    // u_j[d] = w_j x_j[d] in fp32 (one rounding, as in the canonical chain)
-    // for the warp's 8 rows, kept as (u, u) pairs so that the fold's packed
-    // FMAs take them straight from shared memory: lane j < p converts token j
-    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
-    const uint16_t* bs = reinterpret_cast<const uint16_t*>(sb + lay.b_off);
-    float4* u2w = reinterpret_cast<float4*>(smem + lay.u2_off) + warp * lay.KB * 4;
-    if (lane < p) {
-      const uint4 xw = *reinterpret_cast<const uint4*>(xs + lane * kDim + 8 * warp);
-      const uint32_t xq[4] = {xw.x, xw.y, xw.z, xw.w};
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const float u0 = __fmul_rn(wj, bf16lo(xq[q])), u1 = __fmul_rn(wj, bf16hi(xq[q]));
-        u2w[lane * 4 + q] = make_float4(u0, u0, u1, u1);
-      }
-    }
-    // acc = e^{c_end} * S0f (S0f = the stored value, code x scale for 8-bit)
+    // acc = e^{c_end} * S0f
     float2 acc[4][4];
-    const float2 dec2 = make_float2(decay, decay);
 #pragma unroll
     for (int i4 = 0; i4 < 4; ++i4) {
       const int row = r0 + i4;
-      float2 v[4];
+      float v[8];
       if constexpr (DT == RSSM_F32) {
         const float4* p4 = reinterpret_cast<const float4*>(sb + (row * kDstate + c0) * 4);
         const float4 x0 = p4[0], x1 = p4[1];
-        v[0] = make_float2(x0.x, x0.y); v[1] = make_float2(x0.z, x0.w);
-        v[2] = make_float2(x1.x, x1.y); v[3] = make_float2(x1.z, x1.w);
+        v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w;
+        v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
       } else if constexpr (DT == RSSM_BF16) {
         const uint4 q = *reinterpret_cast<const uint4*>(sb + swizzled_offset<2>(row, c0));
-        v[0] = make_float2(bf16lo(q.x), bf16hi(q.x)); v[1] = make_float2(bf16lo(q.y), bf16hi(q.y));
-        v[2] = make_float2(bf16lo(q.z), bf16hi(q.z)); v[3] = make_float2(bf16lo(q.w), bf16hi(q.w));
+        v[0] = bf16lo(q.x); v[1] = bf16hi(q.x); v[2] = bf16lo(q.y); v[3] = bf16hi(q.y);
+        v[4] = bf16lo(q.z); v[5] = bf16hi(q.z); v[6] = bf16lo(q.w); v[7] = bf16hi(q.w);
       } else if constexpr (DT == RSSM_F16) {
         const uint4 q = *reinterpret_cast<const uint4*>(sb + swizzled_offset<2>(row, c0));
-        v[0] = h2f2(q.x); v[1] = h2f2(q.y); v[2] = h2f2(q.z); v[3] = h2f2(q.w);
+        float2 t0 = h2f2(q.x), t1 = h2f2(q.y), t2 = h2f2(q.z), t3 = h2f2(q.w);
+        v[0] = t0.x; v[1] = t0.y; v[2] = t1.x; v[3] = t1.y; v[4] = t2.x; v[5] = t2.y; v[6] = t3.x; v[7] = t3.y;
       } else {
         const uint2 q = *reinterpret_cast<const uint2*>(sb + row * kDstate + c0);
         const float sc = reinterpret_cast<const float*>(sb + lay.scale_off)[row];
-        const float2 sc2 = make_float2(sc, sc);
 #pragma unroll
-        for (int e2 = 0; e2 < 4; ++e2) {
-          const uint32_t w = e2 < 2 ? q.x : q.y;
-          const int e = 2 * e2;
-          float2 code;
+        for (int e = 0; e < 8; ++e) {
+          const uint32_t w = e < 4 ? q.x : q.y;
+          float code;
           if constexpr (DT == RSSM_I8) {
             // code q as fp32 without a conversion instruction:
             // (2^23 + (q + 128)) - (2^23 + 128), every step exact
-            const float2 biased = make_float2(
-                __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | (e & 3))),
-                __uint_as_float(__byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | ((e + 1) & 3))));
-            code = __fadd2_rn(biased, make_float2(-8388736.0f, -8388736.0f));
+            const uint32_t bits = __byte_perm(w ^ 0x80808080u, 0x4B000000u, 0x7540u | (e & 3));
+            code = __fsub_rn(__uint_as_float(bits), 8388736.0f);
           } else {
-            code = make_float2(e4m3_to_f32(static_cast<uint8_t>((w >> (8 * (e & 3))) & 0xffu)),
-                               e4m3_to_f32(static_cast<uint8_t>((w >> (8 * ((e + 1) & 3))) & 0xffu)));
+            code = e4m3_to_f32(static_cast<uint8_t>((w >> (8 * (e & 3))) & 0xffu));
           }
-          v[e2] = __fmul2_rn(code, sc2);
+          v[e] = __fmul_rn(code, sc);
         }
       }
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        // (2-byte kernels, which also hold the tensor-core fold, multiply one
-        // at a time and stay within their registers)
-        acc[i4][q] = k2B ? make_float2(__fmul_rn(decay, v[q].x), __fmul_rn(decay, v[q].y)) : __fmul2_rn(dec2, v[q]);
+        acc[i4][q] = make_float2(__fmul_rn(decay, v[2 * q]), __fmul_rn(decay, v[2 * q + 1]));
     }
-    // acc[d][n] = fma(u_j[d], B_j[n], acc), j ascending
-    __syncwarp();  // the warp's u pairs are in place
-    const float4* u2r = u2w + 2 * (lane >> 4);  // this lane's rows r0..r0+3
-#pragma unroll 2
+    // acc[d][n] = fma(u_j[d], B_j[n], acc), j ascending, u_j[d] = w_j x_j[d]
+    const uint16_t* xs = reinterpret_cast<const uint16_t*>(sb + lay.x_off);
+    const uint16_t* bs = reinterpret_cast<const uint16_t*>(sb + lay.b_off);
+#pragma unroll 4
     for (int j = 0; j < p; ++j) {
-      const float4 ua = u2r[j * 4], ub = u2r[j * 4 + 1];
+      const float w = __shfl_sync(0xffffffffu, wj, j);
+      const uint2 xw = *reinterpret_cast<const uint2*>(xs + j * kDim + r0);
+      const float u0v = __fmul_rn(w, bf16lo(xw.x)), u1v = __fmul_rn(w, bf16hi(xw.x));
+      const float u2v = __fmul_rn(w, bf16lo(xw.y)), u3v = __fmul_rn(w, bf16hi(xw.y));
       const uint4 bw = *reinterpret_cast<const uint4*>(bs + j * kDstate + c0);
       const float2 bb[4] = {make_float2(bf16lo(bw.x), bf16hi(bw.x)), make_float2(bf16lo(bw.y), bf16hi(bw.y)),
                             make_float2(bf16lo(bw.z), bf16hi(bw.z)), make_float2(bf16lo(bw.w), bf16hi(bw.w))};
-      const float2 uu[4] = {make_float2(ua.x, ua.y), make_float2(ua.z, ua.w), make_float2(ub.x, ub.y),
-                            make_float2(ub.z, ub.w)};
+      const float2 uu[4] = {make_float2(u0v, u0v), make_float2(u1v, u1v), make_float2(u2v, u2v), make_float2(u3v, u3v)};
 #pragma unroll
       for (int i4 = 0; i4 < 4; ++i4)
 #pragma unroll
