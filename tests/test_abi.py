@@ -91,6 +91,12 @@ def test_entry_points_reject_bad_arguments_before_launching(lib):
     assert lib.rssm_flush(c, p, p, p, nul, 4, 4, 0, 0, p, 8, nul) == 3
     assert lib.rssm_init_state(c, ctypes.c_void_p((1 << 20) + 4), p, 2, 0, nul) == 1  # misaligned states
     assert lib.rssm_accept(c, nul, nul, nul, nul, 4, 4, nul) == 1
+    # rssm_accept_flush(cache, A, slot_idx, pnat, accepted, accept_cu, accept_T, cu, batch, T, force, seed, ...)
+    assert lib.rssm_accept_flush(c, p, p, p, nul, nul, 4, nul, 4, 4, 0, 0, p, 1 << 20, nul) == 1  # no accepted
+    assert lib.rssm_accept_flush(c, p, p, p, p, nul, -1, nul, 4, 4, 0, 0, p, 1 << 20, nul) == 1  # accept_T < 0
+    assert lib.rssm_accept_flush(c, p, p, p, p, nul, 4, nul, 4, 4, 2, 0, p, 1 << 20, nul) == 1  # force not 0/1
+    assert lib.rssm_accept_flush(c, p, p, p, p, nul, 4, nul, 4, 4, 0, 0, p, 8, nul) == 3
+    assert lib.rssm_accept_flush(c, p, p, p, nul, nul, 4, nul, 0, 4, 0, 0, p, 0, nul) == 0  # empty batch
     # empty batches are a no-op
     assert lib.rssm_step(c, *args, 0, 4, p, p, 0, nul) == 0
     assert lib.rssm_flush(c, p, p, p, nul, 0, 4, 0, 0, p, 0, nul) == 0
