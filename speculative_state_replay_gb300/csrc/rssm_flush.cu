@@ -10,7 +10,10 @@
 //       S0' = e^{c_end} S0 + sum_j e^{c_end-c_j} dt'_j x_j (x) B_j
 //   in fp32, canonical order, then rounds to the state format; the CTA that
 //   finishes classifying last advances the ring bookkeeping (ring_start += p
-//   mod L, pnat = 0, epoch += 1) while the folds run.
+//   mod L, pnat = 0, epoch += 1) while the folds run.  Under
+//   rssm_accept_flush the classification first applies the previous step's
+//   acceptance (pnat += accepted, under rssm_accept's checks) and the
+//   bookkeeping writes every active row's new pnat.
 #include <cuda_runtime.h>
 
 #include <cstring>
