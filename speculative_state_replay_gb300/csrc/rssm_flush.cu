@@ -135,7 +135,7 @@ struct FoldMeta {
 
 struct FoldLayout {
   int ns, KB;
-  uint32_t s0_bytes, scale_off, x_off, b_off, dt_off, sc_off, stage_bytes;
+  uint32_t s0_bytes, scale_off, x_off, b_off, dt_off, sc_off, w_off, stage_bytes;
   uint32_t meta_off, rows_off, stages_off, total;
 };
 
@@ -149,7 +149,7 @@ __host__ __device__ constexpr int fold_bs(int dtype) { return fold_2byte(dtype) 
 
 // barriers | per-stage metadata | the records of the flushed rows this CTA
 // folds (up to `maxrows`) | stages; one stage: S0 | 8-bit scales | live x rows
-// | live B rows | live dt' | A of the head
+// | live B rows | live dt' | A of the head | the fold weights
 __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int maxrows) {
   FoldLayout f;
   f.ns = ns;
@@ -168,6 +168,8 @@ __host__ __device__ inline FoldLayout fold_layout(int dtype, int L, int ns, int 
   o += f.KB * 4;
   f.sc_off = o;
   o += 16;
+  f.w_off = o;  // the fold weights w_j (32 floats) and e^{c_end}, written by the weights warp
+  o += 48 * 4;
   f.stage_bytes = (o + align - 1) & ~(align - 1);
   f.meta_off = 256;  // after the barriers
   f.rows_off = 512;
@@ -209,15 +211,19 @@ __device__ __forceinline__ void store_read_checkpoint(const Cache& c, float (&ac
 // those units.  The bookkeeping is written by the CTA that takes the last ticket
 // once it has classified (a self-resetting ticket), i.e. after every CTA has
 // read the values it replaces; nothing in the kernel reads them afterwards.
+// the flush's CTA: 8 consumer warps, the producer warp, the weights warp
+constexpr int kWeightsWarp = kConsumerWarps + 1;
+constexpr int kFlushThreads = kThreads + 32;
+
 template <int DT>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kFlushThreads, 2)
     flush_kernel(const __grid_constant__ CUtensorMap s0map, FlushArgs a, int ns, int maxrows) {
   extern __shared__ __align__(128) uint8_t smem_raw[];
   constexpr bool k2B = fold_2byte(DT);
   constexpr int XS = fold_xs(DT), BS = fold_bs(DT);
   uint8_t* smem = k2B ? reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023))
                       : smem_raw;
-  __shared__ int wsum[kThreads / 32];
+  __shared__ int wsum[kFlushThreads / 32];
   __shared__ int s_last;
   const Cache& c = a.c;
   const FoldLayout lay = fold_layout(DT, c.L, ns, maxrows);
@@ -226,6 +232,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int L = c.L, H = c.H;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + 8;
+  uint64_t* wready = full + 16;  // the stage's fold weights are in place
   FoldMeta* meta = reinterpret_cast<FoldMeta*>(smem + lay.meta_off);
   FlushRec* rows_s = reinterpret_cast<FlushRec*>(smem + lay.rows_off);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -234,6 +241,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int st = 0; st < lay.ns; ++st) {
       mbar_init(&full[st], 1 + 32);  // producer lane 0 + one cp.async arrival per producer lane
       mbar_init(&empty[st], kConsumerWarps);
+      mbar_init(&wready[st], 1);
     }
     fence_barrier_init();
   }
@@ -242,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   // pass 1: the number of flushed rows (CTA 0 reports bad rows); the flagged
   // rows' ring start and epoch are prefetched for pass 2
   int count = 0;
-  for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+  for (int b0 = 0; b0 < a.batch; b0 += kFlushThreads) {
     const int b = b0 + tid;
     const RowFlag f = b < a.batch ? row_flag(a, b, blockIdx.x == 0) : RowFlag{0, 0, 0, 0};
     if (f.flag) {
@@ -265,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     // pass 2: compacted positions; the records of the rows this CTA folds
     const int li_last = static_cast<int>((u0 + nu - 1) / H);
     int base = 0;
-    for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+    for (int b0 = 0; b0 < a.batch; b0 += kFlushThreads) {
       const int b = b0 + tid;
       const RowFlag f = b < a.batch ? row_flag(a, b, false) : RowFlag{0, 0, 0, 0};
       int tot = 0;
@@ -399,6 +407,42 @@ __global__ void __launch_bounds__(kThreads, 2)
       // let copies already in flight land before the CTA can exit
       for (int i = max(0, issued - lay.ns); i < issued; ++i) mbar_wait(&full[i % lay.ns], (i / lay.ns) & 1);
     }
+  } else if (nu > 0 && warp == kWeightsWarp) {
+    // ---------------- weights warp ----------------
+    // Per unit, once the stage has landed: the canonical cumulative sums c_j
+    // (sequential fp32, the oracle's order) and the weights w_j = e^{c_end -
+    // c_j} dt'_j and e^{c_end}, into the stage for all consumer warps (one warp
+    // forms them instead of each of the eight).  The stage is not refilled
+    // before the consumers release it, and they read the weights first.
+    int st = 0;
+    uint32_t ph = 0;
+    for (int i = 0; i < nu; ++i) {
+      if (i > 0 && ++st == lay.ns) {
+        st = 0;
+        ph ^= 1u;
+      }
+      if (!mbar_wait(&full[st], ph)) {
+        if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
+        break;
+      }
+      uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
+      const int p = meta[st].p;
+      const float hA = reinterpret_cast<const float*>(sb + lay.sc_off)[0];
+      const float dtj = lane < p ? reinterpret_cast<const float*>(sb + lay.dt_off)[lane] : 0.0f;
+      const float aj = lane < p ? __fmul_rn(hA, dtj) : 0.0f;
+      float cj = 0.0f;
+#pragma unroll 4
+      for (int k = 0; k < p; ++k) {
+        const float ak = __shfl_sync(0xffffffffu, aj, k);
+        if (lane >= k) cj = __fadd_rn(cj, ak);
+      }
+      const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
+      float* wsm = reinterpret_cast<float*>(sb + lay.w_off);
+      wsm[lane] = lane < p ? __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj) : 0.0f;
+      if (lane == 0) wsm[32] = spec_exp(c_end);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&wready[st]);
+    }
   } else if (nu > 0) {
   // ---------------- consumer warps: rows 8*warp .. 8*warp+7, each on its own ----------------
   // lane: rows r0..r0+3, columns c0..c0+7
@@ -410,27 +454,20 @@ __global__ void __launch_bounds__(kThreads, 2)
       st = 0;
       ph ^= 1u;
     }
-    if (!mbar_wait(&full[st], ph)) {
+    // the stage's copies (observed directly: complete by the time the weights
+    // are) and its weights
+    if (!mbar_wait(&full[st], ph) || !mbar_wait(&wready[st], ph)) {
       if (lane == 0) set_error(c.err, RSSM_ERRBIT_TIMEOUT);
       break;
     }
     const uint8_t* sb = smem + lay.stages_off + st * lay.stage_bytes;
     const FoldMeta m = meta[st];
     const int p = m.p;
-    // canonical cumulative sums c_j (sequential fp32) and the weights
-    // w_j = e^{c_end - c_j} dt'_j (lane j holds w_j), decay = e^{c_end}
-    const float hA = reinterpret_cast<const float*>(sb + lay.sc_off)[0];
-    const float dtj = lane < p ? reinterpret_cast<const float*>(sb + lay.dt_off)[lane] : 0.0f;
-    const float aj = lane < p ? __fmul_rn(hA, dtj) : 0.0f;
-    float cj = 0.0f;
-#pragma unroll 4
-    for (int k = 0; k < p; ++k) {
-      const float ak = __shfl_sync(0xffffffffu, aj, k);
-      if (lane >= k) cj = __fadd_rn(cj, ak);
-    }
-    const float c_end = p > 0 ? __shfl_sync(0xffffffffu, cj, p - 1) : 0.0f;
-    const float wj = lane < p ? __fmul_rn(spec_exp(__fsub_rn(c_end, cj)), dtj) : 0.0f;
-    const float decay = spec_exp(c_end);
+    // the weights w_j = e^{c_end - c_j} dt'_j (lane j holds w_j) and
+    // decay = e^{c_end}, formed by the weights warp
+    const float* wsm = reinterpret_cast<const float*>(sb + lay.w_off);
+    const float wj = wsm[lane];
+    const float decay = wsm[32];
     if constexpr (k2B) {
       if (c.rounding == RSSM_ROUND_NEAREST && p >= kMmaMinP && !c.read_state) {
         // The fold on the tensor cores: S0' = e^{c_end} S0 + U Bm, U[d][j] =
@@ -783,7 +820,7 @@ static int launch_flush_t(const FlushArgs& a, int num_sms, cudaStream_t st) {
   CUtensorMap map;
   memset(&map, 0, sizeof(map));
   if (fold_2byte(DT) && !encode_state_map(a.c, &map, 1)) return cudaErrorInvalidValue;
-  e = launch_pdl(flush_kernel<DT>, dim3(grid), dim3(kThreads), lay.total, st, map, a, ns, maxrows);
+  e = launch_pdl(flush_kernel<DT>, dim3(grid), dim3(kFlushThreads), lay.total, st, map, a, ns, maxrows);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
