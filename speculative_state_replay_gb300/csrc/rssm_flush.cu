@@ -207,11 +207,11 @@ __device__ __forceinline__ void store_read_checkpoint(const Cache& c, float (&ac
 // Classification, fold, requantisation and bookkeeping of rssm_flush in one
 // kernel.  Every CTA classifies all rows (two passes over slot_idx, pnat and
 // the sequence bounds) and keeps the records of the flushed rows its range of
-// (flushed row, head) units covers; the producer and consumer warps then fold
-// those units.  The bookkeeping is written by the CTA that takes the last ticket
-// once it has classified (a self-resetting ticket), i.e. after every CTA has
-// read the values it replaces; nothing in the kernel reads them afterwards.
-// the flush's CTA: 8 consumer warps, the producer warp, the weights warp
+// (flushed row, head) units covers; then the producer warp fills the stages,
+// the weights warp forms each unit's fold weights and the 8 consumer warps
+// fold.  The bookkeeping is written by the CTA that takes the last ticket once
+// it has classified (a self-resetting ticket), i.e. after every CTA has read
+// the values it replaces; nothing in the kernel reads them afterwards.
 constexpr int kWeightsWarp = kConsumerWarps + 1;
 constexpr int kFlushThreads = kThreads + 32;
 
